@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of one EXL3 trellis MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: the GLM-5.3-Flash-shaped decode step (288 routed experts, top-8,
+hidden 4096, intermediate 2048, K=2 codes, 4 bf16 tokens, plus an fp16 shared
+expert), synthetic seeded data.  One JSON line on rank 0.
+
+ours:      the CUDA library through its C ABI; the step is captured once in a
+           CUDA graph and replayed; L2 is flushed (512 MiB write) before every
+           timed step; per-stage CUDA events inside the graph give the dominant
+           kernel's duration.  e2e: the same forward through the public API
+           with pinned-host inputs copied in and the output copied out inside
+           the timed region.
+reference: the CPU oracle as it stands, on this host, on a bounded sample
+           (one (token, expert) pair per step).
+Under torchrun (N > 1) every rank runs its own token batch (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "decode"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
+    """Time the CPU oracle on n_pairs (token, expert) pairs of token 0 and the
+    shared expert of token 0; returns (tokens/s, seconds used, sample text)."""
+    import numpy as np
+
+    import oracle
+    from trellis_quantized_moe_exl3_gb300 import synth
+    codes = codes if codes is not None else [synth.layer_codes(spec, p) for p in range(3)]
+    sides = [synth.side_vectors(spec, p) for p in range(3)]
+    ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
+                      [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
+                      shared_w=shared_w)
+    ids, w, _, _ = oracle.route(logits, wl.top_k)
+    t0 = time.perf_counter()
+    for j in range(n_pairs):
+        t, jj = divmod(j, wl.top_k)
+        ol.expert_pair(x[t % wl.T], wl.act == "bf16", int(ids[t % wl.T, jj]), float(w[t % wl.T, jj]))
+    t_pairs = (time.perf_counter() - t0) / n_pairs
+    t1 = time.perf_counter()
+    if shared_w is not None:
+        ol.shared_row(x[0], wl.act == "bf16")
+    t_shared = time.perf_counter() - t1
+    per_token = wl.top_k * t_pairs + t_shared
+    sample = (f"{n_pairs} (token, expert) pair(s) of the {wl.T}-token decode step + the shared "
+              f"expert of one token; tokens/s = 1 / ({wl.top_k} x pair time + shared time)")
+    return 1.0 / per_token, time.perf_counter() - t0, sample
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from trellis_quantized_moe_exl3_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    spec = wl.layers[0]
+    x, logits = synth.workload_inputs(wl)
+    codes = [synth.layer_codes(spec, p) for p in range(3)]
+    sides = [synth.side_vectors(spec, p) for p in range(3)]
+    sw = synth.shared_weights(spec)
+    ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
+                      [s[0] for s in sides], [s[1] for s in sides], shared_w=sw)
+    ids, w, _, _ = oracle.route(logits, wl.top_k)
+    pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
+    for s in range(args.warmup):
+        t, j = pairs[s % len(pairs)]
+        ol.expert_pair(x[t], True, int(ids[t, j]), float(w[t, j]))
+    ts = time.perf_counter()
+    ol.shared_row(x[0], True)
+    t_shared = time.perf_counter() - ts
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        t, j = pairs[(args.warmup + s) % len(pairs)]
+        ol.expert_pair(x[t], True, int(ids[t, j]), float(w[t, j]))
+    t_pair = (time.perf_counter() - t0) / args.steps
+    per_token = wl.top_k * t_pair + t_shared
+    value = 1.0 / per_token
+    sample = (f"one (token, expert) pair of the {wl.T}-token decode step per step; tokens/s = "
+              f"1 / ({wl.top_k} x mean pair time + shared-expert time of one token)")
+    line = {
+        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_token * 1e3 * wl.T, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    s = wl.layers[0]
+    return {"workload": (f"{wl.name}: {s.num_experts} experts top-{wl.top_k}, hidden {s.hidden}, "
+                         f"inter {s.inter}, K={list(s.K)}, T={wl.T} {wl.act}"
+                         + (", + fp16 shared expert" if s.shared else "")),
+            "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
+            "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round,
+            "l2": "flushed (512 MiB write) before every timed step"}
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args):
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from trellis_quantized_moe_exl3_gb300 import _lib, synth
+    from trellis_quantized_moe_exl3_gb300 import build as lib_build
+    from trellis_quantized_moe_exl3_gb300.api import Layer
+
+    world, rank, local = dist_env()
+    lib_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    spec = wl.layers[0]
+    codes = [synth.layer_codes(spec, p) for p in range(3)]
+    sides = [synth.side_vectors(spec, p) for p in range(3)]
+    sw = synth.shared_weights(spec)
+    # every rank runs its own token batch (weak scaling)
+    x_np = synth.activations(wl.seed + 1000 * rank, wl.T, spec.hidden, wl.act)
+    lg_np = synth.router_logits(spec.seed + 1000 * rank, wl.T, spec.num_experts, wl.routing)
+
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    d_codes = [t16(c) for c in codes]
+    d_suh = [t16(s[0]).view(torch.float16) for s in sides]
+    d_svh = [t16(s[1]).view(torch.float16) for s in sides]
+    d_sw = [t16(a).view(torch.float16) for a in sw]
+    layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw)
+    x = t16(x_np).view(torch.bfloat16)
+    lg = torch.from_numpy(lg_np).to(dev)
+    T, k = wl.T, wl.top_k
+    ws = layer.workspace(T, k, dev)
+    out = torch.empty_like(x)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    L = _lib.lib()
+
+    # stage events recorded inside the forward (and inside the graph)
+    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(_lib.EXL3_NUM_STAGE_EVENTS)]
+    with torch.cuda.stream(s):
+        for e in stage_ev:
+            e.record(s)
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * _lib.EXL3_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_ev])
+    _lib.check(L.exl3_layer_set_stage_events(layer.handle, arr, _lib.EXL3_NUM_STAGE_EVENTS),
+               "set_stage_events")
+
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+    torch.cuda.synchronize()
+
+    # active experts of this batch (for the algorithmic bytes)
+    from trellis_quantized_moe_exl3_gb300.api import route
+    r_ids, _, r_off, _ = route(lg, k)
+    counts = torch.diff(r_off).cpu().numpy()
+    n_active = int((counts > 0).sum())
+
+    use_graph = True
+    c0 = L.exl3_launch_count()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+    except Exception:
+        use_graph = False
+    launches_per_step = int(L.exl3_launch_count() - c0)
+
+    def step():
+        if use_graph:
+            g.replay()
+        else:
+            layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+
+    start_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    end_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize()
+
+    stage_ms = np.zeros(_lib.EXL3_NUM_STAGE_EVENTS - 1)
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    clocks = ClockSampler(gpu_index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    step_ms = []
+    with torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush.zero_()
+            start_ev[i].record(s)
+            step()
+            end_ev[i].record(s)
+            end_ev[i].synchronize()
+            step_ms.append(start_ev[i].elapsed_time(end_ev[i]))
+            for j in range(_lib.EXL3_NUM_STAGE_EVENTS - 1):
+                stage_ms[j] += stage_ev[j].elapsed_time(stage_ev[j + 1])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    stage_ms /= args.steps
+    tot = float(np.sum(step_ms))
+    if world > 1:
+        t = torch.tensor([tot], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot = float(t.item())
+    ms_per_step = tot / args.steps
+    value = world * T * args.steps / (tot / 1e3)
+
+    # e2e: public API with host buffers, copies inside the timed region
+    x_host = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).view(torch.bfloat16).pin_memory()
+    lg_host = torch.from_numpy(lg_np).pin_memory()
+    out_host = torch.empty((T, spec.hidden), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(lg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    L.exl3_layer_set_stage_events(layer.handle, None, 0)
+    e2e_ms = []
+    with torch.cuda.stream(s):
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0.record(s)
+            x_d.copy_(x_host, non_blocking=True)
+            lg_d.copy_(lg_host, non_blocking=True)
+            layer.forward(x_d, lg_d, k, out=out, ws=ws, stream=s)
+            out_host.copy_(out, non_blocking=True)
+            e1.record(s)
+            e1.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+    e2e_tot = float(np.sum(e2e_ms))
+    if world > 1:
+        t = torch.tensor([e2e_tot], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+    e2e_value = world * T * args.steps / (e2e_tot / 1e3)
+
+    # roofline of the dominant kernel (largest stage)
+    hbm, bf16_tf, src = peaks()
+    H, I = spec.hidden, spec.inter
+    code_b = [H * I * spec.K[p] // 8 for p in range(3)]
+    side_b = [(H + I) * 2] * 3
+    stage_names = _lib.STAGE_NAMES
+    stage_bytes = {
+        "gate_up": n_active * (code_b[0] + code_b[1] + side_b[0] + side_b[1]),
+        "down": n_active * (code_b[2] + side_b[2]),
+        "shared": 3 * H * I * 2,
+    }
+    dom = max(stage_bytes, key=lambda n: stage_ms[stage_names.index(n)])
+    dom_ms = float(stage_ms[stage_names.index(dom)])
+    achieved = stage_bytes[dom] / (dom_ms / 1e3) / 1e9
+    step_bytes = sum(stage_bytes.values())
+    line = {
+        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 (MMA operands; fp32 accumulate; bf16 activations in/out)",
+        "data": "synthetic (seeded PCG64): uniform uint16 codes, side vectors 1+0.1N(0,1), "
+                "N(0,1) activations and router logits",
+        "config": {**workload_config(wl), "cuda_graph": use_graph, "n_active_experts": n_active},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "algorithmic_bytes": stage_bytes[dom], "ms": dom_ms,
+                     "peak_source": f"{src} (hbm_gbs, burst)"},
+        "step_roofline": {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
+                          "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm,
+                          "what": "code + side-vector + shared-expert bytes of one step / step time"},
+        "stage_ms": {n: float(v) for n, v in zip(stage_names, stage_ms)},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2 + lg_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2),
+                "ms_per_step": e2e_tot / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        rate, secs, sample = oracle_pair_rate(wl, spec, x_np, lg_np, 3, shared_w=sw, codes=codes)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": sample, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

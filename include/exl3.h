@@ -1,0 +1,166 @@
+/*
+ * exl3.h -- C ABI of the GB300 (sm_103a) library for one routed-expert MoE
+ * layer whose expert weights are EXL3 K-bit trellis codes.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [p1] "GLM-5.3-Flash EXL3 (~2.1 bpw, SM70 tile order)"
+ *   [p2] "GLM-5.3 Flash EXL3 for 2x DGX Sparks"
+ *   [p3] "GLM-5.3-Flash EXL3 K2"
+ *   [p4] "GLM-5.3-Flash · exlr8 (K2/K3/K4)"
+ *
+ * Conventions for every entry point:
+ *   - Tensors are caller-owned memory; "device" pointers must be CUDA device
+ *     (or managed) memory of the current device, "host" pointers host memory.
+ *     The library never frees them.  A layer handle borrows the weight
+ *     pointers given to exl3_layer_create and must not outlive them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises the host
+ *     unless stated.  exl3_moe_route and exl3_moe_forward never allocate and
+ *     never read device data on the host, so they can be captured in a CUDA
+ *     graph (the pages capture decode steps in graphs: [p2] What runs, Graphs).
+ *   - Errors: argument, shape and width errors are returned before any launch
+ *     and leave outputs untouched.  A failed launch returns EXL3_ERR_CUDA.
+ *     Inconsistencies found on the device (bad expert id in a table, a wait
+ *     that timed out) set a status word in the workspace, read back with
+ *     exl3_get_device_status.
+ *   - Layouts are row-major and densely packed unless stated.
+ *
+ * Format v1 (the library's reading of the pages, which name the format but
+ * do not define its bits): codes of one projection of one expert are uint16 [in/16][out/16][16*K]
+ * ([p1] intro: packed int16 words holding 16/K weights; [p4] Loading: 16x16
+ * tiles, a 4096x128 half at width K is 65,536*K bytes); suh is fp16 [in],
+ * svh fp16 [out] ([p2] What runs: trellis + suh + svh + mcg).
+ */
+#ifndef EXL3_H
+#define EXL3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct exl3_layer exl3_layer_t; /* opaque, immutable after create */
+
+typedef enum {
+    EXL3_OK = 0,
+    EXL3_ERR_ARG = 1,       /* null pointer, bad enum, top_k out of range */
+    EXL3_ERR_SHAPE = 2,     /* dimensions not multiples of 128, T < 0, ... */
+    EXL3_ERR_K = 3,         /* code width not in {2, 3, 4} */
+    EXL3_ERR_WORKSPACE = 4, /* workspace null or smaller than required */
+    EXL3_ERR_CUDA = 5,      /* a CUDA call or launch failed */
+    EXL3_ERR_DEVICE = 6     /* no sm_100-family device / device status set */
+} exl3_status;
+
+typedef enum { EXL3_F16 = 0, EXL3_BF16 = 1 } exl3_dtype;
+
+/* Kernel path for the expert GEMMs.  AUTO picks the grouped GEMV for
+ * decode-sized steps (few tokens per expert) and the tcgen05 grouped GEMM
+ * for prefill-sized steps. */
+typedef enum { EXL3_PATH_AUTO = 0, EXL3_PATH_GEMV = 1, EXL3_PATH_GEMM = 2 } exl3_path;
+
+/* Projection index: 0 = gate, 1 = up, 2 = down. */
+typedef struct {
+    int num_experts;             /* E, 1..1024 */
+    int hidden;                  /* H, multiple of 128 */
+    int inter;                   /* I, multiple of 128 */
+    int K[3];                    /* code width per projection, 2..4 */
+    int fp8_round;               /* 1 = round codebook outputs to FP8 E4M3 before the side
+                                    vectors ([p4] intro, the exlr8 rule) */
+    uint32_t mcg_mult;           /* mcg multiplier (odd); 0 = 0x9E3779B1 */
+    const uint16_t *codes[3];    /* device, [E][in/16][out/16][16*K[p]] */
+    const uint16_t *suh[3];      /* device fp16 bits, [E][in] */
+    const uint16_t *svh[3];      /* device fp16 bits, [E][out] */
+    const uint16_t *shared_w[3]; /* device fp16 bits, dense [in][out], or all NULL: one
+                                    unquantized shared expert added with weight 1
+                                    ([p4] intro: one shared expert per MoE layer) */
+} exl3_layer_desc;
+
+/* Validate `desc` and build a handle (host allocation only).  Errors:
+ * EXL3_ERR_ARG (null pointers, shared_w partly NULL), EXL3_ERR_SHAPE,
+ * EXL3_ERR_K, EXL3_ERR_DEVICE (current device is not compute capability
+ * 10.x). */
+exl3_status exl3_layer_create(const exl3_layer_desc *desc, exl3_layer_t **out);
+void exl3_layer_destroy(exl3_layer_t *layer);
+
+/* Decode projection `proj` of `expert` to a dense fp16 matrix out[in][out]
+ * (device).  apply_side = 0: the codebook values (after the E4M3 rule when the
+ * layer has fp8_round); apply_side = 1: fp16(fp32(fp32(v*suh[i])*svh[o])).
+ * Bit-exact check path for the format ([p2] Cold prefill: the dense
+ * "LinearEXL3 reference").  Errors: EXL3_ERR_ARG for bad expert/proj/null. */
+exl3_status exl3_decode_dense(const exl3_layer_t *layer, int expert, int proj, int apply_side,
+                              uint16_t *out, void *stream);
+
+/* Bytes of workspace exl3_moe_route needs for T tokens, E experts, top_k. */
+size_t exl3_route_workspace_size(int T, int E, int top_k);
+
+/* Top-k routing and segment tables ([p4] intro: 288 experts, top-8; [p2] Cold
+ * prefill (E3): device-side segment tables, no host sync).
+ *   logits      device fp32 [T][E]
+ *   ids         device int32 [T][top_k]  experts by descending logit, ties to
+ *               the lower index, NaN as -inf
+ *   w           device fp32 [T][top_k]   softmax over the k selected logits
+ *   seg_offsets device int32 [E+1]       pairs with expert < e
+ *   seg_pairs   device int32 [T*top_k]   pair ids t*top_k+j, expert-major,
+ *               ascending inside an expert
+ *   ws          device, >= exl3_route_workspace_size bytes
+ * T = 0 is valid (offsets all zero).  1 <= top_k <= min(E, 16). */
+exl3_status exl3_moe_route(const float *logits, int T, int E, int top_k, int32_t *ids, float *w,
+                           int32_t *seg_offsets, int32_t *seg_pairs, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Bytes of workspace exl3_moe_forward needs for T tokens and top_k (all
+ * paths).  Deterministic in (layer shape, T, top_k). */
+size_t exl3_moe_workspace_size(const exl3_layer_t *layer, int T, int top_k);
+
+/* One MoE layer forward ([p2] Cold prefill (E3): gather, gate/up + SwiGLU,
+ * down + scatter; [p1] Running it: decodes the trellis inside the matmul):
+ *   x      device [T][H] in dtype dt (fp16 or bf16)
+ *   logits device fp32 [T][E]
+ *   out    device [T][H] in dtype dt; y_t = sum_j w_tj * expert_{id_tj}(x_t)
+ *          (+ shared(x_t)), summed over j in order, no atomics
+ *   ws     device workspace of >= exl3_moe_workspace_size(layer, T, top_k)
+ * out may not alias x. */
+exl3_status exl3_moe_forward(const exl3_layer_t *layer, const void *x, exl3_dtype dt,
+                             const float *logits, int T, int top_k, void *out, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/* As exl3_moe_forward, plus an optional residual (device [T][H] in dt, may
+ * be NULL; out = round(residual + y)) and an explicit kernel path. */
+exl3_status exl3_moe_forward_ex(const exl3_layer_t *layer, const void *x, exl3_dtype dt,
+                                const float *logits, int T, int top_k, const void *residual,
+                                void *out, int path, void *ws, size_t ws_bytes, void *stream);
+
+/* Unweighted RMSNorm of each row: out = round(x / sqrt(mean(x^2) + eps)),
+ * fp32 arithmetic, x and out device [T][H] in dt (out may alias x).  Used
+ * between layers of a stacked prefill. */
+exl3_status exl3_rmsnorm(const void *x, exl3_dtype dt, int T, int H, float eps, void *out,
+                         void *stream);
+
+/* Synchronise `stream` and read the device status word of a forward/route
+ * workspace (0 = fine). */
+exl3_status exl3_get_device_status(const void *ws, void *stream, int32_t *status);
+
+/* Stage-boundary profiling.  When set, every forward on this layer records
+ * events[i] (cudaEvent_t, created by the caller) on its stream at these
+ * boundaries: 0 start, 1 routing done, 2 gather done, 3 gate/up done,
+ * 4 down input prepared, 5 down done, 6 shared expert done, 7 combine done.
+ * n_events must be EXL3_NUM_STAGE_EVENTS; events = NULL clears the hook.
+ * For measurement only: not safe while another thread runs a forward on the
+ * same layer. */
+#define EXL3_NUM_STAGE_EVENTS 8
+exl3_status exl3_layer_set_stage_events(exl3_layer_t *layer, void *const *events, int n_events);
+
+/* Number of kernels this library has launched in the process so far (a
+ * host-side counter; launches captured into a CUDA graph count once, at
+ * capture). */
+uint64_t exl3_launch_count(void);
+
+const char *exl3_status_string(exl3_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_H */

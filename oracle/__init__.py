@@ -93,6 +93,11 @@ def lib():
                                              u16p, ctypes.c_int, ctypes.c_int, u16p,
                                              ctypes.c_int, u16p]
             L.oracle_moe_forward.restype = ctypes.c_int
+            L.oracle_expert_pair.argtypes = [ctypes.POINTER(OracleLayer), u16p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_float, u16p]
+            L.oracle_expert_pair.restype = ctypes.c_int
+            L.oracle_shared_row.argtypes = [ctypes.POINTER(OracleLayer), u16p, ctypes.c_int, u16p]
+            L.oracle_shared_row.restype = None
             L.oracle_rmsnorm_row.argtypes = [u16p, ctypes.c_int, ctypes.c_double, u16p]
             L.oracle_rmsnorm_row.restype = None
             _lib = L
@@ -236,6 +241,23 @@ class Layer:
                                       _ptr(logits), T, top_k, _ptr(tokens), tokens.size, _ptr(y))
         if rc != 0:
             raise MemoryError("oracle_moe_forward failed to allocate")
+        return y
+
+
+    def expert_pair(self, x_row_bits: np.ndarray, x_is_bf16: bool, expert: int,
+                    weight: float) -> np.ndarray:
+        """weight * expert(x_row) in fp64 (one (token, expert) pair)."""
+        x_row_bits = np.ascontiguousarray(x_row_bits, dtype=np.uint16)
+        r = np.zeros(self.hidden, np.float64)
+        if lib().oracle_expert_pair(ctypes.byref(self.st), _ptr(x_row_bits), int(bool(x_is_bf16)),
+                                    int(expert), float(weight), _ptr(r)) != 0:
+            raise MemoryError("oracle_expert_pair failed to allocate")
+        return r
+
+    def shared_row(self, x_row_bits: np.ndarray, x_is_bf16: bool) -> np.ndarray:
+        x_row_bits = np.ascontiguousarray(x_row_bits, dtype=np.uint16)
+        y = np.zeros(self.hidden, np.float64)
+        lib().oracle_shared_row(ctypes.byref(self.st), _ptr(x_row_bits), int(bool(x_is_bf16)), _ptr(y))
         return y
 
 

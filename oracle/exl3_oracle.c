@@ -500,6 +500,43 @@ int oracle_moe_forward(const oracle_layer *L, const uint16_t *x, int x_is_bf16,
     return 0;
 }
 
+/* One (token, expert) pair: decode the expert and compute w * expert(x) for
+ * one activation row (fp64).  The unit of the CPU baseline's bounded sample. */
+int oracle_expert_pair(const oracle_layer *L, const uint16_t *x_row, int x_is_bf16, int e,
+                       float wgt, double *r)
+{
+    int H = L->hidden, I = L->inter;
+    double *xr = (double *)malloc((size_t)H * sizeof(double));
+    double *Vg = (double *)malloc((size_t)H * I * sizeof(double));
+    double *Vu = (double *)malloc((size_t)H * I * sizeof(double));
+    double *Vd = (double *)malloc((size_t)I * H * sizeof(double));
+    if (!xr || !Vg || !Vu || !Vd)
+        return 1;
+    for (int i = 0; i < H; i++)
+        xr[i] = x_is_bf16 ? oracle_bf16_to_double(x_row[i]) : oracle_f16_to_double(x_row[i]);
+    decode_proj_double(L, 0, e, Vg);
+    decode_proj_double(L, 1, e, Vu);
+    decode_proj_double(L, 2, e, Vd);
+    expert_row(L, e, Vg, Vu, Vd, xr, (double)wgt, r);
+    free(xr);
+    free(Vg);
+    free(Vu);
+    free(Vd);
+    return 0;
+}
+
+/* Shared expert of one activation row (fp64), added into y. */
+void oracle_shared_row(const oracle_layer *L, const uint16_t *x_row, int x_is_bf16, double *y)
+{
+    int H = L->hidden;
+    double *xr = (double *)malloc((size_t)H * sizeof(double));
+    for (int i = 0; i < H; i++)
+        xr[i] = x_is_bf16 ? oracle_bf16_to_double(x_row[i]) : oracle_f16_to_double(x_row[i]);
+    if (L->shared_w[0])
+        shared_row(L, xr, y);
+    free(xr);
+}
+
 /* Unweighted RMSNorm of one row (fp64), eps added to the mean square.
  * reading: the long-prefill workload chains layers with a residual add; the
  * pages give no norm, and without one the synthetic magnitudes overflow, so

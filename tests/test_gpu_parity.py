@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Decode and routing must match bit for bit; layer
+outputs must meet max|gpu-oracle|/max|oracle| <= 2e-2 and relative Frobenius
+error <= 5e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import HostLayer, act_to_f64, assert_layer_close, oracle_forward_parallel
+from trellis_quantized_moe_exl3_gb300 import synth
+from trellis_quantized_moe_exl3_gb300.api import device_status, rmsnorm, route
+
+pytestmark = pytest.mark.gpu
+
+
+def _u16(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _act(bits, act):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    return t.view(torch.bfloat16 if act == "bf16" else torch.float16)
+
+
+# ------------------------------------------------------------------ decode
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_dense_every_state(fp8):
+    """65,536 tiles whose first word is the tile index: weight 0 of tile n has
+    state n, so every trellis state is decoded; the whole 4096x4096 matrix
+    must equal the oracle's bit for bit."""
+    K = 2
+    rng = np.random.default_rng(20)
+    codes = rng.integers(0, 65536, size=(1, 256, 256, 16 * K), dtype=np.uint16)
+    codes[0, :, :, 0] = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    spec = synth.LayerSpec(seed=0, num_experts=1, hidden=4096, inter=4096, K=(K, K, K),
+                           fp8_round=fp8)
+    hl = HostLayer(spec, codes=[codes, codes, codes])
+    layer = hl.device()
+    got = _u16(layer.decode_dense(0, 0))
+    ref = oracle.decode_dense(codes[0], 4096, 4096, K, fp8_round=fp8)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("K,fp8", [(3, False), (4, False), (3, True), (4, True), (2, True)])
+def test_decode_dense_widths_and_side(K, fp8):
+    spec = synth.LayerSpec(seed=30 + K, num_experts=3, hidden=256, inter=384, K=(K, K, K),
+                           fp8_round=fp8)
+    hl = HostLayer(spec)
+    layer = hl.device(mult=0x2545F491)
+    for e in range(3):
+        for p in range(3):
+            fin, fout = spec.dims(p)
+            for side in (False, True):
+                got = _u16(layer.decode_dense(e, p, apply_side=side))
+                ref = oracle.decode_dense(hl.codes[p][e], fin, fout, K, mult=0x2545F491,
+                                          fp8_round=fp8, suh=hl.suh[p][e] if side else None,
+                                          svh=hl.svh[p][e] if side else None)
+                assert np.array_equal(got, ref), (e, p, side)
+
+
+def test_decode_dense_full_size_experts():
+    wl = synth.WORKLOADS["prefill"]
+    spec = wl.layers[0]
+    codes = [np.stack([synth.expert_codes(spec, p, e) for e in (0, 287)]) for p in range(3)]
+    small = synth.LayerSpec(seed=spec.seed, num_experts=2, K=spec.K, fp8_round=True)
+    hl = HostLayer(small, codes=codes)
+    layer = hl.device()
+    for e in range(2):
+        for p in range(3):
+            fin, fout = small.dims(p)
+            got = _u16(layer.decode_dense(e, p))
+            ref = oracle.decode_dense(codes[p][e], fin, fout, spec.K[p], fp8_round=True)
+            assert np.array_equal(got, ref), (e, p)
+
+
+# ------------------------------------------------------------------ routing
+
+
+def _route_cases():
+    rng = np.random.default_rng(40)
+    cases = []
+    for name in ("tiny", "decode", "verify3", "prefill"):
+        wl = synth.WORKLOADS[name]
+        s = wl.layers[0]
+        cases.append((name, synth.router_logits(s.seed, wl.T, s.num_experts, wl.routing), wl.top_k))
+    wl = synth.WORKLOADS["long"]
+    cases.append(("long", synth.router_logits(wl.layers[0].seed, wl.T, 288, "zipf"), 8))
+    odd = rng.standard_normal((300, 40)).astype(np.float32)   # E not a multiple of 32, 3 chunks
+    odd[1, 5] = odd[1, 30] = 50.0                               # tie
+    odd[2, :] = 1.0                                             # all tied
+    odd[3, 7] = np.nan
+    odd[4, :] = -np.inf
+    odd[5, :] = np.nan
+    odd[6, :3] = np.inf
+    cases.append(("odd", odd, 5))
+    cases.append(("k1", rng.standard_normal((129, 288)).astype(np.float32), 1))
+    cases.append(("k16", rng.standard_normal((77, 64)).astype(np.float32), 16))
+    cases.append(("T1", rng.standard_normal((1, 288)).astype(np.float32), 8))
+    cases.append(("E8k8", rng.standard_normal((33, 8)).astype(np.float32), 8))
+    return cases
+
+
+@pytest.mark.parametrize("case", _route_cases(), ids=lambda c: c[0])
+def test_route_bit_exact(case):
+    _, logits, k = case
+    ids, w, off, pairs = route(torch.from_numpy(logits).cuda(), k)
+    r_ids, r_w, r_off, r_pairs = oracle.route(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    assert np.array_equal(w.cpu().numpy().view(np.int32), r_w.view(np.int32))
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    assert np.array_equal(pairs.cpu().numpy(), r_pairs)
+
+
+def test_route_empty():
+    ids, w, off, pairs = route(torch.zeros((0, 288), dtype=torch.float32, device="cuda"), 8)
+    assert (off.cpu().numpy() == 0).all()
+
+
+# ------------------------------------------------------------------ layer
+
+
+def _run_small(spec, T, top_k, act, path=0, residual=False, seed=50):
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x = synth.activations(seed, T, spec.hidden, act)
+    logits = synth.router_logits(seed, T, spec.num_experts, "normal")
+    xt = _act(x, act)
+    res = _act(synth.activations(seed + 1, T, spec.hidden, act), act) if residual else None
+    out = layer.forward(xt, torch.from_numpy(logits).cuda(), top_k, residual=res, path=path)
+    torch.cuda.synchronize()
+    ref = hl.oracle().forward(x, act == "bf16", logits, top_k)
+    if residual:
+        ref = ref + act_to_f64(res)
+    return act_to_f64(out), ref, layer
+
+
+def test_forward_tiny_workload():
+    wl = synth.WORKLOADS["tiny"]
+    spec = wl.layers[0]
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x, logits = synth.workload_inputs(wl)
+    out = layer.forward(_act(x, wl.act), torch.from_numpy(logits).cuda(), wl.top_k)
+    torch.cuda.synchronize()
+    ref = hl.oracle().forward(x, False, logits, wl.top_k)
+    assert_layer_close(act_to_f64(out), ref)
+    assert device_status(layer.workspace(wl.T, wl.top_k)) == 0
+
+
+@pytest.mark.parametrize("K,fp8,shared,T,k,act", [
+    ((2, 2, 3), False, False, 37, 4, "bf16"),
+    ((3, 3, 4), False, True, 9, 3, "f16"),
+    ((4, 4, 2), True, False, 20, 6, "bf16"),
+    ((2, 2, 2), True, True, 1, 1, "bf16"),
+    ((4, 4, 4), False, False, 64, 8, "bf16"),   # several token groups per expert
+])
+def test_forward_small_variants(K, fp8, shared, T, k, act):
+    spec = synth.LayerSpec(seed=60 + sum(K), num_experts=10, hidden=384, inter=256, K=K,
+                           fp8_round=fp8, shared=shared)
+    out, ref, _ = _run_small(spec, T, k, act)
+    assert_layer_close(out, ref)
+
+
+def test_forward_residual():
+    spec = synth.LayerSpec(seed=70, num_experts=6, hidden=256, inter=128, K=(3, 3, 3))
+    out, ref, _ = _run_small(spec, 12, 2, "bf16", residual=True)
+    assert_layer_close(out, ref)
+
+
+def test_forward_zero_tokens():
+    spec = synth.LayerSpec(seed=71, num_experts=4, hidden=128, inter=128, K=(2, 2, 2))
+    layer = HostLayer(spec).device()
+    x = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
+    out = layer.forward(x, torch.zeros((0, 4), dtype=torch.float32, device="cuda"), 2)
+    assert out.shape == (0, 128)
+
+
+def test_rmsnorm_vs_oracle():
+    x = synth.activations(80, 33, 512, "bf16")
+    xt = _act(x, "bf16") * 7
+    got = act_to_f64(rmsnorm(xt))
+    xf = act_to_f64(xt)
+    ref = np.stack([oracle.rmsnorm_row(r, 1e-6) for r in xf])
+    assert np.abs(got - ref).max() <= 2 ** -7 * np.abs(ref).max()
+
+
+def test_graph_capture_replays_same_output():
+    spec = synth.LayerSpec(seed=72, num_experts=8, hidden=256, inter=128, K=(2, 2, 2), shared=True)
+    hl = HostLayer(spec)
+    layer = hl.device()
+    T, k = 4, 2
+    x = _act(synth.activations(72, T, 256, "bf16"), "bf16")
+    lg = torch.from_numpy(synth.router_logits(72, T, 8, "normal")).cuda()
+    ws = layer.workspace(T, k)
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+    torch.cuda.synchronize()
+    first = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
+
+
+# ------------------------------------------------------------------ workloads
+
+
+def _workload_parity(name, tokens_fn, path=0):
+    wl = synth.WORKLOADS[name]
+    spec = wl.layers[0]
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x, logits = synth.workload_inputs(wl)
+    out = layer.forward(_act(x, wl.act), torch.from_numpy(logits).cuda(), wl.top_k, path=path)
+    torch.cuda.synchronize()
+    assert device_status(layer.workspace(wl.T, wl.top_k)) == 0
+    toks = tokens_fn(wl, logits)
+    ref = oracle_forward_parallel(hl.oracle(), x, wl.act == "bf16", logits, wl.top_k, toks)
+    got = act_to_f64(out)[toks]
+    return assert_layer_close(got, ref)
+
+
+def test_decode_workload_all_tokens():
+    _workload_parity("decode", lambda wl, lg: list(range(wl.T)))
+
+
+@pytest.mark.parametrize("name", ["verify3", "verify4"])
+def test_verify_workloads_sampled(name):
+    _workload_parity(name, lambda wl, lg: [0, 9, 22, 31])
+
+
+def _prefill_tokens(wl, logits):
+    ids, _, off, pairs = oracle.route(logits, wl.top_k)
+    cnt = np.diff(off)
+    e_small = int(np.argmin(np.where(cnt > 0, cnt, 1 << 30)))
+    t_small = int(pairs[off[e_small]]) // wl.top_k
+    e_big = int(np.argmax(cnt))
+    t_big = int(pairs[off[e_big + 1] - 1]) // wl.top_k
+    return sorted({0, wl.T - 1, t_small, t_big})
+
+
+def test_prefill_workload_sampled():
+    _workload_parity("prefill", _prefill_tokens)
+
+
+def test_long_workload_sampled():
+    """Four stacked layers (K2, K3, K2, K4) with pre-RMSNorm and residual."""
+    wl = synth.WORKLOADS["long"]
+    x0 = synth.activations(wl.seed, wl.T, 4096, "bf16")
+    toks = [0, 5000, wl.T - 1]
+    xt = _act(x0, "bf16")
+    x_ref = x0[toks]
+    for li, spec in enumerate(wl.layers):
+        hl = HostLayer(spec)
+        layer = hl.device()
+        logits = synth.router_logits(spec.seed, wl.T, spec.num_experts, wl.routing)
+        xn = rmsnorm(xt)
+        nxt = layer.forward(xn, torch.from_numpy(logits).cuda(), wl.top_k, residual=xt)
+        torch.cuda.synchronize()
+        # oracle: the same chain per sampled token
+        xr = oracle.bf16_bits_to_f64(x_ref)
+        xn_bits = np.stack([oracle.f64_to_bf16_bits(oracle.rmsnorm_row(r, 1e-6)) for r in xr])
+        y = oracle_forward_parallel(hl.oracle(), xn_bits, True, logits[toks], wl.top_k,
+                                    range(len(toks)))
+        x_ref = np.stack([oracle.f64_to_bf16_bits(r) for r in xr + y])
+        xt = nxt
+        del layer, hl
+        torch.cuda.empty_cache()
+    got = act_to_f64(xt)[toks]
+    ref = oracle.bf16_bits_to_f64(x_ref)
+    assert_layer_close(got, ref)

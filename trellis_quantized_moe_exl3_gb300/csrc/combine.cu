@@ -1,0 +1,111 @@
+// Combine: y_t = sum_{j=0..k-1} r_{t,j} (fixed order) + shared(x_t)
+// (+ residual), rounded once to the output dtype.  Atomic-free: the down
+// projection wrote every pair row to its own slot (t, j).  Page "GLM-5.3
+// Flash EXL3 for 2x DGX Sparks", section Cold prefill (E3): down + scatter.
+// Also the RMSNorm used between stacked layers of a long prefill.
+#include "common.cuh"
+#include "internal.h"
+
+namespace exl3 {
+
+namespace {
+
+__device__ __forceinline__ void store_act4(void* out, int bf16, size_t idx, float4 v) {
+  if (bf16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) = u;
+  } else {
+    __half2 a = __floats2half2_rn(v.x, v.y);
+    __half2 b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) = u;
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ r, int T, int k,
+                                                      int H, const float* __restrict__ sp, int ns,
+                                                      const void* __restrict__ resid,
+                                                      void* __restrict__ out, int bf16) {
+  const size_t n4 = (size_t)T * H / 4;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n4;
+       v += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = v / (H / 4), o = (v % (H / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; j++) {
+      const float4 q = *reinterpret_cast<const float4*>(r + (t * k + j) * H + o);
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
+    if (sp) {
+      float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < ns; s++) {
+        const float4 q = *reinterpret_cast<const float4*>(sp + ((size_t)s * T + t) * H + o);
+        s4.x += q.x; s4.y += q.y; s4.z += q.z; s4.w += q.w;
+      }
+      acc.x += s4.x; acc.y += s4.y; acc.z += s4.z; acc.w += s4.w;
+    }
+    if (resid) {
+      acc.x += load_act(resid, bf16, t * H + o + 0);
+      acc.y += load_act(resid, bf16, t * H + o + 1);
+      acc.z += load_act(resid, bf16, t * H + o + 2);
+      acc.w += load_act(resid, bf16, t * H + o + 3);
+    }
+    store_act4(out, bf16, t * H + o, acc);
+  }
+}
+
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const void* __restrict__ x, int bf16, int H,
+                                                      float eps, void* __restrict__ out) {
+  __shared__ float s_w[32];
+  const size_t t = blockIdx.x;
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = load_act(x, bf16, t * H + i);
+    ss = fmaf(v, v, ss);
+  }
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += s_w[w];
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+  __syncthreads();  // all reads of x done before any in-place write
+  for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
+    float4 v;
+    v.x = load_act(x, bf16, t * H + i) * inv;
+    v.y = load_act(x, bf16, t * H + i + 1) * inv;
+    v.z = load_act(x, bf16, t * H + i + 2) * inv;
+    v.w = load_act(x, bf16, t * H + i + 3) * inv;
+    store_act4(out, bf16, t * H + i, v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* r, int T, int top_k, int H, const float* shared_part,
+                           int shared_splits, const void* residual, void* out, int out_bf16,
+                           cudaStream_t st) {
+  const size_t n4 = (size_t)T * H / 4;
+  int blocks = (int)((n4 + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  combine_kernel<<<blocks, 256, 0, st>>>(r, T, top_k, H, shared_part, shared_splits, residual, out,
+                                         out_bf16);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void* x, int bf16, int T, int H, float eps, void* out,
+                           cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  rmsnorm_kernel<<<T, 256, 0, st>>>(x, bf16, H, eps, out);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace exl3

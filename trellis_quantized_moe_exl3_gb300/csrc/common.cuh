@@ -1,0 +1,167 @@
+// Device helpers shared by the kernels of the EXL3 MoE library (sm_103a).
+//
+// Format v1 (the library's reading of the pages; "GLM-5.3-Flash EXL3 (~2.1
+// bpw, SM70 tile order)" intro, "GLM-5.3-Flash · exlr8 (K2/K3/K4)" intro,
+// Loading and Calibration):
+//   * one 16x16 tile = 16*K little-endian uint16 words = a circular bit string
+//     of 256*K bits, least significant bit of word 0 first;
+//   * weight t's 16-bit state is the window of 16 bits starting at bit t*K;
+//   * mcg codebook: x = state * mult (mod 2^32), m = (x & 0x8FFF8FFF) ^
+//     0x3B603B60, whose 16-bit halves are two fp16 numbers a (low) and b (high);
+//     the weight is fp16(a + b), optionally rounded to FP8 E4M3 (nearest even,
+//     saturating) before the side vectors;
+//   * tile order gb300_v1: weight t = 64c + 8r0 + 4hf + j sits at output row
+//     r0 + 8(j&1) and input column c + 4(j>>1) + 8hf.
+// Lane c (0..3) of an MMA quad owns bits [64cK, 64(c+1)K) of a tile, i.e. the
+// 8K bytes at byte offset 8Kc, plus the first 16-K bits of lane c+1 (mod 4).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace exl3 {
+
+constexpr uint32_t kMcgMask = 0x8FFF8FFFu;
+constexpr uint32_t kMcgXor = 0x3B603B60u;
+
+// ---------------------------------------------------------------- routing exp
+// exp for the routing softmax, defined for bit-exact agreement with any other
+// implementation of the same rule: inputs below -86 (and -inf, NaN) give 0;
+// n = rint(x*log2(e)); Cody-Waite reduction with the Cephes two-part ln2
+// (0.693359375, -2.12194440e-4) by fma; degree-7 Taylor polynomial with fp32
+// coefficients 1/n! in Horner form by fma; exact scaling by 2^n (n >= -124).
+__device__ __forceinline__ float exp_route(float x) {
+  if (!(x >= -86.0f)) return 0.0f;
+  const float t = __fmul_rn(x, 0x1.715476p+0f);
+  const float n = rintf(t);
+  float r = __fmaf_rn(-n, 0x1.63p-1f, x);
+  r = __fmaf_rn(-n, -0x1.bd0106p-13f, r);
+  float p = 0x1.a01a02p-13f;            // 1/5040
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/720
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/120
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/24
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/6
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int ni = (int)n;
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+// ---------------------------------------------------------------- trellis
+// Number of 32-bit words a quad lane owns (8K bytes) plus one word of its
+// right neighbour for the window overlap.
+template <int K>
+struct LaneWords {
+  static constexpr int kOwn = 2 * K;
+  uint32_t w[2 * K + 1];
+};
+
+// State of lane-local weight u (0..63): bits [uK, uK+16) of the lane stream.
+// u is a compile-time constant after unrolling, so this is one funnel shift
+// (or plain shift) and one mask.
+template <int K>
+__device__ __forceinline__ uint32_t lane_state(const LaneWords<K>& lw, int u) {
+  const int o = u * K;
+  const int wi = o >> 5;
+  const int sh = o & 31;
+  uint32_t v;
+  if (sh == 0)
+    v = lw.w[wi];
+  else if (sh <= 16)
+    v = lw.w[wi] >> sh;
+  else
+    v = __funnelshift_r(lw.w[wi], lw.w[wi + 1], sh);
+  return v & 0xFFFFu;
+}
+
+// mcg codebook before the final add: the two fp16 halves {a (low), b (high)}.
+__device__ __forceinline__ uint32_t mcg_halves(uint32_t s, uint32_t mult) {
+  return ((s * mult) & kMcgMask) ^ kMcgXor;
+}
+
+// fp16 RNE of a + b for two weights at once: {a0,b0},{a1,b1} -> {v0,v1}.
+__device__ __forceinline__ uint32_t sum_halves2(uint32_t m0, uint32_t m1) {
+  const uint32_t lo = __byte_perm(m0, m1, 0x5410);  // {a0, a1}
+  const uint32_t hi = __byte_perm(m0, m1, 0x7632);  // {b0, b1}
+  __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&lo),
+                      *reinterpret_cast<const __half2*>(&hi));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// E4M3 rule on two fp16 values: round to FP8 E4M3 (RNE, satfinite) and back;
+// every E4M3 value is exact in fp16.
+__device__ __forceinline__ uint32_t e4m3_round2(uint32_t v2) {
+  uint16_t f8;
+  uint32_t back;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(f8) : "r"(v2));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(f8));
+  return back;
+}
+
+// Load a quad lane's 8K bytes from global memory (read once: no L1 allocate)
+// and fetch the neighbour's first word with a shuffle inside the quad.
+template <int K>
+__device__ __forceinline__ void load_lane_words(LaneWords<K>& lw, const uint16_t* tile_lane) {
+  if constexpr (K == 2) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(tile_lane));
+    lw.w[0] = v.x; lw.w[1] = v.y; lw.w[2] = v.z; lw.w[3] = v.w;
+  } else if constexpr (K == 3) {
+#pragma unroll
+    for (int q = 0; q < 3; q++) {
+      uint2 v;
+      asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                   : "=r"(v.x), "=r"(v.y) : "l"(tile_lane + 4 * q));
+      lw.w[2 * q] = v.x; lw.w[2 * q + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      uint4 v;
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(tile_lane + 8 * q));
+      lw.w[4 * q] = v.x; lw.w[4 * q + 1] = v.y; lw.w[4 * q + 2] = v.z; lw.w[4 * q + 3] = v.w;
+    }
+  }
+}
+
+// Neighbour word: lane c of a quad takes lane (c+1) mod 4's first word.
+template <int K>
+__device__ __forceinline__ void fetch_neighbour(LaneWords<K>& lw) {
+  const int lane = threadIdx.x & 31;
+  lw.w[2 * K] = __shfl_sync(0xffffffffu, lw.w[0], (lane & ~3) | ((lane + 1) & 3));
+}
+
+// ---------------------------------------------------------------- MMA
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulate (legacy warp MMA).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- misc
+__device__ __forceinline__ float load_act(const void* x, int is_bf16, size_t idx) {
+  const uint16_t b = reinterpret_cast<const uint16_t*>(x)[idx];
+  if (is_bf16) return __uint_as_float((uint32_t)b << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+// Power-of-two exponent that maps amax into [2^14, 2^15), for fp16 operands.
+__device__ __forceinline__ int fp16_scale_exp(float amax) {
+  if (!(amax > 0.0f) || !isfinite(amax)) return 0;
+  int e = ilogbf(amax);
+  int s = 14 - e;
+  return s < -100 ? -100 : (s > 100 ? 100 : s);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace exl3

@@ -1,0 +1,89 @@
+// Internal launch interface between the C ABI (layer.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/exl3.h"
+
+namespace exl3 {
+
+// Host-side count of kernel launches (exl3_launch_count).
+void note_launches(int n);
+
+constexpr uint32_t kDefaultMcgMult = 0x9E3779B1u;
+constexpr int kRouteChunk = 128;   // tokens per routing CTA
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+
+// Device status bits (workspace status word).
+enum : int32_t {
+  kStatusBadExpert = 1,   // an expert id outside [0, E) reached a kernel
+  kStatusBadSegment = 2,  // a segment table entry out of range
+  kStatusTimeout = 4,     // a bounded wait gave up
+};
+
+struct RouteBuffers {
+  int32_t* ids;          // [P]
+  float* w;              // [P]
+  int32_t* seg_offsets;  // [E+1]
+  int32_t* seg_pairs;    // [P]
+  int32_t* pair_pos;     // [P]  position of pair p in seg_pairs
+  int32_t* active;       // [E+1]: active[0] = count, active[1..] = experts with pairs
+  int32_t* chunk_counts; // [nchunks][E]
+  int32_t* rank;         // [P]
+  int32_t* status;       // [1]
+};
+
+size_t route_scratch_bytes(int T, int E, int top_k);
+// Carves RouteBuffers out of `ws` (ids/w/seg may be caller-provided: non-null
+// fields of `given` are kept).
+void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb);
+cudaError_t launch_route(const float* logits, int T, int E, int top_k, const RouteBuffers& rb,
+                         cudaStream_t st);
+
+struct LayerView {
+  int E, H, I;
+  int K[3];
+  int fp8;
+  uint32_t mult;
+  const uint16_t* codes[3];
+  const uint16_t* suh[3];
+  const uint16_t* svh[3];
+  const uint16_t* shared_w[3];
+  size_t code_stride[3];  // uint16 words per expert
+};
+
+cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int apply_side,
+                                uint16_t* out, cudaStream_t st);
+
+// ---- grouped GEMV path (decode-sized steps)
+struct GemvBuffers {
+  uint32_t* xs_gu;   // [P][2][H] fp16x2 (dup), permuted per 16-block
+  float* xs_gu_inv;  // [P][2]
+  float* h;          // [P][I] fp32 (pair-sorted rows)
+  uint32_t* xs_d;    // [P][I] fp16x2 (dup), permuted
+  float* xs_d_inv;   // [P]
+  float* r;          // [P][H] fp32 rows by pair id
+};
+size_t gemv_scratch_bytes(int T, int top_k, int H, int I);
+void gemv_carve(void* ws, int T, int top_k, int H, int I, GemvBuffers* gb);
+// ev (may be null): events recorded after gather [2], gate/up [3], down prep [4], down [5].
+cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
+                            const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,
+                            cudaStream_t st);
+
+// ---- shared expert (dense fp16)
+constexpr int kSharedKPer = 128;  // rows of W per split
+size_t shared_scratch_bytes(int T, int H, int I);
+cudaError_t launch_shared(const LayerView& L, const void* x, int x_bf16, int T, float* part_gu,
+                          float* part_d, cudaStream_t st);
+
+// ---- combine / norm
+cudaError_t launch_combine(const float* r, int T, int top_k, int H, const float* shared_part,
+                           int shared_splits, const void* residual, void* out, int out_bf16,
+                           cudaStream_t st);
+cudaError_t launch_rmsnorm(const void* x, int bf16, int T, int H, float eps, void* out,
+                           cudaStream_t st);
+
+}  // namespace exl3

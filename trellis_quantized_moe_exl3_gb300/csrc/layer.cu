@@ -1,0 +1,255 @@
+// C ABI of the EXL3 MoE library: argument validation, workspace layout and
+// the launch sequence of one layer forward.  See include/exl3.h for the
+// contract of each entry point.
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "internal.h"
+
+using namespace exl3;
+
+struct exl3_layer {
+  LayerView v;
+  int has_shared;
+  cudaEvent_t ev[EXL3_NUM_STAGE_EVENTS];
+  int has_ev;
+};
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void exl3::note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+exl3_status check_device() {
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXL3_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return EXL3_ERR_DEVICE;
+  return major == 10 ? EXL3_OK : EXL3_ERR_DEVICE;
+}
+
+// Forward workspace: [route scratch][ids][w][seg_offsets][seg_pairs][gemv][shared]
+struct FwdLayout {
+  size_t route, ids, w, off, pairs, gemv, shared, total;
+};
+
+FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
+  FwdLayout f{};
+  const size_t P = (size_t)T * k;
+  size_t o = 0;
+  f.route = o; o += al(route_scratch_bytes(T, L.E, k));
+  f.ids = o; o += al(P * 4);
+  f.w = o; o += al(P * 4);
+  f.off = o; o += al((size_t)(L.E + 1) * 4);
+  f.pairs = o; o += al(P * 4);
+  f.gemv = o; o += al(gemv_scratch_bytes(T, k, L.H, L.I));
+  f.shared = o; o += has_shared ? al(shared_scratch_bytes(T, L.H, L.I)) : 0;
+  f.total = o;
+  return f;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* exl3_status_string(exl3_status s) {
+  switch (s) {
+    case EXL3_OK: return "ok";
+    case EXL3_ERR_ARG: return "invalid argument";
+    case EXL3_ERR_SHAPE: return "invalid shape";
+    case EXL3_ERR_K: return "code width must be 2, 3 or 4 (gate and up equal)";
+    case EXL3_ERR_WORKSPACE: return "workspace missing or too small";
+    case EXL3_ERR_CUDA: return "CUDA error";
+    case EXL3_ERR_DEVICE: return "unsupported device or device status set";
+  }
+  return "unknown status";
+}
+
+exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
+  if (!d || !out) return EXL3_ERR_ARG;
+  *out = nullptr;
+  if (d->num_experts < 1 || d->num_experts > kMaxExperts) return EXL3_ERR_SHAPE;
+  if (d->hidden <= 0 || d->inter <= 0 || d->hidden % 128 || d->inter % 128) return EXL3_ERR_SHAPE;
+  for (int p = 0; p < 3; p++)
+    if (d->K[p] < 2 || d->K[p] > 4) return EXL3_ERR_K;
+  if (d->K[0] != d->K[1]) return EXL3_ERR_K;
+  const uint32_t mult = d->mcg_mult ? d->mcg_mult : kDefaultMcgMult;
+  if (!(mult & 1u)) return EXL3_ERR_ARG;
+  int nshared = 0;
+  for (int p = 0; p < 3; p++) {
+    if (!d->codes[p] || !d->suh[p] || !d->svh[p]) return EXL3_ERR_ARG;
+    if (!aligned16(d->codes[p])) return EXL3_ERR_ARG;
+    nshared += d->shared_w[p] != nullptr;
+    if (d->shared_w[p] && !aligned16(d->shared_w[p])) return EXL3_ERR_ARG;
+  }
+  if (nshared != 0 && nshared != 3) return EXL3_ERR_ARG;
+  exl3_status ds = check_device();
+  if (ds != EXL3_OK) return ds;
+  exl3_layer* L = static_cast<exl3_layer*>(calloc(1, sizeof(exl3_layer)));
+  if (!L) return EXL3_ERR_ARG;
+  LayerView& v = L->v;
+  v.E = d->num_experts; v.H = d->hidden; v.I = d->inter;
+  v.fp8 = d->fp8_round ? 1 : 0;
+  v.mult = mult;
+  for (int p = 0; p < 3; p++) {
+    v.K[p] = d->K[p];
+    v.codes[p] = d->codes[p];
+    v.suh[p] = d->suh[p];
+    v.svh[p] = d->svh[p];
+    v.shared_w[p] = d->shared_w[p];
+    const size_t in = p == 2 ? v.I : v.H, outf = p == 2 ? v.H : v.I;
+    v.code_stride[p] = (in / 16) * (outf / 16) * 16 * (size_t)d->K[p];
+  }
+  L->has_shared = nshared == 3;
+  *out = L;
+  return EXL3_OK;
+}
+
+void exl3_layer_destroy(exl3_layer_t* layer) { free(layer); }
+
+exl3_status exl3_decode_dense(const exl3_layer_t* layer, int expert, int proj, int apply_side,
+                              uint16_t* out, void* stream) {
+  if (!layer || !out || proj < 0 || proj > 2 || expert < 0 || expert >= layer->v.E)
+    return EXL3_ERR_ARG;
+  if (launch_decode_dense(layer->v, expert, proj, apply_side ? 1 : 0, out,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  return EXL3_OK;
+}
+
+size_t exl3_route_workspace_size(int T, int E, int top_k) {
+  if (T < 0 || E < 1 || top_k < 1) return 0;
+  return route_scratch_bytes(T, E, top_k);
+}
+
+exl3_status exl3_moe_route(const float* logits, int T, int E, int top_k, int32_t* ids, float* w,
+                           int32_t* seg_offsets, int32_t* seg_pairs, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts) return EXL3_ERR_SHAPE;
+  if (top_k < 1 || top_k > kMaxTopK || top_k > E) return EXL3_ERR_ARG;
+  if (!seg_offsets || !ws) return ws ? EXL3_ERR_ARG : EXL3_ERR_WORKSPACE;
+  if (T > 0 && (!logits || !ids || !w || !seg_pairs)) return EXL3_ERR_ARG;
+  if (ws_bytes < route_scratch_bytes(T, E, top_k)) return EXL3_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteBuffers rb{};
+  route_carve(ws, T, E, top_k, &rb);
+  rb.ids = ids; rb.w = w; rb.seg_offsets = seg_offsets; rb.seg_pairs = seg_pairs;
+  if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (launch_route(logits, T, E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
+  return EXL3_OK;
+}
+
+size_t exl3_moe_workspace_size(const exl3_layer_t* layer, int T, int top_k) {
+  if (!layer || T < 0 || top_k < 1) return 0;
+  return fwd_layout(layer->v, layer->has_shared, T, top_k).total;
+}
+
+exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
+                                const float* logits, int T, int top_k, const void* residual,
+                                void* out, int path, void* ws, size_t ws_bytes, void* stream) {
+  if (!layer) return EXL3_ERR_ARG;
+  const LayerView& L = layer->v;
+  if (dt != EXL3_F16 && dt != EXL3_BF16) return EXL3_ERR_ARG;
+  if (path < EXL3_PATH_AUTO || path > EXL3_PATH_GEMM) return EXL3_ERR_ARG;
+  if (T < 0) return EXL3_ERR_SHAPE;
+  if (top_k < 1 || top_k > kMaxTopK || top_k > L.E) return EXL3_ERR_ARG;
+  if (T == 0) return EXL3_OK;
+  if (!x || !logits || !out) return EXL3_ERR_ARG;
+  if (!aligned16(x) || !aligned16(out) || (residual && !aligned16(residual))) return EXL3_ERR_ARG;
+  if (x == out) return EXL3_ERR_ARG;
+  const FwdLayout f = fwd_layout(L, layer->has_shared, T, top_k);
+  if (!ws) return EXL3_ERR_WORKSPACE;
+  if (ws_bytes < f.total) return EXL3_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  RouteBuffers rb{};
+  route_carve(base + f.route, T, L.E, top_k, &rb);
+  rb.ids = reinterpret_cast<int32_t*>(base + f.ids);
+  rb.w = reinterpret_cast<float*>(base + f.w);
+  rb.seg_offsets = reinterpret_cast<int32_t*>(base + f.off);
+  rb.seg_pairs = reinterpret_cast<int32_t*>(base + f.pairs);
+  const int bf16 = dt == EXL3_BF16;
+
+  const cudaEvent_t* ev = layer->has_ev ? layer->ev : nullptr;
+  auto rec = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], st);
+  };
+  rec(0);
+  if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (launch_route(logits, T, L.E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
+  rec(1);
+
+  GemvBuffers gb{};
+  gemv_carve(base + f.gemv, T, top_k, L.H, L.I, &gb);
+  if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
+
+  const float* sp = nullptr;
+  int ns = 0;
+  if (layer->has_shared) {
+    float* pgu = reinterpret_cast<float*>(base + f.shared);
+    float* pd = pgu + al((size_t)2 * (L.H / kSharedKPer) * T * L.I * 4) / 4;
+    if (launch_shared(L, x, bf16, T, pgu, pd, st) != cudaSuccess) return EXL3_ERR_CUDA;
+    sp = pd;
+    ns = L.I / kSharedKPer;
+  }
+  rec(6);
+  if (launch_combine(gb.r, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  rec(7);
+  return EXL3_OK;
+}
+
+exl3_status exl3_moe_forward(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
+                             const float* logits, int T, int top_k, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return exl3_moe_forward_ex(layer, x, dt, logits, T, top_k, nullptr, out, EXL3_PATH_AUTO, ws,
+                             ws_bytes, stream);
+}
+
+exl3_status exl3_rmsnorm(const void* x, exl3_dtype dt, int T, int H, float eps, void* out,
+                         void* stream) {
+  if (dt != EXL3_F16 && dt != EXL3_BF16) return EXL3_ERR_ARG;
+  if (T < 0 || H <= 0 || H % 4) return EXL3_ERR_SHAPE;
+  if (T > 0 && (!x || !out || !aligned16(out))) return EXL3_ERR_ARG;
+  if (launch_rmsnorm(x, dt == EXL3_BF16, T, H, eps, out, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return EXL3_ERR_CUDA;
+  return EXL3_OK;
+}
+
+exl3_status exl3_layer_set_stage_events(exl3_layer_t* layer, void* const* events, int n_events) {
+  if (!layer) return EXL3_ERR_ARG;
+  if (!events) {
+    layer->has_ev = 0;
+    return EXL3_OK;
+  }
+  if (n_events != EXL3_NUM_STAGE_EVENTS) return EXL3_ERR_ARG;
+  for (int i = 0; i < EXL3_NUM_STAGE_EVENTS; i++) {
+    if (!events[i]) return EXL3_ERR_ARG;
+    layer->ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  layer->has_ev = 1;
+  return EXL3_OK;
+}
+
+uint64_t exl3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+exl3_status exl3_get_device_status(const void* ws, void* stream, int32_t* status) {
+  if (!ws || !status) return EXL3_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (cudaMemcpy(status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  return *status ? EXL3_ERR_DEVICE : EXL3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// Top-k routing and device-side segment tables.
+//
+// Page "GLM-5.3-Flash · exlr8 (K2/K3/K4)", intro: 288 routed experts with
+// top-8 routing.  Page "GLM-5.3 Flash EXL3 for 2x DGX Sparks", section Cold
+// prefill (E3): the expert launches are built from device-side segment
+// tables, with no per-expert launches and no host sync.
+//
+// Rules: experts by descending fp32 logit, ties to the lower index, NaN as
+// -inf; w_j = e_j / sum_j e_j (fp32, summed in j order) with e_j =
+// exp_route(l_j - l_max), the difference taken as 0 when l_j == l_max.
+// seg_offsets[e] counts pairs with expert < e; seg_pairs lists pair ids
+// t*k + j expert-major and ascending inside an expert (a stable counting
+// sort: per-chunk counts, a scan over (expert, chunk), a scatter by rank).
+#include "common.cuh"
+#include "internal.h"
+
+namespace exl3 {
+
+namespace {
+
+// One warp selects the top-k of one token.  MAXPL = logits held per lane.
+template <int MAXPL>
+__device__ __forceinline__ void warp_topk(const float* __restrict__ lrow, int E, int k,
+                                          int* my_id, float* my_w) {
+  const int lane = threadIdx.x & 31;
+  float v[MAXPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < MAXPL; i++) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float f = lrow[e];
+      v[i] = isnan(f) ? -INFINITY : f;
+    } else {
+      v[i] = -INFINITY;
+      taken |= 1u << i;
+    }
+  }
+  float lmax = 0.0f, mine_l = 0.0f;
+  int mine_e = 0;
+  for (int j = 0; j < k; j++) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < MAXPL; i++) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      mine_e = be;
+      mine_l = bv;
+    }
+    if (j == 0) lmax = bv;
+  }
+  // softmax over the k selected, in j order
+  float ex = 0.0f;
+  if (lane < k) {
+    const float d = (mine_l == lmax) ? 0.0f : __fsub_rn(mine_l, lmax);
+    ex = exp_route(d);
+  }
+  float sum = 0.0f;
+  for (int j = 0; j < k; j++) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+  *my_id = mine_e;
+  *my_w = (lane < k) ? __fdiv_rn(ex, sum) : 0.0f;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) smem_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < nw ? smem_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    if (lane < nw) smem_warp[lane] = s;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int base = wid > 0 ? smem_warp[wid - 1] : 0;
+  const int res = base + x - v;
+  if (total) *total = smem_warp[nw - 1];
+  __syncthreads();
+  return res;
+}
+
+// Per-chunk stage: top-k of kRouteChunk tokens, local stable ranks and
+// per-expert counts.  With `fused` (single chunk) it also finishes the
+// tables: offsets, active list and scatter.
+template <int MAXPL>
+__global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restrict__ logits, int T,
+                                                           int E, int k, RouteBuffers rb,
+                                                           int fused) {
+  __shared__ int s_ids[kRouteChunk * kMaxTopK];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_warp[32];
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kRouteChunk;
+  const int nt = min(kRouteChunk, T - t0);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int tl = wid; tl < nt; tl += nw) {
+    const int t = t0 + tl;
+    int id;
+    float wt;
+    warp_topk<MAXPL>(logits + (size_t)t * E, E, k, &id, &wt);
+    if (lane < k) {
+      rb.ids[(size_t)t * k + lane] = id;
+      rb.w[(size_t)t * k + lane] = wt;
+      s_ids[tl * k + lane] = id;
+    }
+  }
+  __syncthreads();
+  // stable local ranks: one warp walks the tokens in order; the k experts of a
+  // token are distinct, so lane j can bump its counter without conflicts
+  if (wid == 0) {
+    for (int tl = 0; tl < nt; tl++) {
+      if (lane < k) {
+        const int e = s_ids[tl * k + lane];
+        const int r = s_cnt[e];
+        s_cnt[e] = r + 1;
+        rb.rank[(size_t)(t0 + tl) * k + lane] = r;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (!fused) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      rb.chunk_counts[(size_t)chunk * E + e] = s_cnt[e];
+    return;
+  }
+  // fused: offsets = exclusive scan of the counts, active list, scatter
+  int total = 0, n_act = 0;
+  const int cnt = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
+  const int off = block_exclusive_scan(cnt, s_warp, &total);
+  const int aidx = block_exclusive_scan(cnt > 0 ? 1 : 0, s_warp, &n_act);
+  if (threadIdx.x < E) {
+    rb.seg_offsets[threadIdx.x] = off;
+    if (cnt > 0) rb.active[1 + aidx] = threadIdx.x;
+  }
+  if (threadIdx.x == 0) {
+    rb.seg_offsets[E] = total;
+    rb.active[0] = n_act;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) s_cnt[threadIdx.x] = off;  // segment starts
+  __syncthreads();
+  for (int pl = threadIdx.x; pl < nt * k; pl += blockDim.x) {
+    const size_t p = (size_t)t0 * k + pl;
+    const int e = s_ids[pl];
+    const int pos = s_cnt[e] + rb.rank[p];
+    rb.seg_pairs[pos] = (int)p;
+    rb.pair_pos[p] = pos;
+  }
+}
+
+// Scan stage (one CTA): exclusive prefix over chunks per expert, offsets over
+// experts, active list.  chunk_counts becomes the base of each (chunk, e).
+__global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, RouteBuffers rb) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; c++) {
+      const int v = rb.chunk_counts[(size_t)c * E + e];
+      rb.chunk_counts[(size_t)c * E + e] = tot;
+      tot += v;
+    }
+  }
+  int total = 0, n_act = 0;
+  const int off = block_exclusive_scan(tot, s_warp, &total);
+  const int aidx = block_exclusive_scan(tot > 0 ? 1 : 0, s_warp, &n_act);
+  if (e < E) {
+    rb.seg_offsets[e] = off;
+    if (tot > 0) rb.active[1 + aidx] = e;
+    for (int c = 0; c < nchunks; c++) rb.chunk_counts[(size_t)c * E + e] += off;
+  }
+  if (threadIdx.x == 0) {
+    rb.seg_offsets[E] = total;
+    rb.active[0] = n_act;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, RouteBuffers rb) {
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kRouteChunk;
+  const int nt = min(kRouteChunk, T - t0);
+  for (int pl = threadIdx.x; pl < nt * k; pl += blockDim.x) {
+    const size_t p = (size_t)t0 * k + pl;
+    const int e = rb.ids[p];
+    if (e < 0 || e >= E) {
+      atomicOr(rb.status, kStatusBadExpert);
+      continue;
+    }
+    const int pos = rb.chunk_counts[(size_t)chunk * E + e] + rb.rank[p];
+    rb.seg_pairs[pos] = (int)p;
+    rb.pair_pos[p] = pos;
+  }
+}
+
+__global__ void route_empty_kernel(int E, RouteBuffers rb) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) rb.seg_offsets[e] = 0;
+  if (threadIdx.x == 0) rb.active[0] = 0;
+}
+
+template <int MAXPL>
+cudaError_t launch_chunks(const float* logits, int T, int E, int k, const RouteBuffers& rb,
+                          int nchunks, cudaStream_t st) {
+  const int threads = nchunks == 1 ? 1024 : 512;
+  route_chunk_kernel<MAXPL><<<nchunks, threads, 0, st>>>(logits, T, E, k, rb, nchunks == 1);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+size_t route_scratch_bytes(int T, int E, int top_k) {
+  const size_t P = (size_t)T * top_k;
+  const size_t nchunks = (T + kRouteChunk - 1) / kRouteChunk;
+  size_t b = 0;
+  b += align256(sizeof(int32_t) * 4);            // status
+  b += align256(sizeof(int32_t) * P);            // pair_pos
+  b += align256(sizeof(int32_t) * (E + 1));      // active
+  b += align256(sizeof(int32_t) * nchunks * E);  // chunk counts
+  b += align256(sizeof(int32_t) * P);            // rank
+  return b;
+}
+
+void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb) {
+  const size_t P = (size_t)T * top_k;
+  const size_t nchunks = (T + kRouteChunk - 1) / kRouteChunk;
+  char* p = static_cast<char*>(ws);
+  rb->status = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * 4);
+  rb->pair_pos = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * P);
+  rb->active = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (E + 1));
+  rb->chunk_counts = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * nchunks * E);
+  rb->rank = reinterpret_cast<int32_t*>(p);
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBuffers& rb,
+                         cudaStream_t st) {
+  if (T == 0) {
+    route_empty_kernel<<<1, 256, 0, st>>>(E, rb);
+    note_launches(1);
+    return cudaGetLastError();
+  }
+  const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
+  const int pl = (E + 31) / 32;
+  cudaError_t err;
+  if (pl <= 1) err = launch_chunks<1>(logits, T, E, k, rb, nchunks, st);
+  else if (pl <= 2) err = launch_chunks<2>(logits, T, E, k, rb, nchunks, st);
+  else if (pl <= 4) err = launch_chunks<4>(logits, T, E, k, rb, nchunks, st);
+  else if (pl <= 9) err = launch_chunks<9>(logits, T, E, k, rb, nchunks, st);
+  else if (pl <= 16) err = launch_chunks<16>(logits, T, E, k, rb, nchunks, st);
+  else err = launch_chunks<32>(logits, T, E, k, rb, nchunks, st);
+  if (err != cudaSuccess || nchunks == 1) return err;
+  route_scan_kernel<<<1, 1024, 0, st>>>(E, nchunks, rb);
+  note_launches(1);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  route_scatter_kernel<<<nchunks, 256, 0, st>>>(T, E, k, rb);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace exl3
