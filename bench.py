@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="decode (default), verify3, verify4, prefill: parity/profiling cases")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (smaller device footprint for profilers)")
     return ap.parse_args()
 
 
@@ -188,6 +192,18 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def pick_workload(args):
+    import dataclasses
+
+    from trellis_quantized_moe_exl3_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    spec = wl.layers[0]
+    if args.experts:
+        spec = dataclasses.replace(spec, num_experts=args.experts)
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-E{args.experts}")
+    return wl, spec
+
+
 def workload_config(wl):
     s = wl.layers[0]
     return {"workload": (f"{wl.name}: {s.num_experts} experts top-{wl.top_k}, hidden {s.hidden}, "
@@ -217,11 +233,10 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = synth.WORKLOADS[WORKLOAD]
-    spec = wl.layers[0]
+    wl, spec = pick_workload(args)
     codes = [synth.layer_codes(spec, p) for p in range(3)]
     sides = [synth.side_vectors(spec, p) for p in range(3)]
-    sw = synth.shared_weights(spec)
+    sw = synth.shared_weights(spec) if spec.shared else None
     # every rank runs its own token batch (weak scaling)
     x_np = synth.activations(wl.seed + 1000 * rank, wl.T, spec.hidden, wl.act)
     lg_np = synth.router_logits(spec.seed + 1000 * rank, wl.T, spec.num_experts, wl.routing)
@@ -230,7 +245,7 @@ def run_ours(args):
     d_codes = [t16(c) for c in codes]
     d_suh = [t16(s[0]).view(torch.float16) for s in sides]
     d_svh = [t16(s[1]).view(torch.float16) for s in sides]
-    d_sw = [t16(a).view(torch.float16) for a in sw]
+    d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
     layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw)
     x = t16(x_np).view(torch.bfloat16)
     lg = torch.from_numpy(lg_np).to(dev)
@@ -377,7 +392,7 @@ def run_ours(args):
     stage_bytes = {
         "gate_up": n_active * (code_b[0] + code_b[1] + side_b[0] + side_b[1]),
         "down": n_active * (code_b[2] + side_b[2]),
-        "shared": 3 * H * I * 2,
+        "shared": 3 * H * I * 2 if sw else 0,
     }
     dom = max(stage_bytes, key=lambda n: stage_ms[stage_names.index(n)])
     dom_ms = float(stage_ms[stage_names.index(dom)])
@@ -407,7 +422,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
         rate, secs, sample = oracle_pair_rate(wl, spec, x_np, lg_np, 3, shared_w=sw, codes=codes)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": sample, "seconds": secs}
