@@ -11,6 +11,17 @@ namespace exl3 {
 // Host-side count of kernel launches (exl3_launch_count).
 void note_launches(int n);
 
+// Record a profiling event; inside stream capture it becomes an external
+// event node, so it can still be timed after graph replay.
+inline void record_stage_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
+}
+
 constexpr uint32_t kDefaultMcgMult = 0x9E3779B1u;
 constexpr int kRouteChunk = 128;   // tokens per routing CTA
 constexpr int kMaxTopK = 16;

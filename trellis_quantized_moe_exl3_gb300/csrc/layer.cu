@@ -181,7 +181,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
 
   const cudaEvent_t* ev = layer->has_ev ? layer->ev : nullptr;
   auto rec = [&](int i) {
-    if (ev) cudaEventRecordWithFlags(ev[i], st, cudaEventRecordExternal);
+    if (ev) record_stage_event(ev[i], st);
   };
   rec(0);
   if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;

@@ -307,7 +307,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
                             const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,
                             cudaStream_t st) {
   auto rec = [&](int i) {
-    if (ev && ev[i]) cudaEventRecordWithFlags(ev[i], st, cudaEventRecordExternal);
+    if (ev && ev[i]) record_stage_event(ev[i], st);
   };
   const int P = T * top_k;
   const int slots = P < L.E ? P : L.E;
