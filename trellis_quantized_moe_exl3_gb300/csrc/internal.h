@@ -26,6 +26,7 @@ constexpr uint32_t kDefaultMcgMult = 0x9E3779B1u;
 constexpr int kRouteChunk = 128;   // tokens per routing CTA
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
+constexpr int kGroup = 8;          // tokens per GEMV token group (MMA N)
 
 // Device status bits (workspace status word).
 enum : int32_t {
@@ -44,7 +45,16 @@ struct RouteBuffers {
   int32_t* chunk_counts; // [nchunks][E]
   int32_t* rank;         // [P]
   int32_t* status;       // [1]
+  int32_t* group_off;    // [E+1]: first token group of each expert; [E] = number of groups
+  int32_t* groups;       // [max_groups][4]: {expert, first position, count, 0}
 };
+
+// Upper bound on the number of kGroup-token groups over all experts.
+inline size_t max_groups(int T, int E, int top_k) {
+  const size_t P = (size_t)T * top_k;
+  const size_t a = (P + kGroup - 1) / kGroup + ((size_t)E < P ? (size_t)E : P);
+  return a < P ? a : P;
+}
 
 size_t route_scratch_bytes(int T, int E, int top_k);
 // Carves RouteBuffers out of `ws` (ids/w/seg may be caller-provided: non-null
@@ -70,15 +80,19 @@ cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int ap
 
 // ---- grouped GEMV path (decode-sized steps)
 struct GemvBuffers {
-  uint32_t* xs_gu;   // [P][2][H] fp16x2 (dup), permuted per 16-block
+  uint32_t* xs_gu;   // [group][2][H/16][8][16] fp16x2 (dup), permuted per 16-block
   float* xs_gu_inv;  // [P][2]
   float* h;          // [P][I] fp32 (pair-sorted rows)
-  uint32_t* xs_d;    // [P][I] fp16x2 (dup), permuted
+  uint32_t* xs_d;    // [group][I/16][8][16] fp16x2 (dup), permuted
   float* xs_d_inv;   // [P]
   float* r;          // [P][H] fp32 rows by pair id
+  float* partial;    // K-split partial sums
+  int32_t* counters; // K-split tickets
+  size_t n_counters;
+  int ns_gu, ns_d;   // K splits of the two launches
 };
-size_t gemv_scratch_bytes(int T, int top_k, int H, int I);
-void gemv_carve(void* ws, int T, int top_k, int H, int I, GemvBuffers* gb);
+size_t gemv_scratch_bytes(int T, int top_k, int E, int H, int I);
+void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb);
 // ev (may be null): events recorded after gather [2], gate/up [3], down prep [4], down [5].
 cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
                             const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,

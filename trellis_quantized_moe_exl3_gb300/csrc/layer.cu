@@ -51,7 +51,7 @@ FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
   f.w = o; o += al(P * 4);
   f.off = o; o += al((size_t)(L.E + 1) * 4);
   f.pairs = o; o += al(P * 4);
-  f.gemv = o; o += al(gemv_scratch_bytes(T, k, L.H, L.I));
+  f.gemv = o; o += al(gemv_scratch_bytes(T, k, L.E, L.H, L.I));
   f.shared = o; o += has_shared ? al(shared_scratch_bytes(T, L.H, L.I)) : 0;
   f.total = o;
   return f;
@@ -189,7 +189,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   rec(1);
 
   GemvBuffers gb{};
-  gemv_carve(base + f.gemv, T, top_k, L.H, L.I, &gb);
+  gemv_carve(base + f.gemv, T, top_k, L.E, L.H, L.I, &gb);
   if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
 
   const float* sp = nullptr;

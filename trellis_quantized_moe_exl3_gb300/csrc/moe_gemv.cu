@@ -1,35 +1,54 @@
 // Grouped GEMV path for decode-sized steps (a few tokens per expert).
 //
 // Page "GLM-5.3-Flash EXL3 (~2.1 bpw, SM70 tile order)", Running it: the
-// expert kernels decode the trellis inside the matmul; Speed: per-lane window
-// loads of the strip-major tiles.  Page "GLM-5.3 Flash EXL3 for 2x DGX
-// Sparks", section Cold prefill (E3): gather, gate/up + SwiGLU, down +
-// scatter, driven by device-side segment tables.
+// expert kernels decode the trellis inside the matmul; Speed: direct per-lane
+// window loads of strip-major tiles with deep prefetch.  Page "GLM-5.3 Flash
+// EXL3 for 2x DGX Sparks", section Cold prefill (E3): gather, gate/up +
+// SwiGLU, down + scatter, driven by device-side segment tables.
 //
-// Work item = (active expert, 128-output strip, group of 8 tokens).  Each
-// warp of a CTA takes every W-th 16-input block; per block it streams the 8
-// consecutive tiles of the strip with one coalesced load per lane (8K bytes
-// per lane), decodes its 64 weights in registers (the 16-K bit overlap comes
-// from the next lane of the quad by shuffle) and feeds them to mma.m16n8k16
-// with the K dimension doubled: the A register of weight (o, i) is the
-// codebook's {a, b} fp16 pair itself and the B register holds {x_i, x_i}, so
-// the tensor core forms (a + b) * x_i without a separate add.  (The exact sum
-// a + b differs from the format's fp16(a + b) by at most half an fp16 ulp,
-// far inside the layer tolerance; with the E4M3 rule the rounded value is
-// formed first and placed as {v, 0}.)  Partial sums of the W warps are added
-// in a fixed order in shared memory; no atomics anywhere.
+// Work item = (token group of <= 8 positions of one expert, 128-output strip,
+// K split).  A persistent grid walks the items.  Per CTA one producer warp
+// streams, with bulk copies (TMA engine) into a ring of shared-memory stages,
+// the code rows of the strip (8 consecutive tiles per 16-input block) and the
+// matching activation rows (8 tokens x 16 inputs); 8 consumer warps each take
+// one block of a stage: every lane loads its 8K bytes of a tile (the 16-K bit
+// window overlap comes from the next lane of the quad by shuffle), decodes 64
+// weights in registers and feeds mma.m16n8k16 with the K dimension doubled:
+// the A register of weight (o, i) is the codebook's {a, b} fp16 pair itself
+// and the B register holds {x_i, x_i}, so the tensor core forms (a + b) x_i
+// with no separate add.  (The exact a + b differs from the format's
+// fp16(a + b) by at most half an fp16 ulp; with the E4M3 rule the rounded
+// value is formed first and placed as {v, 0}.)
+//
+// Partial sums of the 8 warps are added in a fixed tree order in shared
+// memory; K splits write their partials to the workspace and the CTA that
+// completes an item last (atomic ticket) adds them in split order.  The
+// result does not depend on scheduling and no atomics touch the data.
 //
 // Activations enter as fp16 with a power-of-two scale per (pair, projection)
-// chosen from the row's max |x * suh| (undone in the epilogue), so the fp16
+// chosen from the row's max |x * suh| and undone in the epilogue, so the fp16
 // operand never overflows whatever the input magnitude.
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace exl3 {
 
 namespace {
 
-constexpr int kW = 4;  // warps per CTA
+constexpr int kCW = 8;                     // consumer warps per CTA
+constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
+constexpr int kXsChunk = kGroup * 16 * 4;  // 8 tokens x 16 inputs x fp16x2
+
+template <int K, int NPROJ>
+struct Cfg {
+  static constexpr int kCodeChunk = 8 * 32 * K;  // 8 tiles of one 16-input block
+  static constexpr int kStageBytes = kCW * NPROJ * (kCodeChunk + kXsChunk);
+  static constexpr int kStages = (NPROJ == 2 && K >= 3) ? 3 : 4;
+  static constexpr int kRedBytes = 4 * NPROJ * 1024 * 4;  // half the warps spill at a time
+  static constexpr int kBarOff = kStages * kStageBytes + kRedBytes;
+  static constexpr int kSmem = kBarOff + 2 * kStages * 8;
+};
 
 __device__ __forceinline__ float block_max(float v, float* s_tmp) {
   for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -54,18 +73,28 @@ __device__ __forceinline__ int perm_slot(int idx) {
   return 4 * (r & 3) + (r >> 2);
 }
 
-// x rows of the pairs in segment order, times suh of gate and up, scaled.
+// Token group and slot of a segment position.
+__device__ __forceinline__ void group_of(const int32_t* seg_offsets, const int32_t* group_off, int e,
+                                         int pos, int* g, int* slot) {
+  const int l = pos - seg_offsets[e];
+  *g = group_off[e] + l / kGroup;
+  *slot = l % kGroup;
+}
+
+// x rows of the pairs, times suh of gate and up, scaled, into the
+// group-interleaved layout [group][proj][in/16][8 tokens][16] (fp16x2).
 __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__ x, int x_bf16,
-                                                        int H, int k, const int32_t* seg_pairs,
-                                                        const int32_t* ids,
+                                                        int H, int k, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_g,
                                                         const uint16_t* __restrict__ suh_u,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
-  const int p = seg_pairs[pos];
-  const int t = p / k, e = ids[p];
+  const int p = rb.seg_pairs[pos];
+  const int t = p / k, e = rb.ids[p];
+  int g, slot;
+  group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
   const uint16_t* sg = suh_g + (size_t)e * H;
   const uint16_t* su = suh_u + (size_t)e * H;
   float ag = 0.0f, au = 0.0f;
@@ -78,11 +107,12 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   au = block_max(au, s_tmp);
   const int eg = fp16_scale_exp(ag), eu = fp16_scale_exp(au);
   const float scg = ldexpf(1.0f, eg), scu = ldexpf(1.0f, eu);
-  uint32_t* og = xs + (size_t)pos * 2 * H;
-  uint32_t* ou = og + H;
+  const int nb = H / 16;
+  uint32_t* og = xs + (size_t)g * 2 * nb * kXsChunk / 4;
+  uint32_t* ou = og + (size_t)nb * kXsChunk / 4;
   for (int idx = threadIdx.x; idx < H; idx += blockDim.x) {
     const float xv = load_act(x, x_bf16, (size_t)t * H + idx);
-    const int dst = (idx & ~15) + perm_slot(idx);
+    const size_t dst = ((size_t)(idx >> 4) * kGroup + slot) * 16 + perm_slot(idx);
     og[dst] = dup_f16(xv * __half2float(__ushort_as_half(sg[idx])) * scg);
     ou[dst] = dup_f16(xv * __half2float(__ushort_as_half(su[idx])) * scu);
   }
@@ -92,16 +122,17 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   }
 }
 
-// h rows (pair-sorted) times suh of down, scaled, permuted, duplicated.
+// h rows (by position) times suh of down, scaled, group-interleaved.
 __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ h, int I,
-                                                        const int32_t* seg_pairs,
-                                                        const int32_t* ids,
+                                                        RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
-  const int e = ids[seg_pairs[pos]];
+  const int e = rb.ids[rb.seg_pairs[pos]];
+  int g, slot;
+  group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
   const uint16_t* sd = suh_d + (size_t)e * I;
   const float* hr = h + (size_t)pos * I;
   float am = 0.0f;
@@ -110,9 +141,10 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
   am = block_max(am, s_tmp);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
-  uint32_t* o = xs + (size_t)pos * I;
+  uint32_t* o = xs + (size_t)g * (I / 16) * kXsChunk / 4;
   for (int idx = threadIdx.x; idx < I; idx += blockDim.x)
-    o[(idx & ~15) + perm_slot(idx)] = dup_f16(hr[idx] * __half2float(__ushort_as_half(sd[idx])) * sc);
+    o[((size_t)(idx >> 4) * kGroup + slot) * 16 + perm_slot(idx)] =
+        dup_f16(hr[idx] * __half2float(__ushort_as_half(sd[idx])) * sc);
   if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex);
 }
 
@@ -141,166 +173,353 @@ __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& 
   }
 }
 
-struct GemvParams {
-  const uint16_t* codes[2];
-  size_t stride[2];       // uint16 words per expert
-  int in, out;
-  uint32_t mult;
-  const uint16_t* svh[2]; // [E][out]
-  const uint32_t* xs;     // [pos][NPROJ][in] fp16x2 permuted
-  const float* xs_inv;    // [pos][NPROJ]
-  const int32_t* seg_offsets;
-  const int32_t* active;
-  const int32_t* seg_pairs;
-  const float* wts;       // router weights by pair id
-  float* h_out;           // NPROJ == 2: [pos][out]
-  float* r_out;           // NPROJ == 1: [pair id][out]
-};
-
-__device__ __forceinline__ uint4 ld_b(const uint32_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-template <int K, int FP8, int NPROJ>
-__global__ void __launch_bounds__(kW * 32) gemv_kernel(GemvParams p) {
-  extern __shared__ float s_red[];  // [kW][NPROJ][1024]
-  const int strips = p.out / 128;
-  const int slot = blockIdx.x / strips, s = blockIdx.x % strips;
-  if (slot >= p.active[0]) return;
-  const int e = p.active[1 + slot];
-  const int seg0 = p.seg_offsets[e], seg1 = p.seg_offsets[e + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
-  const int nblk = p.in / 16;
-  const size_t row_words = (size_t)(p.out / 16) * 16 * K;
-  const uint16_t* cbase[NPROJ];
+template <int K>
+__device__ __forceinline__ void lds_lane_words(LaneWords<K>& lw, const uint8_t* p) {
+  if constexpr (K == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    lw.w[0] = v.x; lw.w[1] = v.y; lw.w[2] = v.z; lw.w[3] = v.w;
+  } else if constexpr (K == 3) {
 #pragma unroll
-  for (int pj = 0; pj < NPROJ; pj++)
-    cbase[pj] = p.codes[pj] + p.stride[pj] * e + (size_t)8 * s * 16 * K + lane * 4 * K;
-
-  for (int tg0 = seg0; tg0 < seg1; tg0 += 8) {
-    float acc[NPROJ][8][4];
-#pragma unroll
-    for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-      for (int r = 0; r < 8; r++)
-#pragma unroll
-        for (int d = 0; d < 4; d++) acc[pj][r][d] = 0.0f;
-    const int bpos = tg0 + g;
-    const bool bvalid = bpos < seg1;
-    const uint32_t* xrow[NPROJ];
-#pragma unroll
-    for (int pj = 0; pj < NPROJ; pj++)
-      xrow[pj] = p.xs + ((size_t)(bvalid ? bpos : seg0) * NPROJ + pj) * p.in + 4 * c;
-
-    LaneWords<K> cur[NPROJ], nxt[NPROJ];
-    uint4 cb[NPROJ], nb[NPROJ];
-    int i = warp;
-    if (i < nblk) {
-#pragma unroll
-      for (int pj = 0; pj < NPROJ; pj++) {
-        load_lane_words<K>(cur[pj], cbase[pj] + (size_t)i * row_words);
-        cb[pj] = bvalid ? ld_b(xrow[pj] + i * 16) : make_uint4(0, 0, 0, 0);
-      }
+    for (int q = 0; q < 3; q++) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p + 8 * q);
+      lw.w[2 * q] = v.x; lw.w[2 * q + 1] = v.y;
     }
-    for (; i < nblk; i += kW) {
-      const int inext = i + kW;
-      if (inext < nblk) {
+  } else {
 #pragma unroll
-        for (int pj = 0; pj < NPROJ; pj++) {
-          load_lane_words<K>(nxt[pj], cbase[pj] + (size_t)inext * row_words);
-          nb[pj] = bvalid ? ld_b(xrow[pj] + inext * 16) : make_uint4(0, 0, 0, 0);
-        }
-      }
-#pragma unroll
-      for (int pj = 0; pj < NPROJ; pj++) {
-        fetch_neighbour<K>(cur[pj]);
-        decode_mma<K, FP8>(cur[pj], cb[pj], acc[pj], p.mult);
-      }
-#pragma unroll
-      for (int pj = 0; pj < NPROJ; pj++) {
-        cur[pj] = nxt[pj];
-        cb[pj] = nb[pj];
-      }
-    }
-    __syncthreads();  // the previous group's epilogue has finished with s_red
-    float* my = s_red + (size_t)warp * NPROJ * 1024;
-#pragma unroll
-    for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-      for (int r = 0; r < 8; r++)
-#pragma unroll
-        for (int d = 0; d < 4; d++) my[pj * 1024 + (r * 32 + lane) * 4 + d] = acc[pj][r][d];
-    __syncthreads();
-    for (int v = threadIdx.x; v < 1024; v += blockDim.x) {
-      float sum[NPROJ];
-#pragma unroll
-      for (int pj = 0; pj < NPROJ; pj++) sum[pj] = 0.0f;
-      for (int w = 0; w < kW; w++)
-#pragma unroll
-        for (int pj = 0; pj < NPROJ; pj++) sum[pj] += s_red[((size_t)w * NPROJ + pj) * 1024 + v];
-      const int r0 = v >> 7, ln = (v >> 2) & 31, d = v & 3;
-      const int o = 16 * (8 * s + (ln >> 2)) + r0 + 8 * (d >> 1);
-      const int pos = tg0 + 2 * (ln & 3) + (d & 1);
-      if (pos < seg1) {
-        if constexpr (NPROJ == 2) {
-          const float G = sum[0] * p.xs_inv[2 * pos] *
-                          __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o]));
-          const float U = sum[1] * p.xs_inv[2 * pos + 1] *
-                          __half2float(__ushort_as_half(p.svh[1][(size_t)e * p.out + o]));
-          p.h_out[(size_t)pos * p.out + o] = silu_f(G) * U;
-        } else {
-          const int pid = p.seg_pairs[pos];
-          p.r_out[(size_t)pid * p.out + o] =
-              sum[0] * p.xs_inv[pos] *
-              __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o])) * p.wts[pid];
-        }
-      }
+    for (int q = 0; q < 2; q++) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p + 16 * q);
+      lw.w[4 * q] = v.x; lw.w[4 * q + 1] = v.y; lw.w[4 * q + 2] = v.z; lw.w[4 * q + 3] = v.w;
     }
   }
 }
 
+struct GemvParams {
+  const uint16_t* codes[2];
+  size_t stride[2];        // uint16 words per expert
+  int in, out;
+  uint32_t mult;
+  const uint16_t* svh[2];  // [E][out]
+  const uint32_t* xs;      // [group][NPROJ][in/16][8][16] fp16x2
+  const float* xs_inv;     // [pos][NPROJ]
+  const int32_t* groups;   // [g][4] {expert, pos0, count, 0}
+  const int32_t* n_groups; // device scalar
+  const int32_t* seg_pairs;
+  const float* wts;        // router weights by pair id
+  float* h_out;            // NPROJ == 2: [pos][out]
+  float* r_out;            // NPROJ == 1: [pair id][out]
+  float* partial;          // [group][strip][nsplit][NPROJ][1024]
+  int32_t* counters;       // [group][strip], zero on entry, left zero
+  int32_t* status;
+  int nsplit;
+};
+
 template <int K, int FP8, int NPROJ>
-cudaError_t launch_gemv(const GemvParams& gp, int grid, cudaStream_t st) {
-  const size_t smem = (size_t)kW * NPROJ * 1024 * sizeof(float);
-  gemv_kernel<K, FP8, NPROJ><<<grid, kW * 32, smem, st>>>(gp);
+__global__ void __maxnreg__(112) gemv_kernel(GemvParams p) {
+  using C = Cfg<K, NPROJ>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + C::kStages;
+  float* red = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  __shared__ int s_abort, s_stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCW);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int strips = p.out / 128;
+  const int nblk = p.in / 16;
+  const int bps = nblk / p.nsplit;
+  const int stages_per_item = bps / kCW;
+  const int n_items = p.n_groups[0] * strips * p.nsplit;
+  const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    int r = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int s = item % strips;
+      const int gq = item / strips;
+      const int q = gq % p.nsplit, g = gq / p.nsplit;
+      const int e = p.groups[4 * g];
+      for (int st = 0; st < stages_per_item; st++) {
+        if (!mbar_wait_bounded(&empty[r], ph ^ 1)) {
+          atomicOr(p.status, kStatusTimeout);
+          s_abort = 1;
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[r], C::kStageBytes);
+        __syncwarp();
+        if (lane < 2 * NPROJ * kCW) {
+          const int kind = lane & 1, pj = (lane >> 1) % NPROJ, w = (lane >> 1) / NPROJ;
+          const int blk = q * bps + st * kCW + w;
+          uint8_t* stage = smem + (size_t)r * C::kStageBytes;
+          if (kind == 0) {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
+                                 (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
+            bulk_g2s(stage + (w * NPROJ + pj) * C::kCodeChunk, src, C::kCodeChunk, &full[r]);
+          } else {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xs) +
+                                 (((size_t)g * NPROJ + pj) * nblk + blk) * kXsChunk;
+            bulk_g2s(stage + kCW * NPROJ * C::kCodeChunk + (w * NPROJ + pj) * kXsChunk, src,
+                     kXsChunk, &full[r]);
+          }
+        }
+        issued++;
+        if (++r == C::kStages) {
+          r = 0;
+          ph ^= 1;
+        }
+      }
+    }
+    // every issued stage is consumed unless the consumers stopped early; wait
+    // (bounded) for the copies still in flight before this warp leaves
+    const int tail = issued < C::kStages ? issued : C::kStages;
+    for (int i = 0; i < tail; i++) {
+      if (--r < 0) {
+        r = C::kStages - 1;
+        ph ^= 1;
+      }
+      mbar_wait_bounded(&full[r], ph);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g_l = lane >> 2, c_l = lane & 3;
+  int r = 0;
+  uint32_t ph = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int s = item % strips;
+    const int gq = item / strips;
+    const int q = gq % p.nsplit, g = gq / p.nsplit;
+    float acc[NPROJ][8][4];
+#pragma unroll
+    for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+      for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int d = 0; d < 4; d++) acc[pj][i][d] = 0.0f;
+    for (int st = 0; st < stages_per_item; st++) {
+      if (!mbar_wait_bounded(&full[r], ph)) {
+        atomicOr(p.status, kStatusTimeout);
+        s_abort = 1;
+      }
+      const uint8_t* stage = smem + (size_t)r * C::kStageBytes;
+#pragma unroll
+      for (int pj = 0; pj < NPROJ; pj++) {
+        LaneWords<K> lw;
+        lds_lane_words<K>(lw, stage + (warp * NPROJ + pj) * C::kCodeChunk + lane * 8 * K);
+        fetch_neighbour<K>(lw);
+        const uint4 b = *reinterpret_cast<const uint4*>(
+            stage + kCW * NPROJ * C::kCodeChunk + (warp * NPROJ + pj) * kXsChunk + g_l * 64 + c_l * 16);
+        decode_mma<K, FP8>(lw, b, acc[pj], p.mult);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[r]);
+      if (++r == C::kStages) {
+        r = 0;
+        ph ^= 1;
+      }
+    }
+    // fixed-order tree reduction over the 8 warps: 4+4, 2+2, 1+1
+#pragma unroll
+    for (int half = 4; half >= 1; half >>= 1) {
+      if (warp >= half && warp < 2 * half) {
+        float* dst = red + (size_t)(warp - half) * NPROJ * 1024;
+#pragma unroll
+        for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            *reinterpret_cast<float4*>(dst + pj * 1024 + (i * 32 + lane) * 4) =
+                make_float4(acc[pj][i][0], acc[pj][i][1], acc[pj][i][2], acc[pj][i][3]);
+      }
+      if (half == 1 && threadIdx.x == 0) s_stop = s_abort;  // one snapshot for all warps
+      named_bar_sync(1, kCW * 32);
+      if (warp < half) {
+        const float* src = red + (size_t)warp * NPROJ * 1024;
+#pragma unroll
+        for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const float4 v = *reinterpret_cast<const float4*>(src + pj * 1024 + (i * 32 + lane) * 4);
+            acc[pj][i][0] += v.x; acc[pj][i][1] += v.y; acc[pj][i][2] += v.z; acc[pj][i][3] += v.w;
+          }
+      }
+      named_bar_sync(1, kCW * 32);
+    }
+    if (warp == 0) {
+      bool do_epi = true;
+      if (p.nsplit > 1) {
+        const size_t slot = (size_t)g * strips + s;
+        float* mine = p.partial + ((slot * p.nsplit + q) * NPROJ) * 1024;
+#pragma unroll
+        for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            *reinterpret_cast<float4*>(mine + pj * 1024 + (i * 32 + lane) * 4) =
+                make_float4(acc[pj][i][0], acc[pj][i][1], acc[pj][i][2], acc[pj][i][3]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.counters[slot], 1) == p.nsplit - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        do_epi = last;
+        if (last) {
+          __threadfence();
+#pragma unroll
+          for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+              for (int d = 0; d < 4; d++) acc[pj][i][d] = 0.0f;
+          for (int qq = 0; qq < p.nsplit; qq++) {
+            const float* src = p.partial + ((slot * p.nsplit + qq) * NPROJ) * 1024;
+#pragma unroll
+            for (int pj = 0; pj < NPROJ; pj++)
+#pragma unroll
+              for (int i = 0; i < 8; i++) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4*>(src + pj * 1024 + (i * 32 + lane) * 4));
+                acc[pj][i][0] += v.x; acc[pj][i][1] += v.y; acc[pj][i][2] += v.z; acc[pj][i][3] += v.w;
+              }
+          }
+          if (lane == 0) p.counters[slot] = 0;
+        }
+      }
+      if (do_epi) {
+        const int e = p.groups[4 * g], pos0 = p.groups[4 * g + 1], cnt = p.groups[4 * g + 2];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+          for (int d = 0; d < 4; d++) {
+            const int o = 16 * (8 * s + g_l) + i + 8 * (d >> 1);
+            const int n = 2 * c_l + (d & 1);
+            if (n < cnt) {
+              const int pos = pos0 + n;
+              if constexpr (NPROJ == 2) {
+                const float G = acc[0][i][d] * p.xs_inv[2 * pos] *
+                                __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o]));
+                const float U = acc[1][i][d] * p.xs_inv[2 * pos + 1] *
+                                __half2float(__ushort_as_half(p.svh[1][(size_t)e * p.out + o]));
+                p.h_out[(size_t)pos * p.out + o] = silu_f(G) * U;
+              } else {
+                const int pid = p.seg_pairs[pos];
+                p.r_out[(size_t)pid * p.out + o] =
+                    acc[0][i][d] * p.xs_inv[pos] *
+                    __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o])) * p.wts[pid];
+              }
+            }
+          }
+      }
+    }
+    if (s_stop) break;  // uniform: written before the item's last barrier pair
+  }
+}
+
+template <int K, int FP8, int NPROJ>
+cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
+  using C = Cfg<K, NPROJ>;
+  static int occ = -1, sms = 0;
+  auto kfn = gemv_kernel<K, FP8, NPROJ>;
+  if (occ < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int o = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kThreads, C::kSmem);
+    occ = o < 1 ? 1 : o;
+  }
+  int grid = sms * occ;
+  if (items_ub < grid) grid = items_ub;
+  if (grid < 1) grid = 1;
+  kfn<<<grid, kThreads, C::kSmem, st>>>(gp);
   note_launches(1);
   return cudaGetLastError();
 }
 
 template <int NPROJ>
-cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int grid, cudaStream_t st) {
+cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int items_ub, cudaStream_t st) {
   if (fp8) {
-    if (K == 2) return launch_gemv<2, 1, NPROJ>(gp, grid, st);
-    if (K == 3) return launch_gemv<3, 1, NPROJ>(gp, grid, st);
-    return launch_gemv<4, 1, NPROJ>(gp, grid, st);
+    if (K == 2) return launch_gemv<2, 1, NPROJ>(gp, items_ub, st);
+    if (K == 3) return launch_gemv<3, 1, NPROJ>(gp, items_ub, st);
+    return launch_gemv<4, 1, NPROJ>(gp, items_ub, st);
   }
-  if (K == 2) return launch_gemv<2, 0, NPROJ>(gp, grid, st);
-  if (K == 3) return launch_gemv<3, 0, NPROJ>(gp, grid, st);
-  return launch_gemv<4, 0, NPROJ>(gp, grid, st);
+  if (K == 2) return launch_gemv<2, 0, NPROJ>(gp, items_ub, st);
+  if (K == 3) return launch_gemv<3, 0, NPROJ>(gp, items_ub, st);
+  return launch_gemv<4, 0, NPROJ>(gp, items_ub, st);
 }
 
-static size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
+// K splits: double while each split keeps >= 2 stages of blocks and the
+// upper bound on items stays below ~6 per CTA slot (2 CTAs on 152 SMs).
+int choose_nsplit(size_t groups_ub, int strips, int nblk) {
+  int ns = 1;
+  while (ns < 8 && nblk % (2 * ns * kCW) == 0 && nblk / (2 * ns) >= 2 * kCW &&
+         groups_ub * strips * ns < (size_t)6 * 304)
+    ns *= 2;
+  return ns;
+}
+
+size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
+
+struct GemvLayout {
+  size_t xs_gu, xs_gu_inv, h, xs_d, xs_d_inv, r, partial, counters, total;
+  int ns_gu, ns_d;
+  size_t n_counters;
+};
+
+GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
+  GemvLayout g{};
+  const size_t P = (size_t)T * top_k;
+  const size_t G = max_groups(T, E, top_k);
+  g.ns_gu = choose_nsplit(G, I / 128, H / 16);
+  g.ns_d = choose_nsplit(G, H / 128, I / 16);
+  const size_t part_gu = g.ns_gu > 1 ? G * (I / 128) * g.ns_gu * 2 * 1024 * 4 : 0;
+  const size_t part_d = g.ns_d > 1 ? G * (H / 128) * g.ns_d * 1024 * 4 : 0;
+  g.n_counters = G * ((I > H ? I : H) / 128);
+  size_t o = 0;
+  g.xs_gu = o; o += al(G * 2 * (H / 16) * kXsChunk);
+  g.xs_gu_inv = o; o += al(P * 2 * 4);
+  g.h = o; o += al(P * I * 4);
+  g.xs_d = o; o += al(G * (I / 16) * kXsChunk);
+  g.xs_d_inv = o; o += al(P * 4);
+  g.r = o; o += al(P * H * 4);
+  g.partial = o; o += al(part_gu > part_d ? part_gu : part_d);
+  g.counters = o; o += al(g.n_counters * 4);
+  g.total = o;
+  return g;
+}
 
 }  // namespace
 
-size_t gemv_scratch_bytes(int T, int top_k, int H, int I) {
-  const size_t P = (size_t)T * top_k;
-  return al(P * 2 * H * 4) + al(P * 2 * 4) + al(P * I * 4) + al(P * I * 4) + al(P * 4) +
-         al(P * H * 4);
+size_t gemv_scratch_bytes(int T, int top_k, int E, int H, int I) {
+  return gemv_layout(T, top_k, E, H, I).total;
 }
 
-void gemv_carve(void* ws, int T, int top_k, int H, int I, GemvBuffers* gb) {
-  const size_t P = (size_t)T * top_k;
+void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb) {
+  const GemvLayout g = gemv_layout(T, top_k, E, H, I);
   char* q = static_cast<char*>(ws);
-  gb->xs_gu = reinterpret_cast<uint32_t*>(q); q += al(P * 2 * H * 4);
-  gb->xs_gu_inv = reinterpret_cast<float*>(q); q += al(P * 2 * 4);
-  gb->h = reinterpret_cast<float*>(q); q += al(P * I * 4);
-  gb->xs_d = reinterpret_cast<uint32_t*>(q); q += al(P * I * 4);
-  gb->xs_d_inv = reinterpret_cast<float*>(q); q += al(P * 4);
-  gb->r = reinterpret_cast<float*>(q);
+  gb->xs_gu = reinterpret_cast<uint32_t*>(q + g.xs_gu);
+  gb->xs_gu_inv = reinterpret_cast<float*>(q + g.xs_gu_inv);
+  gb->h = reinterpret_cast<float*>(q + g.h);
+  gb->xs_d = reinterpret_cast<uint32_t*>(q + g.xs_d);
+  gb->xs_d_inv = reinterpret_cast<float*>(q + g.xs_d_inv);
+  gb->r = reinterpret_cast<float*>(q + g.r);
+  gb->partial = reinterpret_cast<float*>(q + g.partial);
+  gb->counters = reinterpret_cast<int32_t*>(q + g.counters);
+  gb->n_counters = g.n_counters;
+  gb->ns_gu = g.ns_gu;
+  gb->ns_d = g.ns_d;
 }
 
 cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
@@ -310,30 +529,33 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     if (ev && ev[i]) record_stage_event(ev[i], st);
   };
   const int P = T * top_k;
-  const int slots = P < L.E ? P : L.E;
+  const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
-  gather_xs_kernel<<<P, 256, 0, st>>>(x, x_bf16, L.H, top_k, rb.seg_pairs, rb.ids, L.suh[0],
-                                      L.suh[1], gb.xs_gu, gb.xs_gu_inv);
+  if ((err = cudaMemsetAsync(gb.counters, 0, gb.n_counters * sizeof(int32_t), st)) != cudaSuccess)
+    return err;
+  gather_xs_kernel<<<P, 256, 0, st>>>(x, x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], gb.xs_gu,
+                                      gb.xs_gu_inv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(2);
 
+  // gate and up share one launch, so they share a width (checked at create)
   GemvParams gu{};
   gu.codes[0] = L.codes[0]; gu.codes[1] = L.codes[1];
   gu.stride[0] = L.code_stride[0]; gu.stride[1] = L.code_stride[1];
   gu.in = L.H; gu.out = L.I; gu.mult = L.mult;
   gu.svh[0] = L.svh[0]; gu.svh[1] = L.svh[1];
   gu.xs = gb.xs_gu; gu.xs_inv = gb.xs_gu_inv;
-  gu.seg_offsets = rb.seg_offsets; gu.active = rb.active; gu.seg_pairs = rb.seg_pairs;
-  gu.wts = rb.w; gu.h_out = gb.h;
-  // gate and up share one launch, so they must share a width
-  if (L.K[0] != L.K[1]) return cudaErrorInvalidValue;
-  if ((err = dispatch_gemv<2>(L.K[0], L.fp8, gu, slots * (L.I / 128), st)) != cudaSuccess)
+  gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
+  gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.h_out = gb.h;
+  gu.partial = gb.partial; gu.counters = gb.counters; gu.status = rb.status;
+  gu.nsplit = gb.ns_gu;
+  if ((err = dispatch_gemv<2>(L.K[0], L.fp8, gu, (int)(G * (L.I / 128) * gu.nsplit), st)) !=
+      cudaSuccess)
     return err;
   rec(3);
 
-  prep_down_kernel<<<P, 256, 0, st>>>(gb.h, L.I, rb.seg_pairs, rb.ids, L.suh[2], gb.xs_d,
-                                      gb.xs_d_inv);
+  prep_down_kernel<<<P, 256, 0, st>>>(gb.h, L.I, rb, L.suh[2], gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(4);
@@ -343,9 +565,11 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   dn.in = L.I; dn.out = L.H; dn.mult = L.mult;
   dn.svh[0] = L.svh[2];
   dn.xs = gb.xs_d; dn.xs_inv = gb.xs_d_inv;
-  dn.seg_offsets = rb.seg_offsets; dn.active = rb.active; dn.seg_pairs = rb.seg_pairs;
-  dn.wts = rb.w; dn.r_out = gb.r;
-  err = dispatch_gemv<1>(L.K[2], L.fp8, dn, slots * (L.H / 128), st);
+  dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
+  dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r;
+  dn.partial = gb.partial; dn.counters = gb.counters; dn.status = rb.status;
+  dn.nsplit = gb.ns_d;
+  err = dispatch_gemv<1>(L.K[2], L.fp8, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
   rec(5);
   return err;
 }

@@ -106,6 +106,19 @@ __device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
   return res;
 }
 
+// Token groups of one expert: kGroup consecutive positions of its segment.
+__device__ __forceinline__ void write_groups(const RouteBuffers& rb, int e, int off, int cnt,
+                                             int goff) {
+  rb.group_off[e] = goff;
+  for (int j = 0; j * kGroup < cnt; j++) {
+    int32_t* gr = rb.groups + (size_t)(goff + j) * 4;
+    gr[0] = e;
+    gr[1] = off + j * kGroup;
+    gr[2] = min(kGroup, cnt - j * kGroup);
+    gr[3] = 0;
+  }
+}
+
 // Per-chunk stage: top-k of kRouteChunk tokens, local stable ranks and
 // per-expert counts.  With `fused` (single chunk) it also finishes the
 // tables: offsets, active list and scatter.
@@ -154,17 +167,21 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
     return;
   }
   // fused: offsets = exclusive scan of the counts, active list, scatter
-  int total = 0, n_act = 0;
+  int total = 0, n_act = 0, n_grp = 0;
   const int cnt = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
   const int off = block_exclusive_scan(cnt, s_warp, &total);
   const int aidx = block_exclusive_scan(cnt > 0 ? 1 : 0, s_warp, &n_act);
+  const int ng = (cnt + kGroup - 1) / kGroup;
+  const int goff = block_exclusive_scan(ng, s_warp, &n_grp);
   if (threadIdx.x < E) {
     rb.seg_offsets[threadIdx.x] = off;
     if (cnt > 0) rb.active[1 + aidx] = threadIdx.x;
+    write_groups(rb, threadIdx.x, off, cnt, goff);
   }
   if (threadIdx.x == 0) {
     rb.seg_offsets[E] = total;
     rb.active[0] = n_act;
+    rb.group_off[E] = n_grp;
   }
   __syncthreads();
   if (threadIdx.x < E) s_cnt[threadIdx.x] = off;  // segment starts
@@ -191,17 +208,21 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, Ro
       tot += v;
     }
   }
-  int total = 0, n_act = 0;
+  int total = 0, n_act = 0, n_grp = 0;
   const int off = block_exclusive_scan(tot, s_warp, &total);
   const int aidx = block_exclusive_scan(tot > 0 ? 1 : 0, s_warp, &n_act);
+  const int ng = (tot + kGroup - 1) / kGroup;
+  const int goff = block_exclusive_scan(ng, s_warp, &n_grp);
   if (e < E) {
     rb.seg_offsets[e] = off;
     if (tot > 0) rb.active[1 + aidx] = e;
     for (int c = 0; c < nchunks; c++) rb.chunk_counts[(size_t)c * E + e] += off;
+    write_groups(rb, e, off, tot, goff);
   }
   if (threadIdx.x == 0) {
     rb.seg_offsets[E] = total;
     rb.active[0] = n_act;
+    rb.group_off[E] = n_grp;
   }
 }
 
@@ -223,7 +244,10 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 }
 
 __global__ void route_empty_kernel(int E, RouteBuffers rb) {
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) rb.seg_offsets[e] = 0;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    rb.seg_offsets[e] = 0;
+    rb.group_off[e] = 0;
+  }
   if (threadIdx.x == 0) rb.active[0] = 0;
 }
 
@@ -249,6 +273,8 @@ size_t route_scratch_bytes(int T, int E, int top_k) {
   b += align256(sizeof(int32_t) * (E + 1));      // active
   b += align256(sizeof(int32_t) * nchunks * E);  // chunk counts
   b += align256(sizeof(int32_t) * P);            // rank
+  b += align256(sizeof(int32_t) * (E + 1));      // group_off
+  b += align256(sizeof(int32_t) * 4 * max_groups(T, E, top_k));  // groups
   return b;
 }
 
@@ -265,6 +291,10 @@ void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb) {
   rb->chunk_counts = reinterpret_cast<int32_t*>(p);
   p += align256(sizeof(int32_t) * nchunks * E);
   rb->rank = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * P);
+  rb->group_off = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (E + 1));
+  rb->groups = reinterpret_cast<int32_t*>(p);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBuffers& rb,
