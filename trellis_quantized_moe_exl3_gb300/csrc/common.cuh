@@ -58,6 +58,25 @@ struct LaneWords {
   uint32_t w[2 * K + 1];
 };
 
+// 32-bit window of the lane stream starting at bit o (o compile-time after
+// unrolling); bits beyond the stream read as 0.
+template <int K>
+__device__ __forceinline__ uint32_t lane_window32(const LaneWords<K>& lw, int o) {
+  const int wi = o >> 5;
+  const int sh = o & 31;
+  const uint32_t lo = lw.w[wi];
+  const uint32_t hi = (wi + 1 < 2 * K + 1) ? lw.w[wi + 1] : 0u;
+  return sh == 0 ? lo : __funnelshift_r(lo, hi, sh);
+}
+
+// An opaque register copy of a constant, so that a multiply by it stays an
+// integer multiply-add (FMA pipe) instead of being rewritten as shifts.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
+  uint32_t r;
+  asm("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
 // State of lane-local weight u (0..63): bits [uK, uK+16) of the lane stream.
 // u is a compile-time constant after unrolling, so this is one funnel shift
 // (or plain shift) and one mask.
@@ -79,6 +98,27 @@ __device__ __forceinline__ uint32_t lane_state(const LaneWords<K>& lw, int u) {
 // mcg codebook before the final add: the two fp16 halves {a (low), b (high)}.
 __device__ __forceinline__ uint32_t mcg_halves(uint32_t s, uint32_t mult) {
   return ((s * mult) & kMcgMask) ^ kMcgXor;
+}
+
+// {a, b} halves of lane-local weight u.  For K = 2 and 4 the 16 bits above a
+// weight's state are exactly the state of weight u + 16/K, so instead of
+// masking the window to 16 bits the hash of the whole 32-bit window is taken
+// and corrected: (s + 2^16 g) * M - ((g * M) << 16) = s * M (mod 2^32), where
+// the low 16 bits of g * M are those of the next window's hash.  This trades
+// two ALU-pipe operations (shift, mask) for one FMA-pipe multiply-add.  For
+// K = 3 the window is masked.
+template <int K>
+__device__ __forceinline__ uint32_t lane_halves(const LaneWords<K>& lw, int u, uint32_t mult,
+                                                uint32_t neg_shift16) {
+  if constexpr (K == 2 || K == 4) {
+    constexpr int step = 16 / K;
+    const uint32_t xa = lane_window32<K>(lw, u * K) * mult;
+    const uint32_t xb = lane_window32<K>(lw, (u + step) * K) * mult;
+    const uint32_t x = xb * neg_shift16 + xa;
+    return (x & kMcgMask) ^ kMcgXor;
+  } else {
+    return mcg_halves(lane_state<K>(lw, u), mult);
+  }
 }
 
 // fp16 RNE of a + b for two weights at once: {a0,b0},{a1,b1} -> {v0,v1}.

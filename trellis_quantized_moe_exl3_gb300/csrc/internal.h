@@ -82,7 +82,7 @@ cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int ap
 struct GemvBuffers {
   uint32_t* xs_gu;   // [group][2][H/16][8][16] fp16x2 (dup), permuted per 16-block
   float* xs_gu_inv;  // [P][2]
-  float* h;          // [P][I] fp32 (pair-sorted rows)
+  float* gu;         // [2][P][I] fp32 gate and up outputs (pair-sorted rows)
   uint32_t* xs_d;    // [group][I/16][8][16] fp16x2 (dup), permuted
   float* xs_d_inv;   // [P]
   float* r;          // [P][H] fp32 rows by pair id

@@ -6,19 +6,21 @@
 // EXL3 for 2x DGX Sparks", section Cold prefill (E3): gather, gate/up +
 // SwiGLU, down + scatter, driven by device-side segment tables.
 //
-// Work item = (token group of <= 8 positions of one expert, 128-output strip,
-// K split).  A persistent grid walks the items.  Per CTA one producer warp
-// streams, with bulk copies (TMA engine) into a ring of shared-memory stages,
-// the code rows of the strip (8 consecutive tiles per 16-input block) and the
-// matching activation rows (8 tokens x 16 inputs); 8 consumer warps each take
-// one block of a stage: every lane loads its 8K bytes of a tile (the 16-K bit
-// window overlap comes from the next lane of the quad by shuffle), decodes 64
-// weights in registers and feeds mma.m16n8k16 with the K dimension doubled:
-// the A register of weight (o, i) is the codebook's {a, b} fp16 pair itself
-// and the B register holds {x_i, x_i}, so the tensor core forms (a + b) x_i
-// with no separate add.  (The exact a + b differs from the format's
-// fp16(a + b) by at most half an fp16 ulp; with the E4M3 rule the rounded
-// value is formed first and placed as {v, 0}.)
+// Work item = (token group of <= 8 positions of one expert, projection,
+// 128-output strip, K split).  A persistent grid walks the items.  Each of
+// the 8 warps of a CTA takes every 8th 16-input block of the item and runs its
+// own asynchronous-copy ring (cp.async, 16 bytes per lane, several blocks
+// ahead, across item boundaries): per block the code row of the strip (8
+// consecutive tiles, 8K bytes per lane) and the matching activation rows
+// (8 tokens x 16 inputs).  Every lane then decodes its 64 weights in
+// registers (the 16-K bit window overlap comes from the next lane of the quad
+// by shuffle) and feeds mma.m16n8k16 with the K dimension doubled: the A
+// register of weight (o, i) is the codebook's {a, b} fp16 pair itself and the
+// B register holds {x_i, x_i}, so the tensor core forms (a + b) x_i with no
+// separate add.  (The exact a + b differs from the format's fp16(a + b) by at
+// most half an fp16 ulp; with the E4M3 rule the rounded value is formed first
+// and placed as {v, 0}.)  Gate and up are separate items; SwiGLU runs in the
+// down projection's input pass.
 //
 // Partial sums of the 8 warps are added in a fixed tree order in shared
 // memory; K splits write their partials to the workspace and the CTA that
@@ -36,18 +38,18 @@ namespace exl3 {
 
 namespace {
 
-constexpr int kCW = 8;                     // consumer warps per CTA
-constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
+constexpr int kCW = 8;                     // warps per CTA
+constexpr int kThreads = kCW * 32;
 constexpr int kXsChunk = kGroup * 16 * 4;  // 8 tokens x 16 inputs x fp16x2
 
-template <int K, int NPROJ>
+template <int K>
 struct Cfg {
   static constexpr int kCodeChunk = 8 * 32 * K;  // 8 tiles of one 16-input block
-  static constexpr int kStageBytes = kCW * NPROJ * (kCodeChunk + kXsChunk);
-  static constexpr int kStages = (NPROJ == 2 && K >= 3) ? 3 : 4;
-  static constexpr int kRedBytes = 4 * NPROJ * 1024 * 4;  // half the warps spill at a time
-  static constexpr int kBarOff = kStages * kStageBytes + kRedBytes;
-  static constexpr int kSmem = kBarOff + 2 * kStages * 8;
+  static constexpr int kSlot = kCodeChunk + kXsChunk;
+  static constexpr int kStages = K == 2 ? 6 : (K == 3 ? 5 : 4);  // per-warp ring depth
+  static constexpr int kWarpRing = kStages * kSlot;
+  static constexpr int kRedOff = kCW * kWarpRing;
+  static constexpr int kSmem = kRedOff + 4 * 1024 * 4;  // tree-reduction buffer
 };
 
 __device__ __forceinline__ float block_max(float v, float* s_tmp) {
@@ -122,9 +124,10 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   }
 }
 
-// h rows (by position) times suh of down, scaled, group-interleaved.
-__global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ h, int I,
-                                                        RouteBuffers rb,
+// h = silu(g) * u for each position's row, times suh of down, scaled,
+// group-interleaved (the down projection's B operand).
+__global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, size_t n_pos,
+                                                        int I, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
@@ -134,33 +137,35 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
   int g, slot;
   group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
   const uint16_t* sd = suh_d + (size_t)e * I;
-  const float* hr = h + (size_t)pos * I;
+  const float* gr = gu + (size_t)pos * I;
+  const float* ur = gu + (n_pos + pos) * I;
   float am = 0.0f;
   for (int idx = threadIdx.x; idx < I; idx += blockDim.x)
-    am = fmaxf(am, fabsf(hr[idx] * __half2float(__ushort_as_half(sd[idx]))));
+    am = fmaxf(am, fabsf(silu_f(gr[idx]) * ur[idx] * __half2float(__ushort_as_half(sd[idx]))));
   am = block_max(am, s_tmp);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
   uint32_t* o = xs + (size_t)g * (I / 16) * kXsChunk / 4;
   for (int idx = threadIdx.x; idx < I; idx += blockDim.x)
     o[((size_t)(idx >> 4) * kGroup + slot) * 16 + perm_slot(idx)] =
-        dup_f16(hr[idx] * __half2float(__ushort_as_half(sd[idx])) * sc);
+        dup_f16(silu_f(gr[idx]) * ur[idx] * __half2float(__ushort_as_half(sd[idx])) * sc);
   if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex);
 }
 
 template <int K, int FP8>
 __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& b,
                                            float (&acc)[8][4], uint32_t mult) {
+  const uint32_t neg16 = opaque_u32(0xFFFF0000u);
 #pragma unroll
   for (int r0 = 0; r0 < 8; r0++) {
 #pragma unroll
     for (int hf = 0; hf < 2; hf++) {
       const int u = 8 * r0 + 4 * hf;
       uint32_t a0, a1, a2, a3;
-      const uint32_t m0 = mcg_halves(lane_state<K>(lw, u + 0), mult);
-      const uint32_t m1 = mcg_halves(lane_state<K>(lw, u + 1), mult);
-      const uint32_t m2 = mcg_halves(lane_state<K>(lw, u + 2), mult);
-      const uint32_t m3 = mcg_halves(lane_state<K>(lw, u + 3), mult);
+      const uint32_t m0 = lane_halves<K>(lw, u + 0, mult, neg16);
+      const uint32_t m1 = lane_halves<K>(lw, u + 1, mult, neg16);
+      const uint32_t m2 = lane_halves<K>(lw, u + 2, mult, neg16);
+      const uint32_t m3 = lane_halves<K>(lw, u + 3, mult, neg16);
       if (!FP8) {
         a0 = m0; a1 = m1; a2 = m2; a3 = m3;
       } else {
@@ -197,176 +202,143 @@ struct GemvParams {
   const uint16_t* codes[2];
   size_t stride[2];        // uint16 words per expert
   int in, out;
+  int nproj;               // projections in this launch (2: gate and up)
   uint32_t mult;
   const uint16_t* svh[2];  // [E][out]
-  const uint32_t* xs;      // [group][NPROJ][in/16][8][16] fp16x2
-  const float* xs_inv;     // [pos][NPROJ]
+  const uint32_t* xs;      // [group][nproj][in/16][8][16] fp16x2
+  const float* xs_inv;     // [pos][nproj]
   const int32_t* groups;   // [g][4] {expert, pos0, count, 0}
   const int32_t* n_groups; // device scalar
   const int32_t* seg_pairs;
-  const float* wts;        // router weights by pair id
-  float* h_out;            // NPROJ == 2: [pos][out]
-  float* r_out;            // NPROJ == 1: [pair id][out]
-  float* partial;          // [group][strip][nsplit][NPROJ][1024]
-  int32_t* counters;       // [group][strip], zero on entry, left zero
+  const float* wts;        // router weights by pair id (down launch)
+  float* gu_out;           // gate/up launch: [proj][pos][out]
+  float* r_out;            // down launch: [pair id][out]
+  float* partial;          // [group][nproj][strip][nsplit][1024]
+  int32_t* counters;       // [group][nproj][strip], zero on entry, left zero
   int32_t* status;
   int nsplit;
+  size_t n_pos;            // positions (row count of gu_out per projection)
 };
 
-template <int K, int FP8, int NPROJ>
-__global__ void __maxnreg__(112) gemv_kernel(GemvParams p) {
-  using C = Cfg<K, NPROJ>;
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int K, int FP8>
+__global__ void __launch_bounds__(kThreads, 3) gemv_kernel(GemvParams p) {
+  using C = Cfg<K>;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* empty = full + C::kStages;
-  float* red = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
-  __shared__ int s_abort, s_stop;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; s++) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
-    }
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
+  uint8_t* ring = smem + warp * C::kWarpRing;
+  float* red = reinterpret_cast<float*>(smem + C::kRedOff);
   const int strips = p.out / 128;
   const int nblk = p.in / 16;
-  const int bps = nblk / p.nsplit;
-  const int stages_per_item = bps / kCW;
-  const int n_items = p.n_groups[0] * strips * p.nsplit;
+  const int bps = nblk / p.nsplit;   // blocks per item
+  const int bpw = bps / kCW;         // blocks per warp per item
+  const int n_items = p.n_groups[0] * p.nproj * p.nsplit * strips;
+  const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int n_jobs = my_items * bpw;  // this warp's blocks, across its items
   const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
 
-  if (warp == kCW) {
-    // ------------------------------------------------------------ producer
-    int r = 0;
-    uint32_t ph = 0;
-    int issued = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int s = item % strips;
-      const int gq = item / strips;
-      const int q = gq % p.nsplit, g = gq / p.nsplit;
-      const int e = p.groups[4 * g];
-      for (int st = 0; st < stages_per_item; st++) {
-        if (!mbar_wait_bounded(&empty[r], ph ^ 1)) {
-          atomicOr(p.status, kStatusTimeout);
-          s_abort = 1;
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[r], C::kStageBytes);
-        __syncwarp();
-        if (lane < 2 * NPROJ * kCW) {
-          const int kind = lane & 1, pj = (lane >> 1) % NPROJ, w = (lane >> 1) / NPROJ;
-          const int blk = q * bps + st * kCW + w;
-          uint8_t* stage = smem + (size_t)r * C::kStageBytes;
-          if (kind == 0) {
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
-                                 (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
-            bulk_g2s(stage + (w * NPROJ + pj) * C::kCodeChunk, src, C::kCodeChunk, &full[r]);
-          } else {
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xs) +
-                                 (((size_t)g * NPROJ + pj) * nblk + blk) * kXsChunk;
-            bulk_g2s(stage + kCW * NPROJ * C::kCodeChunk + (w * NPROJ + pj) * kXsChunk, src,
-                     kXsChunk, &full[r]);
-          }
-        }
-        issued++;
-        if (++r == C::kStages) {
-          r = 0;
-          ph ^= 1;
-        }
-      }
+  // item id -> (group, projection, split, strip); consecutive ids are
+  // neighbouring strips, so concurrent CTAs read adjacent code bytes
+  auto item_of = [&](int it, int& g, int& pj, int& q, int& s) {
+    s = it % strips;
+    int r = it / strips;
+    q = r % p.nsplit;
+    r /= p.nsplit;
+    pj = r % p.nproj;
+    g = r / p.nproj;
+  };
+  // copy the data of this warp's job j into ring slot j % kStages
+  auto issue = [&](int j) {
+    const int it = blockIdx.x + (j / bpw) * gridDim.x;
+    int g, pj, q, s;
+    item_of(it, g, pj, q, s);
+    const int e = p.groups[4 * g];
+    const int blk = q * bps + (j % bpw) * kCW + warp;
+    uint8_t* slot = ring + (j % C::kStages) * C::kSlot;
+    const uint8_t* cs = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
+                        (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
+#pragma unroll
+    for (int c = 0; c < (C::kCodeChunk + 511) / 512; c++)
+      if (c * 512 + lane * 16 < C::kCodeChunk) cp_async16(slot + c * 512 + lane * 16, cs + c * 512 + lane * 16);
+    // activation rows: lane l copies 16 bytes of token slot l / 4; slots the
+    // group does not fill are left alone (their MMA columns are discarded)
+    if ((lane >> 2) < p.groups[4 * g + 2]) {
+      const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(p.xs) +
+                            (((size_t)g * p.nproj + pj) * nblk + blk) * kXsChunk;
+      cp_async16(slot + C::kCodeChunk + lane * 16, xsrc + lane * 16);
     }
-    // every issued stage is consumed unless the consumers stopped early; wait
-    // (bounded) for the copies still in flight before this warp leaves
-    const int tail = issued < C::kStages ? issued : C::kStages;
-    for (int i = 0; i < tail; i++) {
-      if (--r < 0) {
-        r = C::kStages - 1;
-        ph ^= 1;
-      }
-      mbar_wait_bounded(&full[r], ph);
-    }
-    return;
+  };
+
+#pragma unroll
+  for (int j = 0; j < C::kStages - 1; j++) {
+    if (j < n_jobs) issue(j);
+    cp_async_commit();
   }
 
-  // -------------------------------------------------------------- consumers
   const int g_l = lane >> 2, c_l = lane & 3;
-  int r = 0;
-  uint32_t ph = 0;
+  int j = 0;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int s = item % strips;
-    const int gq = item / strips;
-    const int q = gq % p.nsplit, g = gq / p.nsplit;
-    float acc[NPROJ][8][4];
+    int g, pj, q, s;
+    item_of(item, g, pj, q, s);
+    const int cnt = p.groups[4 * g + 2];
+    float acc[8][4];
 #pragma unroll
-    for (int pj = 0; pj < NPROJ; pj++)
+    for (int i = 0; i < 8; i++)
 #pragma unroll
-      for (int i = 0; i < 8; i++)
-#pragma unroll
-        for (int d = 0; d < 4; d++) acc[pj][i][d] = 0.0f;
-    for (int st = 0; st < stages_per_item; st++) {
-      if (!mbar_wait_bounded(&full[r], ph)) {
-        atomicOr(p.status, kStatusTimeout);
-        s_abort = 1;
-      }
-      const uint8_t* stage = smem + (size_t)r * C::kStageBytes;
-#pragma unroll
-      for (int pj = 0; pj < NPROJ; pj++) {
-        LaneWords<K> lw;
-        lds_lane_words<K>(lw, stage + (warp * NPROJ + pj) * C::kCodeChunk + lane * 8 * K);
-        fetch_neighbour<K>(lw);
-        const uint4 b = *reinterpret_cast<const uint4*>(
-            stage + kCW * NPROJ * C::kCodeChunk + (warp * NPROJ + pj) * kXsChunk + g_l * 64 + c_l * 16);
-        decode_mma<K, FP8>(lw, b, acc[pj], p.mult);
-      }
+      for (int d = 0; d < 4; d++) acc[i][d] = 0.0f;
+    for (int b = 0; b < bpw; b++, j++) {
+      if (j + C::kStages - 1 < n_jobs) issue(j + C::kStages - 1);
+      cp_async_commit();
+      cp_async_wait<C::kStages - 1>();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[r]);
-      if (++r == C::kStages) {
-        r = 0;
-        ph ^= 1;
-      }
+      const uint8_t* slot = ring + (j % C::kStages) * C::kSlot;
+      LaneWords<K> lw;
+      lds_lane_words<K>(lw, slot + lane * 8 * K);
+      fetch_neighbour<K>(lw);
+      const uint4 bx = g_l < cnt ? *reinterpret_cast<const uint4*>(slot + C::kCodeChunk + g_l * 64 + c_l * 16)
+                                 : make_uint4(0, 0, 0, 0);
+      decode_mma<K, FP8>(lw, bx, acc, p.mult);
+      __syncwarp();  // the slot is refilled by the next iteration's issue
     }
     // fixed-order tree reduction over the 8 warps: 4+4, 2+2, 1+1
 #pragma unroll
     for (int half = 4; half >= 1; half >>= 1) {
       if (warp >= half && warp < 2 * half) {
-        float* dst = red + (size_t)(warp - half) * NPROJ * 1024;
+        float* dst = red + (size_t)(warp - half) * 1024;
 #pragma unroll
-        for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-          for (int i = 0; i < 8; i++)
-            *reinterpret_cast<float4*>(dst + pj * 1024 + (i * 32 + lane) * 4) =
-                make_float4(acc[pj][i][0], acc[pj][i][1], acc[pj][i][2], acc[pj][i][3]);
+        for (int i = 0; i < 8; i++)
+          *reinterpret_cast<float4*>(dst + (i * 32 + lane) * 4) =
+              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
       }
-      if (half == 1 && threadIdx.x == 0) s_stop = s_abort;  // one snapshot for all warps
-      named_bar_sync(1, kCW * 32);
+      __syncthreads();
       if (warp < half) {
-        const float* src = red + (size_t)warp * NPROJ * 1024;
+        const float* src = red + (size_t)warp * 1024;
 #pragma unroll
-        for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const float4 v = *reinterpret_cast<const float4*>(src + pj * 1024 + (i * 32 + lane) * 4);
-            acc[pj][i][0] += v.x; acc[pj][i][1] += v.y; acc[pj][i][2] += v.z; acc[pj][i][3] += v.w;
-          }
+        for (int i = 0; i < 8; i++) {
+          const float4 v = *reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4);
+          acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
+        }
       }
-      named_bar_sync(1, kCW * 32);
+      __syncthreads();
     }
     if (warp == 0) {
       bool do_epi = true;
       if (p.nsplit > 1) {
-        const size_t slot = (size_t)g * strips + s;
-        float* mine = p.partial + ((slot * p.nsplit + q) * NPROJ) * 1024;
+        const size_t slot = ((size_t)g * p.nproj + pj) * strips + s;
+        float* mine = p.partial + (slot * p.nsplit + q) * 1024;
 #pragma unroll
-        for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-          for (int i = 0; i < 8; i++)
-            *reinterpret_cast<float4*>(mine + pj * 1024 + (i * 32 + lane) * 4) =
-                make_float4(acc[pj][i][0], acc[pj][i][1], acc[pj][i][2], acc[pj][i][3]);
+        for (int i = 0; i < 8; i++)
+          *reinterpret_cast<float4*>(mine + (i * 32 + lane) * 4) =
+              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         __threadfence();
         __syncwarp();
         int last = 0;
@@ -376,21 +348,16 @@ __global__ void __maxnreg__(112) gemv_kernel(GemvParams p) {
         if (last) {
           __threadfence();
 #pragma unroll
-          for (int pj = 0; pj < NPROJ; pj++)
+          for (int i = 0; i < 8; i++)
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-#pragma unroll
-              for (int d = 0; d < 4; d++) acc[pj][i][d] = 0.0f;
+            for (int d = 0; d < 4; d++) acc[i][d] = 0.0f;
           for (int qq = 0; qq < p.nsplit; qq++) {
-            const float* src = p.partial + ((slot * p.nsplit + qq) * NPROJ) * 1024;
+            const float* src = p.partial + (slot * p.nsplit + qq) * 1024;
 #pragma unroll
-            for (int pj = 0; pj < NPROJ; pj++)
-#pragma unroll
-              for (int i = 0; i < 8; i++) {
-                const float4 v =
-                    __ldcg(reinterpret_cast<const float4*>(src + pj * 1024 + (i * 32 + lane) * 4));
-                acc[pj][i][0] += v.x; acc[pj][i][1] += v.y; acc[pj][i][2] += v.z; acc[pj][i][3] += v.w;
-              }
+            for (int i = 0; i < 8; i++) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4));
+              acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
+            }
           }
           if (lane == 0) p.counters[slot] = 0;
         }
@@ -405,33 +372,32 @@ __global__ void __maxnreg__(112) gemv_kernel(GemvParams p) {
             const int n = 2 * c_l + (d & 1);
             if (n < cnt) {
               const int pos = pos0 + n;
-              if constexpr (NPROJ == 2) {
-                const float G = acc[0][i][d] * p.xs_inv[2 * pos] *
-                                __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o]));
-                const float U = acc[1][i][d] * p.xs_inv[2 * pos + 1] *
-                                __half2float(__ushort_as_half(p.svh[1][(size_t)e * p.out + o]));
-                p.h_out[(size_t)pos * p.out + o] = silu_f(G) * U;
+              const float v = acc[i][d] * p.xs_inv[(size_t)pos * p.nproj + pj] *
+                              __half2float(__ushort_as_half(p.svh[pj][(size_t)e * p.out + o]));
+              if (p.gu_out) {
+                p.gu_out[((size_t)pj * p.n_pos + pos) * p.out + o] = v;
               } else {
                 const int pid = p.seg_pairs[pos];
-                p.r_out[(size_t)pid * p.out + o] =
-                    acc[0][i][d] * p.xs_inv[pos] *
-                    __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o])) * p.wts[pid];
+                p.r_out[(size_t)pid * p.out + o] = v * p.wts[pid];
               }
             }
           }
       }
     }
-    if (s_stop) break;  // uniform: written before the item's last barrier pair
   }
+  cp_async_wait<0>();
 }
 
-template <int K, int FP8, int NPROJ>
+template <int K, int FP8>
 cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
-  using C = Cfg<K, NPROJ>;
+  using C = Cfg<K>;
   static int occ = -1, sms = 0;
-  auto kfn = gemv_kernel<K, FP8, NPROJ>;
+  auto kfn = gemv_kernel<K, FP8>;
   if (occ < 0) {
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -448,24 +414,23 @@ cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int NPROJ>
 cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int items_ub, cudaStream_t st) {
   if (fp8) {
-    if (K == 2) return launch_gemv<2, 1, NPROJ>(gp, items_ub, st);
-    if (K == 3) return launch_gemv<3, 1, NPROJ>(gp, items_ub, st);
-    return launch_gemv<4, 1, NPROJ>(gp, items_ub, st);
+    if (K == 2) return launch_gemv<2, 1>(gp, items_ub, st);
+    if (K == 3) return launch_gemv<3, 1>(gp, items_ub, st);
+    return launch_gemv<4, 1>(gp, items_ub, st);
   }
-  if (K == 2) return launch_gemv<2, 0, NPROJ>(gp, items_ub, st);
-  if (K == 3) return launch_gemv<3, 0, NPROJ>(gp, items_ub, st);
-  return launch_gemv<4, 0, NPROJ>(gp, items_ub, st);
+  if (K == 2) return launch_gemv<2, 0>(gp, items_ub, st);
+  if (K == 3) return launch_gemv<3, 0>(gp, items_ub, st);
+  return launch_gemv<4, 0>(gp, items_ub, st);
 }
 
-// K splits: double while each split keeps >= 2 stages of blocks and the
-// upper bound on items stays below ~6 per CTA slot (2 CTAs on 152 SMs).
-int choose_nsplit(size_t groups_ub, int strips, int nblk) {
+// K splits: double while every warp keeps >= 2 blocks per item and the upper
+// bound on items stays below ~6 per CTA slot (3 CTAs on 152 SMs).
+int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
   int ns = 1;
-  while (ns < 8 && nblk % (2 * ns * kCW) == 0 && nblk / (2 * ns) >= 2 * kCW &&
-         groups_ub * strips * ns < (size_t)6 * 304)
+  while (ns < 8 && nblk % (2 * ns * kCW) == 0 && nblk / (2 * ns * kCW) >= 2 &&
+         groups_ub * items_per_group * ns < (size_t)6 * 456)
     ns *= 2;
   return ns;
 }
@@ -473,7 +438,7 @@ int choose_nsplit(size_t groups_ub, int strips, int nblk) {
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct GemvLayout {
-  size_t xs_gu, xs_gu_inv, h, xs_d, xs_d_inv, r, partial, counters, total;
+  size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, partial, counters, total;
   int ns_gu, ns_d;
   size_t n_counters;
 };
@@ -482,15 +447,15 @@ GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
   GemvLayout g{};
   const size_t P = (size_t)T * top_k;
   const size_t G = max_groups(T, E, top_k);
-  g.ns_gu = choose_nsplit(G, I / 128, H / 16);
+  g.ns_gu = choose_nsplit(G, 2 * (I / 128), H / 16);
   g.ns_d = choose_nsplit(G, H / 128, I / 16);
-  const size_t part_gu = g.ns_gu > 1 ? G * (I / 128) * g.ns_gu * 2 * 1024 * 4 : 0;
+  const size_t part_gu = g.ns_gu > 1 ? G * 2 * (I / 128) * g.ns_gu * 1024 * 4 : 0;
   const size_t part_d = g.ns_d > 1 ? G * (H / 128) * g.ns_d * 1024 * 4 : 0;
-  g.n_counters = G * ((I > H ? I : H) / 128);
+  g.n_counters = G * (2 * (I / 128) > H / 128 ? 2 * (I / 128) : H / 128);
   size_t o = 0;
   g.xs_gu = o; o += al(G * 2 * (H / 16) * kXsChunk);
   g.xs_gu_inv = o; o += al(P * 2 * 4);
-  g.h = o; o += al(P * I * 4);
+  g.gu = o; o += al(2 * P * I * 4);
   g.xs_d = o; o += al(G * (I / 16) * kXsChunk);
   g.xs_d_inv = o; o += al(P * 4);
   g.r = o; o += al(P * H * 4);
@@ -511,7 +476,7 @@ void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb
   char* q = static_cast<char*>(ws);
   gb->xs_gu = reinterpret_cast<uint32_t*>(q + g.xs_gu);
   gb->xs_gu_inv = reinterpret_cast<float*>(q + g.xs_gu_inv);
-  gb->h = reinterpret_cast<float*>(q + g.h);
+  gb->gu = reinterpret_cast<float*>(q + g.gu);
   gb->xs_d = reinterpret_cast<uint32_t*>(q + g.xs_d);
   gb->xs_d_inv = reinterpret_cast<float*>(q + g.xs_d_inv);
   gb->r = reinterpret_cast<float*>(q + g.r);
@@ -543,33 +508,33 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   GemvParams gu{};
   gu.codes[0] = L.codes[0]; gu.codes[1] = L.codes[1];
   gu.stride[0] = L.code_stride[0]; gu.stride[1] = L.code_stride[1];
-  gu.in = L.H; gu.out = L.I; gu.mult = L.mult;
+  gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
   gu.svh[0] = L.svh[0]; gu.svh[1] = L.svh[1];
   gu.xs = gb.xs_gu; gu.xs_inv = gb.xs_gu_inv;
   gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
-  gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.h_out = gb.h;
+  gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.gu_out = gb.gu; gu.n_pos = (size_t)P;
   gu.partial = gb.partial; gu.counters = gb.counters; gu.status = rb.status;
   gu.nsplit = gb.ns_gu;
-  if ((err = dispatch_gemv<2>(L.K[0], L.fp8, gu, (int)(G * (L.I / 128) * gu.nsplit), st)) !=
+  if ((err = dispatch_gemv(L.K[0], L.fp8, gu, (int)(G * 2 * (L.I / 128) * gu.nsplit), st)) !=
       cudaSuccess)
     return err;
   rec(3);
 
-  prep_down_kernel<<<P, 256, 0, st>>>(gb.h, L.I, rb, L.suh[2], gb.xs_d, gb.xs_d_inv);
+  prep_down_kernel<<<P, 256, 0, st>>>(gb.gu, (size_t)P, L.I, rb, L.suh[2], gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(4);
 
   GemvParams dn{};
   dn.codes[0] = L.codes[2]; dn.stride[0] = L.code_stride[2];
-  dn.in = L.I; dn.out = L.H; dn.mult = L.mult;
+  dn.in = L.I; dn.out = L.H; dn.nproj = 1; dn.mult = L.mult;
   dn.svh[0] = L.svh[2];
   dn.xs = gb.xs_d; dn.xs_inv = gb.xs_d_inv;
   dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r;
   dn.partial = gb.partial; dn.counters = gb.counters; dn.status = rb.status;
   dn.nsplit = gb.ns_d;
-  err = dispatch_gemv<1>(L.K[2], L.fp8, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
+  err = dispatch_gemv(L.K[2], L.fp8, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
   rec(5);
   return err;
 }
