@@ -252,12 +252,19 @@ def test_prefill_workload_sampled():
 
 
 def test_long_workload_sampled():
-    """Four stacked layers (K2, K3, K2, K4) with pre-RMSNorm and residual."""
+    """Four stacked layers (K2, K3, K2, K4) with pre-RMSNorm and residual.
+
+    The layer tolerance applies to each layer's output, so every layer is
+    checked on the same input on both sides: the oracle takes the GPU's bf16
+    residual x_l for the sampled tokens and computes x_{l+1} = bf16(x_l +
+    MoE(bf16(rmsnorm(x_l)))).  An independent 4-layer oracle chain is also
+    compared end to end against a compounded bound (each layer's bf16
+    re-rounding and the roughly quadratic layer amplify differences)."""
     wl = synth.WORKLOADS["long"]
     x0 = synth.activations(wl.seed, wl.T, 4096, "bf16")
     toks = [0, 5000, wl.T - 1]
     xt = _act(x0, "bf16")
-    x_ref = x0[toks]
+    x_chain = x0[toks]
     for li, spec in enumerate(wl.layers):
         hl = HostLayer(spec)
         layer = hl.device()
@@ -265,15 +272,21 @@ def test_long_workload_sampled():
         xn = rmsnorm(xt)
         nxt = layer.forward(xn, torch.from_numpy(logits).cuda(), wl.top_k, residual=xt)
         torch.cuda.synchronize()
-        # oracle: the same chain per sampled token
-        xr = oracle.bf16_bits_to_f64(x_ref)
-        xn_bits = np.stack([oracle.f64_to_bf16_bits(oracle.rmsnorm_row(r, 1e-6)) for r in xr])
-        y = oracle_forward_parallel(hl.oracle(), xn_bits, True, logits[toks], wl.top_k,
-                                    range(len(toks)))
-        x_ref = np.stack([oracle.f64_to_bf16_bits(r) for r in xr + y])
+        ol = hl.oracle()
+
+        def oracle_layer(x_bits):
+            xr = oracle.bf16_bits_to_f64(x_bits)
+            xn_bits = np.stack([oracle.f64_to_bf16_bits(oracle.rmsnorm_row(r, 1e-6)) for r in xr])
+            y = oracle_forward_parallel(ol, xn_bits, True, logits[toks], wl.top_k, range(len(toks)))
+            return np.stack([oracle.f64_to_bf16_bits(r) for r in xr + y])
+
+        x_in = xt.cpu().view(torch.int16).numpy().view(np.uint16)[toks]
+        ref = oracle.bf16_bits_to_f64(oracle_layer(x_in))
+        got = act_to_f64(nxt)[toks]
+        assert_layer_close(got, ref)
+        x_chain = oracle_layer(x_chain)
         xt = nxt
         del layer, hl
         torch.cuda.empty_cache()
-    got = act_to_f64(xt)[toks]
-    ref = oracle.bf16_bits_to_f64(x_ref)
-    assert_layer_close(got, ref)
+    assert_layer_close(act_to_f64(xt)[toks], oracle.bf16_bits_to_f64(x_chain), max_rel=4 * 2e-2,
+                       fro_rel=4 * 5e-3)
