@@ -137,13 +137,14 @@ def _run_small(spec, T, top_k, act, path=0, residual=False, seed=50):
     return act_to_f64(out), ref, layer
 
 
-def test_forward_tiny_workload():
+@pytest.mark.parametrize("path", [0, 2], ids=["auto", "gemm"])
+def test_forward_tiny_workload(path):
     wl = synth.WORKLOADS["tiny"]
     spec = wl.layers[0]
     hl = HostLayer(spec)
     layer = hl.device()
     x, logits = synth.workload_inputs(wl)
-    out = layer.forward(_act(x, wl.act), torch.from_numpy(logits).cuda(), wl.top_k)
+    out = layer.forward(_act(x, wl.act), torch.from_numpy(logits).cuda(), wl.top_k, path=path)
     torch.cuda.synchronize()
     ref = hl.oracle().forward(x, False, logits, wl.top_k)
     assert_layer_close(act_to_f64(out), ref)
@@ -157,11 +158,24 @@ def test_forward_tiny_workload():
     ((2, 2, 2), True, True, 1, 1, "bf16"),
     ((4, 4, 4), False, False, 64, 8, "bf16"),   # several token groups per expert
 ])
-def test_forward_small_variants(K, fp8, shared, T, k, act):
+@pytest.mark.parametrize("path", [1, 2], ids=["gemv", "gemm"])
+def test_forward_small_variants(K, fp8, shared, T, k, act, path):
     spec = synth.LayerSpec(seed=60 + sum(K), num_experts=10, hidden=384, inter=256, K=K,
                            fp8_round=fp8, shared=shared)
-    out, ref, _ = _run_small(spec, T, k, act)
+    out, ref, layer = _run_small(spec, T, k, act, path=path)
     assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_forward_gemm_multi_tile(fp8):
+    """Experts with more than 256 tokens (several tensor-core tiles, a ragged
+    last tile), all three code widths, both paths."""
+    spec = synth.LayerSpec(seed=75, num_experts=6, hidden=512, inter=384, K=(4, 4, 3), fp8_round=fp8)
+    for path in (1, 2):
+        out, ref, layer = _run_small(spec, 300, 4, "bf16", path=path)
+        assert_layer_close(out, ref)
+        assert device_status(layer.workspace(300, 4)) == 0
 
 
 def test_forward_residual():

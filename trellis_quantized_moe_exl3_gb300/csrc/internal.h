@@ -98,6 +98,14 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
                             const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,
                             cudaStream_t st);
 
+// ---- grouped GEMM path (prefill-sized steps, tcgen05)
+size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I);
+// ev (may be null): events after gather [2], gate/up [3], down input [4], down [5].
+// *r_out receives the pair-row buffer [P][H] the combine reads.
+cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
+                            const RouteBuffers& rb, void* ws, const cudaEvent_t* ev, float** r_out,
+                            cudaStream_t st);
+
 // ---- shared expert (dense fp16)
 constexpr int kSharedKPer = 128;  // rows of W per split
 size_t shared_scratch_bytes(int T, int H, int I);

@@ -37,10 +37,18 @@ exl3_status check_device() {
   return major == 10 ? EXL3_OK : EXL3_ERR_DEVICE;
 }
 
-// Forward workspace: [route scratch][ids][w][seg_offsets][seg_pairs][gemv][shared]
+// Forward workspace: [route scratch][ids][w][seg_offsets][seg_pairs][expert path][shared]
+// The expert-path region holds the larger of the GEMV and GEMM scratch.
 struct FwdLayout {
   size_t route, ids, w, off, pairs, gemv, shared, total;
 };
+
+// AUTO path: the tensor-core GEMM once an expert sees ~16 tokens on average.
+bool use_gemm(const LayerView& L, int T, int top_k, int path) {
+  if (path == EXL3_PATH_GEMV) return false;
+  if (path == EXL3_PATH_GEMM) return true;
+  return (size_t)T * top_k >= (size_t)16 * L.E;
+}
 
 FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
   FwdLayout f{};
@@ -51,7 +59,9 @@ FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
   f.w = o; o += al(P * 4);
   f.off = o; o += al((size_t)(L.E + 1) * 4);
   f.pairs = o; o += al(P * 4);
-  f.gemv = o; o += al(gemv_scratch_bytes(T, k, L.E, L.H, L.I));
+  const size_t gv = gemv_scratch_bytes(T, k, L.E, L.H, L.I);
+  const size_t gm = gemm_scratch_bytes(T, k, L.E, L.H, L.I);
+  f.gemv = o; o += al(gv > gm ? gv : gm);
   f.shared = o; o += has_shared ? al(shared_scratch_bytes(T, L.H, L.I)) : 0;
   f.total = o;
   return f;
@@ -188,9 +198,17 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (launch_route(logits, T, L.E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
   rec(1);
 
-  GemvBuffers gb{};
-  gemv_carve(base + f.gemv, T, top_k, L.E, L.H, L.I, &gb);
-  if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
+  float* pair_rows = nullptr;
+  if (use_gemm(L, T, top_k, path)) {
+    if (launch_moe_gemm(L, x, bf16, T, top_k, rb, base + f.gemv, ev, &pair_rows, st) !=
+        cudaSuccess)
+      return EXL3_ERR_CUDA;
+  } else {
+    GemvBuffers gb{};
+    gemv_carve(base + f.gemv, T, top_k, L.E, L.H, L.I, &gb);
+    if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
+    pair_rows = gb.r;
+  }
 
   const float* sp = nullptr;
   int ns = 0;
@@ -202,7 +220,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
     ns = L.I / kSharedKPer;
   }
   rec(6);
-  if (launch_combine(gb.r, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
+  if (launch_combine(pair_rows, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(7);
   return EXL3_OK;
