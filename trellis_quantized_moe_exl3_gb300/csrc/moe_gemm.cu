@@ -178,8 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int ks = 0; ks < nks; ks++) {
         const int sb = ks % kBStages;
-        if (!mbar_wait_bounded(&b_empty[sb], ((ks / kBStages) & 1) ^ 1))
-          atomicOr(p.status, kStatusTimeout);
+        mbar_wait_or_abort(&b_empty[sb], ((ks / kBStages) & 1) ^ 1, p.status);
         mbar_arrive_expect_tx(&b_full[sb], nbox * 64 * kKS * 2);
         uint8_t* dst = smem + C::kOffB + sb * kBStage;
         for (int j = 0; j < nbox; j++)
@@ -188,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the last loads were consumed by the MMA thread unless it gave up:
       // wait (bounded) for them before the CTA may exit
       for (int ks = nks - kBStages < 0 ? 0 : nks - kBStages; ks < nks; ks++)
-        mbar_wait_bounded(&b_full[ks % kBStages], (ks / kBStages) & 1);
+        mbar_wait_or_abort(&b_full[ks % kBStages], (ks / kBStages) & 1, p.status);
     }
   } else if (warp == kDec + 1) {
     // ---------------------------------------------------------------- MMA
@@ -196,9 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = umma_idesc_f16(128, n_mma, 1, 0);
       for (int ks = 0; ks < nks; ks++) {
         const int sa = ks % C::kAStages, sb = ks % kBStages;
-        bool ok = mbar_wait_bounded(&a_full[sa], (ks / C::kAStages) & 1);
-        ok = mbar_wait_bounded(&b_full[sb], (ks / kBStages) & 1) && ok;
-        if (!ok) atomicOr(p.status, kStatusTimeout);
+        mbar_wait_or_abort(&a_full[sa], (ks / C::kAStages) & 1, p.status);
+        mbar_wait_or_abort(&b_full[sb], (ks / kBStages) & 1, p.status);
         tc_fence_after();
         const uint32_t a_base = smem_u32(smem + sa * C::kAStage);
         const uint32_t b_base = smem_u32(smem + C::kOffB + sb * kBStage);
@@ -251,8 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       LaneWords<K> lw;
       lds_words<K>(lw, ring + (n % kCodeStages) * C::kCodeChunk + lane * 8 * K);
       fetch_neighbour<K>(lw);
-      if (!mbar_wait_bounded(&a_empty[sa], ((ks / C::kAStages) & 1) ^ 1))
-        atomicOr(p.status, kStatusTimeout);
+      mbar_wait_or_abort(&a_empty[sa], ((ks / C::kAStages) & 1) ^ 1, p.status);
       decode_store<K, FP8>(lw, p.mult, smem + sa * C::kAStage + pj * kAProj, blk, g, c,
                            suh_e + ks * kKS + 16 * blk);
       fence_async_smem();
@@ -262,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();
 
     // ------------------------------------------------------------- epilogue
-    if (!mbar_wait_bounded(acc_full, 0)) atomicOr(p.status, kStatusTimeout);
+    mbar_wait_or_abort(acc_full, 0, p.status);
     tc_fence_after();
     const int q4 = warp & 3, half = warp >> 2;
     const int o = 128 * s + 32 * q4 + lane;

@@ -9,7 +9,7 @@
 
 namespace exl3 {
 
-constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr long long kWaitBudgetCycles = 1000000000LL;  // ~0.5 s at 2 GHz
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,6 +52,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitBudgetCycles) return false;
+  }
+  return true;
+}
+
+// Bounded wait that also gives up as soon as any CTA has recorded a timeout
+// in the device status word (bit 4), so a stuck pipeline ends the whole grid
+// quickly instead of every CTA spending its own budget.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  int it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (((++it) & 63) == 0 && (*reinterpret_cast<volatile int32_t*>(status) & 4)) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      atomicOr(status, 4);
+      return false;
+    }
   }
   return true;
 }
