@@ -45,6 +45,7 @@ def parse():
                     help="decode (default), verify3, verify4, prefill: parity/profiling cases")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profilers)")
+    ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
     return ap.parse_args()
 
 
@@ -197,7 +198,9 @@ def pick_workload(args):
 
     from trellis_quantized_moe_exl3_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
-    spec = wl.layers[0]
+    spec = wl.layers[args.layer]
+    if args.layer:
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-layer{args.layer}")
     if args.experts:
         spec = dataclasses.replace(spec, num_experts=args.experts)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-E{args.experts}")

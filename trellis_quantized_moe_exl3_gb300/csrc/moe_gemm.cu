@@ -7,20 +7,23 @@
 // exlr8 (K2/K3/K4)", Widths: with the E4M3 codebook, prefill runs on the
 // tensor cores.
 //
-// One CTA = (token tile of <= 256 positions of one expert, 128-output strip).
-// D[o][n] = sum_i W[i][o] x[n][i] with A = decoded weights (M = 128 outputs,
-// MN-major in shared memory) and B = activation rows (N = tokens, K-major,
-// loaded by TMA with 128-byte swizzle); fp16 operands, fp32 accumulators in
-// TMEM (gate and up side by side for the first launch).
-//   warps 0-7  decode: each takes one 16-input block of the 64-input K step
-//              (gate/up: 2 projections x 4 blocks; down: 4 blocks, two K steps
-//              in flight), streams its code rows with cp.async, sums the
-//              codebook halves into fp16 (E4M3 rule if set), applies suh and
-//              stores 16-byte chunks into the swizzled A stage;
+// One CTA = (token tile of <= 512 positions of one expert, projection,
+// 128-output strip).  D[o][n] = sum_i W[i][o] x[n][i] with A = decoded
+// weights (M = 128 outputs, MN-major in shared memory) and B = activation rows
+// (N = tokens, K-major, loaded by TMA with 128-byte swizzle); fp16 operands,
+// fp32 accumulators in TMEM: two 256-column accumulators, so every decoded
+// weight serves up to 512 tokens.
+//   warps 0-7  decode: each takes one 16-input block of a 64-input K step (two
+//              K steps in flight), streams its code rows with cp.async into an
+//              interleaved (bank-conflict-free) ring, hashes each 32-bit
+//              window once, sums the codebook halves into fp16 (E4M3 rule if
+//              set), applies suh and stores 16-byte chunks into the swizzled
+//              A stage;
 //   warp 8     TMA producer of the B stages, and TMEM allocator;
 //   warp 9     one thread issues tcgen05.mma and commits stage releases.
-// The epilogue (warps 0-7) reads TMEM: gate/up -> h = silu(g) * u (fp32);
-// down -> router weight * svh * acc into the pair's own row (no atomics).
+// The epilogue (warps 0-7) reads TMEM: gate/up launch -> svh * acc per
+// position (SwiGLU follows in the down projection's input pass); down launch
+// -> router weight * svh * acc into the pair's own row (no atomics).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -32,28 +35,27 @@ namespace exl3 {
 
 namespace {
 
-constexpr int kBN = 256;   // max tokens per tile (MMA N)
-constexpr int kKS = 64;    // inputs per K step
-constexpr int kDec = 8;    // decoder warps
+constexpr int kHalfN = 256;           // tokens per TMEM accumulator (MMA N)
+constexpr int kBN = 2 * kHalfN;       // tokens per tile
+constexpr int kKS = 64;               // inputs per K step
+constexpr int kDec = 8;               // decoder warps
 constexpr int kThreads = (kDec + 2) * 32;
-constexpr int kCodeStages = 4;
-constexpr int kBStages = 3;
-constexpr int kAProj = 128 * kKS * 2;   // 16 KB: one projection's A stage
-constexpr int kBStage = kBN * kKS * 2;  // 32 KB
+constexpr int kJobs = 4;              // 16-input blocks per K step
+constexpr int kPar = kDec / kJobs;    // K steps decoded in parallel
+constexpr int kAStages = 2 * kPar;
+constexpr int kAStage = 128 * kKS * 2;        // 16 KB
+constexpr int kBStages = 2;
+constexpr int kBStage = kBN * kKS * 2;        // 64 KB
+constexpr int kCodeStages = 3;
 
-template <int K, int NPROJ>
+template <int K>
 struct GCfg {
-  static constexpr int kJobs = NPROJ * 4;          // decode jobs per K step
-  static constexpr int kPar = kDec / kJobs;        // K steps decoded in parallel
-  static constexpr int kAStages = 2 * kPar;
-  static constexpr int kAStage = NPROJ * kAProj;
   static constexpr int kCodeChunk = 8 * 32 * K;
   static constexpr int kOffB = kAStages * kAStage;
   static constexpr int kOffCode = kOffB + kBStages * kBStage;
   static constexpr int kOffBar = kOffCode + kDec * kCodeStages * kCodeChunk;
   static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
-  static constexpr int kTmemCols = NPROJ * kBN;
 };
 
 struct GemmParams {
@@ -61,13 +63,14 @@ struct GemmParams {
   size_t stride[2];         // uint16 words per expert
   const uint16_t* suh[2];   // [E][in]
   const uint16_t* svh[2];   // [E][out]
-  int in, out;
+  int in, out, nproj;
   uint32_t mult;
   const int32_t* tiles;     // [t][4] {expert, pos0, count, 0}
   const int32_t* n_tiles;
   const float* xinv;        // [pos] scale of the B rows
-  float* h_out;             // gate/up: [pos][out]
-  float* r_out;             // down: [pair id][out]
+  float* gu_out;            // gate/up launch: [proj][pos][out]
+  size_t n_pos;
+  float* r_out;             // down launch: [pair id][out]
   const int32_t* seg_pairs;
   const float* wts;
   int32_t* status;
@@ -77,87 +80,145 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Copy one code chunk (8 tiles of a 16-input block, 8K bytes per code lane)
+// into the ring slot in an interleaved order: piece q of code lane L sits at
+// (q * 32 + L) * piece, so that the per-lane loads below are conflict-free.
 template <int K>
-__device__ __forceinline__ void lds_words(LaneWords<K>& lw, const uint8_t* p) {
+__device__ __forceinline__ void copy_codes(uint8_t* dst, const uint8_t* src, int lane) {
+  if constexpr (K == 2) {
+    cp_async16(dst + lane * 16, src + lane * 16);
+  } else if constexpr (K == 3) {
 #pragma unroll
-  for (int q = 0; q < 2 * K; q += 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p + 4 * q);
-    lw.w[q] = v.x;
-    lw.w[q + 1] = v.y;
-  }
-}
-
-// Decode this lane's 64 weights of one tile and store them into the MN-major
-// A stage of one projection: lane (g, c) holds outputs 16g..16g+15 (rows of
-// the strip) for inputs c, c+4, c+8, c+12 of block `blk`.
-template <int K, int FP8>
-__device__ __forceinline__ void decode_store(const LaneWords<K>& lw, uint32_t mult, uint8_t* a_proj,
-                                             int blk, int g, int c, const uint16_t* suh_blk) {
-  const uint32_t neg16 = opaque_u32(0xFFFF0000u);
-  const int am = g >> 2;
-  const int ch0 = 2 * (g & 3);
+    for (int Q = 0; Q < 3; Q++) {
+      const int u = Q * 32 + lane;  // 8-byte unit of the chunk
+      cp_async8(dst + ((u % 3) * 32 + u / 3) * 8, src + u * 8);
+    }
+  } else {
 #pragma unroll
-  for (int hf = 0; hf < 2; hf++) {
-#pragma unroll
-    for (int jh = 0; jh < 2; jh++) {
-      const int i = c + 4 * jh + 8 * hf;
-      const int k = 16 * blk + i;
-      const uint16_t sb = __ldg(suh_blk + i);
-      const uint32_t s2 = (uint32_t)sb | ((uint32_t)sb << 16);
-#pragma unroll
-      for (int jl = 0; jl < 2; jl++) {
-        uint32_t v[4];
-#pragma unroll
-        for (int pp = 0; pp < 4; pp++) {
-          const int u0 = 16 * pp + 4 * hf + 2 * jh + jl;
-          const uint32_t m0 = lane_halves<K>(lw, u0, mult, neg16);
-          const uint32_t m1 = lane_halves<K>(lw, u0 + 8, mult, neg16);
-          uint32_t v2 = sum_halves2(m0, m1);
-          if (FP8) v2 = e4m3_round2(v2);
-          __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&v2),
-                              *reinterpret_cast<const __half2*>(&s2));
-          v[pp] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        const int off = am * 1024 + (k >> 3) * 2048 + (k & 7) * 128 + (((ch0 + jl) ^ (k & 7)) << 4);
-        *reinterpret_cast<uint4*>(a_proj + off) = make_uint4(v[0], v[1], v[2], v[3]);
-      }
+    for (int Q = 0; Q < 2; Q++) {
+      const int u = Q * 32 + lane;  // 16-byte unit of the chunk
+      cp_async16(dst + ((u & 1) * 32 + (u >> 1)) * 16, src + u * 16);
     }
   }
 }
 
-template <int K, int FP8, int NPROJ>
+template <int K>
+__device__ __forceinline__ void load_codes(LaneWords<K>& lw, const uint8_t* slot, int lane) {
+  if constexpr (K == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + lane * 16);
+    lw.w[0] = v.x; lw.w[1] = v.y; lw.w[2] = v.z; lw.w[3] = v.w;
+  } else if constexpr (K == 3) {
+#pragma unroll
+    for (int q = 0; q < 3; q++) {
+      const uint2 v = *reinterpret_cast<const uint2*>(slot + (q * 32 + lane) * 8);
+      lw.w[2 * q] = v.x; lw.w[2 * q + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      const uint4 v = *reinterpret_cast<const uint4*>(slot + (q * 32 + lane) * 16);
+      lw.w[4 * q] = v.x; lw.w[4 * q + 1] = v.y; lw.w[4 * q + 2] = v.z; lw.w[4 * q + 3] = v.w;
+    }
+  }
+}
+
+// {a, b} halves of lane weights u = 16 pp .. 16 pp + 15.  For K = 2 and 4 each
+// 32-bit window is hashed once (a sliding window of 16 + 16/K products whose
+// tail is carried to the next pp); see lane_halves for the correction.
+template <int K, int PP>
+__device__ __forceinline__ void halves16(const LaneWords<K>& lw, uint32_t mult, uint32_t neg16,
+                                         uint32_t (&xp)[16 + (K == 3 ? 0 : 16 / K)],
+                                         uint32_t (&m)[16]) {
+  if constexpr (K == 3) {
+#pragma unroll
+    for (int t = 0; t < 16; t++) m[t] = mcg_halves(lane_state<K>(lw, 16 * PP + t), mult);
+  } else {
+    constexpr int step = 16 / K;
+    if constexpr (PP == 0) {
+#pragma unroll
+      for (int t = 0; t < step; t++) xp[t] = lane_window32<K>(lw, t * K) * mult;
+    } else {
+#pragma unroll
+      for (int t = 0; t < step; t++) xp[t] = xp[16 + t];
+    }
+#pragma unroll
+    for (int t = step; t < 16 + step; t++) xp[t] = lane_window32<K>(lw, (16 * PP + t) * K) * mult;
+#pragma unroll
+    for (int t = 0; t < 16; t++) m[t] = ((xp[t + step] * neg16 + xp[t]) & kMcgMask) ^ kMcgXor;
+  }
+}
+
+// Decode this lane's 64 weights of one tile and store them into the MN-major
+// A stage: lane (g, c) holds outputs 16g..16g+15 (rows of the strip) for
+// inputs c, c+4, c+8, c+12 of the block.  off[4hf + 2jh + jl] is the lane's
+// byte offset of the 16-byte chunk (input c + 4jh + 8hf, rows 8jl..8jl+7).
+template <int K, int FP8>
+__device__ __forceinline__ void decode_store(const LaneWords<K>& lw, uint32_t mult, uint32_t neg16,
+                                             uint8_t* a_blk, const int (&off)[8],
+                                             const uint32_t (&s2)[4]) {
+  uint32_t v[8][4];
+  uint32_t xp[16 + (K == 3 ? 0 : 16 / K)];
+  uint32_t m[16];
+#define EXL3_PP(PP)                                                            \
+  halves16<K, PP>(lw, mult, neg16, xp, m);                                     \
+  _Pragma("unroll") for (int idx = 0; idx < 8; idx++) {                        \
+    const int t0 = idx; /* t = 8 rr + 4 hf + 2 jh + jl, rr = 0 */              \
+    uint32_t v2 = sum_halves2(m[t0], m[t0 + 8]);                               \
+    if (FP8) v2 = e4m3_round2(v2);                                             \
+    __half2 hh = __hmul2(*reinterpret_cast<const __half2*>(&v2),               \
+                         *reinterpret_cast<const __half2*>(&s2[idx >> 1]));    \
+    v[idx][PP] = *reinterpret_cast<uint32_t*>(&hh);                            \
+  }
+  EXL3_PP(0)
+  EXL3_PP(1)
+  EXL3_PP(2)
+  EXL3_PP(3)
+#undef EXL3_PP
+#pragma unroll
+  for (int idx = 0; idx < 8; idx++)
+    *reinterpret_cast<uint4*>(a_blk + off[idx]) = make_uint4(v[idx][0], v[idx][1], v[idx][2], v[idx][3]);
+}
+
+template <int K, int FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, GemmParams p) {
-  using C = GCfg<K, NPROJ>;
+  using C = GCfg<K>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const int strips = p.out / 128;
-  const int tile = blockIdx.x / strips, s = blockIdx.x % strips;
+  const int s = blockIdx.x % strips;
+  const int pj = (blockIdx.x / strips) % p.nproj;
+  const int tile = blockIdx.x / (strips * p.nproj);
   if (tile >= p.n_tiles[0]) return;
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
-  const int n_mma = ((cnt + 15) / 16) * 16;
-  const int nbox = (n_mma + 63) / 64;
+  const int n0 = cnt < kHalfN ? ((cnt + 15) / 16) * 16 : kHalfN;
+  const int n1 = cnt > kHalfN ? ((cnt - kHalfN + 15) / 16) * 16 : 0;
+  const int nbox = (n0 + n1 + 63) / 64;
   const int nks = p.in / kKS;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* a_full = bars;
-  uint64_t* a_empty = a_full + C::kAStages;
-  uint64_t* b_full = a_empty + C::kAStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* b_full = a_empty + kAStages;
   uint64_t* b_empty = b_full + kBStages;
   uint64_t* acc_full = b_empty + kBStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kAStages; i++) {
-      mbar_init(&a_full[i], C::kJobs);
+    for (int i = 0; i < kAStages; i++) {
+      mbar_init(&a_full[i], kJobs);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < kBStages; i++) {
@@ -167,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_full, 1);
     fence_mbar_init();
   }
-  if (warp == kDec) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == kDec) tmem_alloc(tmem_slot, 2 * kHalfN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -192,22 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kDec + 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_f16(128, n_mma, 1, 0);
+      const uint32_t id0 = umma_idesc_f16(128, n0, 1, 0);
+      const uint32_t id1 = umma_idesc_f16(128, n1 > 0 ? n1 : 16, 1, 0);
       for (int ks = 0; ks < nks; ks++) {
-        const int sa = ks % C::kAStages, sb = ks % kBStages;
-        mbar_wait_or_abort(&a_full[sa], (ks / C::kAStages) & 1, p.status);
+        const int sa = ks % kAStages, sb = ks % kBStages;
+        mbar_wait_or_abort(&a_full[sa], (ks / kAStages) & 1, p.status);
         mbar_wait_or_abort(&b_full[sb], (ks / kBStages) & 1, p.status);
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + sa * C::kAStage);
+        const uint32_t a_base = smem_u32(smem + sa * kAStage);
         const uint32_t b_base = smem_u32(smem + C::kOffB + sb * kBStage);
 #pragma unroll
         for (int kk = 0; kk < kKS / 16; kk++) {
-          const uint64_t bdesc = umma_desc(b_base + kk * 32, 16, 1024);
-#pragma unroll
-          for (int pj = 0; pj < NPROJ; pj++) {
-            const uint64_t adesc = umma_desc(a_base + pj * kAProj + kk * 4096, 1024, 2048);
-            umma_f16(tmem + pj * kBN, adesc, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-          }
+          const uint64_t adesc = umma_desc(a_base + kk * 4096, 1024, 2048);
+          const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+          umma_f16(tmem, adesc, umma_desc(b_base + kk * 32, 16, 1024), id0, acc);
+          if (n1 > 0)
+            umma_f16(tmem + kHalfN, adesc, umma_desc(b_base + kHalfN * 128 + kk * 32, 16, 1024),
+                     id1, acc);
         }
         umma_commit(&a_empty[sa]);
         umma_commit(&b_empty[sb]);
@@ -216,22 +278,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- decode
-    const int job = warp % C::kJobs;
-    const int pj = job / 4, blk = job % 4;
-    const int ks0 = warp / C::kJobs;
+    const int blk = warp % kJobs;
+    const int ks0 = warp / kJobs;
     const int g = lane >> 2, c = lane & 3;
     uint8_t* ring = smem + C::kOffCode + warp * kCodeStages * C::kCodeChunk;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
                            (size_t)8 * s * 32 * K;
-    const int n_my = (nks - ks0 + C::kPar - 1) / C::kPar;
-    auto issue = [&](int n) {
-      const int ks = ks0 + n * C::kPar;
-      const uint8_t* src = cbase + (size_t)(ks * 4 + blk) * row_bytes;
-      uint8_t* dst = ring + (n % kCodeStages) * C::kCodeChunk;
+    const int n_my = (nks - ks0 + kPar - 1) / kPar;
+    // lane-constant swizzled offsets of this lane's 8 output chunks in a block
+    int off[8];
 #pragma unroll
-      for (int q = 0; q < (C::kCodeChunk + 511) / 512; q++)
-        if (q * 512 + lane * 16 < C::kCodeChunk) cp_async16(dst + q * 512 + lane * 16, src + q * 512 + lane * 16);
+    for (int idx = 0; idx < 8; idx++) {
+      const int hf = idx >> 2, jh = (idx >> 1) & 1, jl = idx & 1;
+      const int kr = c + 4 * jh;  // input row inside its 8-row K group
+      off[idx] = (g >> 2) * 1024 + hf * 2048 + kr * 128 + (((2 * (g & 3) + jl) ^ kr) << 4);
+    }
+    const uint32_t neg16 = opaque_u32(0xFFFF0000u);
+    auto issue = [&](int n) {
+      const int ks = ks0 + n * kPar;
+      copy_codes<K>(ring + (n % kCodeStages) * C::kCodeChunk,
+                    cbase + (size_t)(ks * 4 + blk) * row_bytes, lane);
     };
 #pragma unroll
     for (int n = 0; n < kCodeStages - 1; n++) {
@@ -240,18 +307,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint16_t* suh_e = p.suh[pj] + (size_t)e * p.in;
     for (int n = 0; n < n_my; n++) {
-      const int ks = ks0 + n * C::kPar;
-      const int sa = ks % C::kAStages;
+      const int ks = ks0 + n * kPar;
+      const int sa = ks % kAStages;
       if (n + kCodeStages - 1 < n_my) issue(n + kCodeStages - 1);
       cp_async_commit();
+      uint32_t s2[4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const uint32_t sb = __ldg(suh_e + ks * kKS + 16 * blk + c + 4 * (q & 1) + 8 * (q >> 1));
+        s2[q] = sb | (sb << 16);
+      }
       cp_async_wait<kCodeStages - 1>();
       __syncwarp();
       LaneWords<K> lw;
-      lds_words<K>(lw, ring + (n % kCodeStages) * C::kCodeChunk + lane * 8 * K);
+      load_codes<K>(lw, ring + (n % kCodeStages) * C::kCodeChunk, lane);
       fetch_neighbour<K>(lw);
-      mbar_wait_or_abort(&a_empty[sa], ((ks / C::kAStages) & 1) ^ 1, p.status);
-      decode_store<K, FP8>(lw, p.mult, smem + sa * C::kAStage + pj * kAProj, blk, g, c,
-                           suh_e + ks * kKS + 16 * blk);
+      mbar_wait_or_abort(&a_empty[sa], ((ks / kAStages) & 1) ^ 1, p.status);
+      decode_store<K, FP8>(lw, p.mult, neg16, smem + sa * kAStage + blk * 4096, off, s2);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
@@ -263,35 +335,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const int q4 = warp & 3, half = warp >> 2;
     const int o = 128 * s + 32 * q4 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    const float sv0 = __half2float(__ushort_as_half(p.svh[0][(size_t)e * p.out + o]));
-    const float sv1 = NPROJ == 2 ? __half2float(__ushort_as_half(p.svh[1][(size_t)e * p.out + o])) : 0.f;
-    for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2) && c0 < cnt; c0 += 16) {
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * kHalfN;
+    const float sv = __half2float(__ushort_as_half(p.svh[pj][(size_t)e * p.out + o]));
+    const int base_n = half * kHalfN;
+    for (int c0 = 0; c0 < kHalfN && base_n + c0 < cnt; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
-      if constexpr (NPROJ == 2) {
-        float a1[16];
-        tmem_ld16(trow + kBN + c0, a1);
-        tmem_ld_wait();
+      tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          const int n = c0 + i;
-          if (n < cnt) {
-            const int pos = pos0 + n;
-            const float xi = p.xinv[pos];
-            const float G = a0[i] * xi * sv0, U = a1[i] * xi * sv1;
-            p.h_out[(size_t)pos * p.out + o] = silu_f(G) * U;
-          }
-        }
-      } else {
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-          const int n = c0 + i;
-          if (n < cnt) {
-            const int pos = pos0 + n;
+      for (int i = 0; i < 16; i++) {
+        const int n = base_n + c0 + i;
+        if (n < cnt) {
+          const int pos = pos0 + n;
+          const float v = a0[i] * p.xinv[pos] * sv;
+          if (p.gu_out) {
+            p.gu_out[((size_t)pj * p.n_pos + pos) * p.out + o] = v;
+          } else {
             const int pid = p.seg_pairs[pos];
-            p.r_out[(size_t)pid * p.out + o] = a0[i] * p.xinv[pos] * sv0 * p.wts[pid];
+            p.r_out[(size_t)pid * p.out + o] = v * p.wts[pid];
           }
         }
       }
@@ -301,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kDec) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, 2 * kHalfN);
   }
 }
 
@@ -329,16 +390,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const void* __restrict
   if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -ex);
 }
 
-// h rows as fp16 with a power-of-two row scale (suh of down is applied on
-// the weight side by the decoder, like suh of gate and up).
-__global__ void __launch_bounds__(256) rowscale_kernel(const float* __restrict__ h, int I,
-                                                       uint16_t* __restrict__ hs,
-                                                       float* __restrict__ hinv) {
+// h = silu(g) * u per position row, as fp16 with a power-of-two row scale
+// (suh of down is applied on the weight side by the decoder).
+__global__ void __launch_bounds__(256) swiglu_rows_kernel(const float* __restrict__ gu, size_t n_pos,
+                                                          int I, uint16_t* __restrict__ hs,
+                                                          float* __restrict__ hinv) {
   __shared__ float s_w[32];
   const int pos = blockIdx.x;
-  const float* hr = h + (size_t)pos * I;
+  const float* gr = gu + (size_t)pos * I;
+  const float* ur = gu + (n_pos + pos) * I;
   float am = 0.0f;
-  for (int i = threadIdx.x; i < I; i += blockDim.x) am = fmaxf(am, fabsf(hr[i]));
+  for (int i = threadIdx.x; i < I; i += blockDim.x) am = fmaxf(am, fabsf(silu_f(gr[i]) * ur[i]));
   for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
   if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = am;
   __syncthreads();
@@ -348,7 +410,7 @@ __global__ void __launch_bounds__(256) rowscale_kernel(const float* __restrict__
   const float sc = ldexpf(1.0f, ex);
   uint16_t* dst = hs + (size_t)pos * I;
   for (int i = threadIdx.x; i < I; i += blockDim.x)
-    dst[i] = __half_as_ushort(__float2half_rn(hr[i] * sc));
+    dst[i] = __half_as_ushort(__float2half_rn(silu_f(gr[i]) * ur[i] * sc));
   if (threadIdx.x == 0) hinv[pos] = ldexpf(1.0f, -ex);
 }
 
@@ -359,7 +421,6 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t*
   const int e = threadIdx.x;
   const int cnt = e < E ? seg_offsets[e + 1] - seg_offsets[e] : 0;
   const int nt = (cnt + kBN - 1) / kBN;
-  // block exclusive scan of nt
   const int lane = e & 31, wid = e >> 5, nw = blockDim.x >> 5;
   int x = nt;
   for (int off = 1; off < 32; off <<= 1) {
@@ -422,11 +483,11 @@ bool make_tmap(CUtensorMap* m, const void* base, size_t rows, size_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int K, int FP8, int NPROJ>
+template <int K, int FP8>
 cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, cudaStream_t st) {
-  using C = GCfg<K, NPROJ>;
+  using C = GCfg<K>;
   static bool init = false;
-  auto kfn = gemm_kernel<K, FP8, NPROJ>;
+  auto kfn = gemm_kernel<K, FP8>;
   if (!init) {
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
@@ -437,17 +498,16 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   return cudaGetLastError();
 }
 
-template <int NPROJ>
 cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
                           cudaStream_t st) {
   if (fp8) {
-    if (K == 2) return launch_gemm<2, 1, NPROJ>(tm, gp, grid, st);
-    if (K == 3) return launch_gemm<3, 1, NPROJ>(tm, gp, grid, st);
-    return launch_gemm<4, 1, NPROJ>(tm, gp, grid, st);
+    if (K == 2) return launch_gemm<2, 1>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm<3, 1>(tm, gp, grid, st);
+    return launch_gemm<4, 1>(tm, gp, grid, st);
   }
-  if (K == 2) return launch_gemm<2, 0, NPROJ>(tm, gp, grid, st);
-  if (K == 3) return launch_gemm<3, 0, NPROJ>(tm, gp, grid, st);
-  return launch_gemm<4, 0, NPROJ>(tm, gp, grid, st);
+  if (K == 2) return launch_gemm<2, 0>(tm, gp, grid, st);
+  if (K == 3) return launch_gemm<3, 0>(tm, gp, grid, st);
+  return launch_gemm<4, 0>(tm, gp, grid, st);
 }
 
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -458,7 +518,7 @@ size_t max_tiles(int T, int E, int top_k) {
 }
 
 struct GemmLayout {
-  size_t xg, xinv, h, hs, hinv, r, tiles, ntiles, total;
+  size_t xg, xinv, gu, hs, hinv, r, tiles, ntiles, total;
 };
 
 GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
@@ -467,7 +527,7 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
   size_t o = 0;
   g.xg = o; o += al(P * H * 2);
   g.xinv = o; o += al(P * 4);
-  g.h = o; o += al(P * I * 4);
+  g.gu = o; o += al(2 * P * I * 4);
   g.hs = o; o += al(P * I * 2);
   g.hinv = o; o += al(P * 4);
   g.r = o; o += al(P * H * 4);
@@ -493,7 +553,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   char* base = static_cast<char*>(ws);
   uint16_t* xg = reinterpret_cast<uint16_t*>(base + g.xg);
   float* xinv = reinterpret_cast<float*>(base + g.xinv);
-  float* h = reinterpret_cast<float*>(base + g.h);
+  float* gu_buf = reinterpret_cast<float*>(base + g.gu);
   uint16_t* hs = reinterpret_cast<uint16_t*>(base + g.hs);
   float* hinv = reinterpret_cast<float*>(base + g.hinv);
   float* r = reinterpret_cast<float*>(base + g.r);
@@ -517,13 +577,15 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.stride[0] = L.code_stride[0]; gu.stride[1] = L.code_stride[1];
   gu.suh[0] = L.suh[0]; gu.suh[1] = L.suh[1];
   gu.svh[0] = L.svh[0]; gu.svh[1] = L.svh[1];
-  gu.in = L.H; gu.out = L.I; gu.mult = L.mult;
-  gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.h_out = h; gu.status = rb.status;
-  if ((err = dispatch_gemm<2>(L.K[0], L.fp8, tm_x, gu, mt * (L.I / 128), st)) != cudaSuccess)
+  gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
+  gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.gu_out = gu_buf; gu.n_pos = (size_t)P;
+  gu.status = rb.status;
+  // gate and up share one launch, so they share a width (checked at create)
+  if ((err = dispatch_gemm(L.K[0], L.fp8, tm_x, gu, mt * 2 * (L.I / 128), st)) != cudaSuccess)
     return err;
   rec(3);
 
-  rowscale_kernel<<<P, 256, 0, st>>>(h, L.I, hs, hinv);
+  swiglu_rows_kernel<<<P, 256, 0, st>>>(gu_buf, (size_t)P, L.I, hs, hinv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(4);
@@ -531,10 +593,10 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   GemmParams dn{};
   dn.codes[0] = L.codes[2]; dn.stride[0] = L.code_stride[2];
   dn.suh[0] = L.suh[2]; dn.svh[0] = L.svh[2];
-  dn.in = L.I; dn.out = L.H; dn.mult = L.mult;
+  dn.in = L.I; dn.out = L.H; dn.nproj = 1; dn.mult = L.mult;
   dn.tiles = tiles; dn.n_tiles = ntiles; dn.xinv = hinv; dn.r_out = r;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
-  err = dispatch_gemm<1>(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
+  err = dispatch_gemm(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
   rec(5);
   return err;
 }
