@@ -47,13 +47,15 @@ constexpr int kAStage = 128 * kKS * 2;        // 16 KB
 constexpr int kBStages = 2;
 constexpr int kBStage = kBN * kKS * 2;        // 64 KB
 constexpr int kCodeStages = 3;
+constexpr int kMaxCluster = 4;        // strips of one tile sharing activation loads
 
 template <int K>
 struct GCfg {
   static constexpr int kCodeChunk = 8 * 32 * K;
   static constexpr int kOffB = kAStages * kAStage;
   static constexpr int kOffCode = kOffB + kBStages * kBStage;
-  static constexpr int kOffBar = kOffCode + kDec * kCodeStages * kCodeChunk;
+  static constexpr int kOffScal = kOffCode + kDec * kCodeStages * kCodeChunk;
+  static constexpr int kOffBar = kOffScal + kBN * 8;  // per-token scale and pair id
   static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
 };
@@ -74,6 +76,7 @@ struct GemmParams {
   const int32_t* seg_pairs;
   const float* wts;
   int32_t* status;
+  int cluster;              // CTAs per cluster (divides the strip count)
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
@@ -223,32 +226,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kBStages; i++) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_empty[i], p.cluster);  // released by the MMA of every CTA of the cluster
     }
     mbar_init(acc_full, 1);
     fence_mbar_init();
   }
   if (warp == kDec) tmem_alloc(tmem_slot, 2 * kHalfN);
+  // per-token epilogue scalars: scale = 1/row-scale (* router weight), pair id
+  float* s_scale = reinterpret_cast<float*>(smem + C::kOffScal);
+  int32_t* s_pid = reinterpret_cast<int32_t*>(s_scale + kBN);
+  for (int n = threadIdx.x; n < cnt; n += blockDim.x) {
+    const int pos = pos0 + n;
+    float sc = p.xinv[pos];
+    int pid = 0;
+    if (!p.gu_out) {
+      pid = p.seg_pairs[pos];
+      sc *= p.wts[pid];
+    }
+    s_scale[n] = sc;
+    s_pid[n] = pid;
+  }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // peers may multicast into this CTA only after its barriers exist
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1);
+  const int crank = (int)cluster_ctarank();
 
   if (warp == kDec) {
     // ---------------------------------------------------------------- TMA
+    // Every CTA of the cluster computes another strip of the same tile, so the
+    // activation boxes are shared: CTA r loads boxes j = r (mod cluster) and
+    // multicasts them; a stage is refilled once all CTAs released it.
     if (lane == 0) {
       for (int ks = 0; ks < nks; ks++) {
         const int sb = ks % kBStages;
         mbar_wait_or_abort(&b_empty[sb], ((ks / kBStages) & 1) ^ 1, p.status);
         mbar_arrive_expect_tx(&b_full[sb], nbox * 64 * kKS * 2);
         uint8_t* dst = smem + C::kOffB + sb * kBStage;
-        for (int j = 0; j < nbox; j++)
-          tma_load_2d(dst + j * 64 * kKS * 2, &tmap_b, ks * kKS, pos0 + 64 * j, &b_full[sb]);
+        for (int j = crank; j < nbox; j += p.cluster)
+          tma_load_2d_multicast(dst + j * 64 * kKS * 2, &tmap_b, ks * kKS, pos0 + 64 * j,
+                                &b_full[sb], cmask);
       }
-      // the last loads were consumed by the MMA thread unless it gave up:
-      // wait (bounded) for them before the CTA may exit
-      for (int ks = nks - kBStages < 0 ? 0 : nks - kBStages; ks < nks; ks++)
+      // before leaving: all boxes for this CTA have landed, and every CTA of
+      // the cluster has released the last stages (their release arrives here)
+      for (int ks = nks - kBStages < 0 ? 0 : nks - kBStages; ks < nks; ks++) {
         mbar_wait_or_abort(&b_full[ks % kBStages], (ks / kBStages) & 1, p.status);
+        mbar_wait_or_abort(&b_empty[ks % kBStages], (ks / kBStages) & 1, p.status);
+      }
     }
   } else if (warp == kDec + 1) {
     // ---------------------------------------------------------------- MMA
@@ -272,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      id1, acc);
         }
         umma_commit(&a_empty[sa]);
-        umma_commit(&b_empty[sb]);
+        umma_commit_multicast(&b_empty[sb], cmask);
       }
       umma_commit(acc_full);
     }
@@ -300,6 +326,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       copy_codes<K>(ring + (n % kCodeStages) * C::kCodeChunk,
                     cbase + (size_t)(ks * 4 + blk) * row_bytes, lane);
     };
+    // The shared ring is only a few jobs deep, so code rows are also pulled
+    // into L2 kL2Ahead jobs ahead: the ring's copies then hit L2.
+    constexpr int kL2Ahead = 8;
+    auto prefetch_l2 = [&](int n) {
+      if (n < n_my && lane * 128 < C::kCodeChunk) {
+        const int ks = ks0 + n * kPar;
+        const uint8_t* a = cbase + (size_t)(ks * 4 + blk) * row_bytes + lane * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      }
+    };
+    for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
 #pragma unroll
     for (int n = 0; n < kCodeStages - 1; n++) {
       if (n < n_my) issue(n);
@@ -311,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sa = ks % kAStages;
       if (n + kCodeStages - 1 < n_my) issue(n + kCodeStages - 1);
       cp_async_commit();
+      prefetch_l2(n + kL2Ahead);
       uint32_t s2[4];
 #pragma unroll
       for (int q = 0; q < 4; q++) {
@@ -346,14 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 16; i++) {
         const int n = base_n + c0 + i;
         if (n < cnt) {
-          const int pos = pos0 + n;
-          const float v = a0[i] * p.xinv[pos] * sv;
-          if (p.gu_out) {
-            p.gu_out[((size_t)pj * p.n_pos + pos) * p.out + o] = v;
-          } else {
-            const int pid = p.seg_pairs[pos];
-            p.r_out[(size_t)pid * p.out + o] = v * p.wts[pid];
-          }
+          const float v = a0[i] * s_scale[n] * sv;
+          if (p.gu_out)
+            p.gu_out[((size_t)pj * p.n_pos + pos0 + n) * p.out + o] = v;
+          else
+            p.r_out[(size_t)s_pid[n] * p.out + o] = v;
         }
       }
     }
@@ -364,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kHalfN);
   }
+  cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
 // Activation rows in position order, fp16 with a power-of-two scale per row
@@ -493,9 +529,21 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
     if (e != cudaSuccess) return e;
     init = true;
   }
-  kfn<<<grid, kThreads, C::kSmem, st>>>(tm, gp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = gp.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kfn, tm, gp);
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
@@ -511,6 +559,14 @@ cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParam
 }
 
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Largest cluster size (<= kMaxCluster) that divides the number of strips, so
+// a cluster always holds strips of one tile.
+int cluster_for(int strips) {
+  int c = kMaxCluster;
+  while (c > 1 && strips % c) c >>= 1;
+  return c;
+}
 
 size_t max_tiles(int T, int E, int top_k) {
   const size_t P = (size_t)T * top_k;
@@ -580,6 +636,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
   gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.gu_out = gu_buf; gu.n_pos = (size_t)P;
   gu.status = rb.status;
+  gu.cluster = cluster_for(L.I / 128);
   // gate and up share one launch, so they share a width (checked at create)
   if ((err = dispatch_gemm(L.K[0], L.fp8, tm_x, gu, mt * 2 * (L.I / 128), st)) != cudaSuccess)
     return err;
@@ -596,6 +653,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   dn.in = L.I; dn.out = L.H; dn.nproj = 1; dn.mult = L.mult;
   dn.tiles = tiles; dn.n_tiles = ntiles; dn.xinv = hinv; dn.r_out = r;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
+  dn.cluster = cluster_for(L.H / 128);
   err = dispatch_gemm(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
   rec(5);
   return err;
