@@ -110,6 +110,34 @@ exl3_status exl3_moe_route(const float *logits, int T, int E, int top_k, int32_t
                            int32_t *seg_offsets, int32_t *seg_pairs, void *ws, size_t ws_bytes,
                            void *stream);
 
+/* Size of the device array behind exl3_moe_route_static: 1 MiB, held on every
+ * device that loads this library until the process exits. */
+#define EXL3_ROUTE_STATIC_SCRATCH_BYTES (1u << 20)
+
+/* exl3_moe_route without a workspace argument.  The pages have no counterpart:
+ * it exists for callers that cannot allocate device memory themselves, such
+ * as a plugin whose host framework owns every device allocation and hands out
+ * only the tensors of the call, or a loop that must not call cudaMalloc
+ * because cudaMalloc can synchronise the device.  The caller still provides
+ * logits and the four outputs, with the layouts, rules and errors of
+ * exl3_moe_route; the routing scratch is instead a library-owned device array
+ * of EXL3_ROUTE_STATIC_SCRATCH_BYTES.  No call allocates or frees memory.
+ *   - Sizes whose exl3_route_workspace_size(T, E, top_k) exceeds
+ *     EXL3_ROUTE_STATIC_SCRATCH_BYTES return EXL3_ERR_SHAPE before any launch;
+ *     any T <= 4096 with E <= 1024 and top_k <= 16 fits.
+ *   - The first call on a device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture begins.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents.  Each call clears what has to start at zero, but calls
+ *     whose work overlaps on the GPU (different streams without ordering,
+ *     several host threads) race on it: order them on one stream.
+ *   - The device status word lives in that array, so exl3_get_device_status
+ *     cannot read it. */
+exl3_status exl3_moe_route_static(const float *logits, int T, int E, int top_k, int32_t *ids,
+                                  float *w, int32_t *seg_offsets, int32_t *seg_pairs,
+                                  void *stream);
+
 /* Bytes of workspace exl3_moe_forward needs for T tokens and top_k (all
  * paths).  Deterministic in (layer shape, T, top_k). */
 size_t exl3_moe_workspace_size(const exl3_layer_t *layer, int T, int top_k);

@@ -67,6 +67,8 @@ def lib():
     L.exl3_route_workspace_size.restype = sz
     L.exl3_moe_route.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp, sz, vp]
     L.exl3_moe_route.restype = i
+    L.exl3_moe_route_static.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp]
+    L.exl3_moe_route_static.restype = i
     L.exl3_moe_workspace_size.argtypes = [vp, i, i]
     L.exl3_moe_workspace_size.restype = sz
     L.exl3_moe_forward.argtypes = [vp, vp, i, vp, i, i, vp, vp, sz, vp]
