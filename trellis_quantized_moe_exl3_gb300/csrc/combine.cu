@@ -28,17 +28,20 @@ __device__ __forceinline__ void store_act4(void* out, int bf16, size_t idx, floa
   }
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ r, int T, int k,
-                                                      int H, const float* __restrict__ sp, int ns,
-                                                      const void* __restrict__ resid,
-                                                      void* __restrict__ out, int bf16) {
+// One thread per group of 4 outputs, for unsplit pair rows: the k pair rows
+// and the shared-expert partials are added in order.
+__global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restrict__ r, int T,
+                                                           int k, int H,
+                                                           const float* __restrict__ sp, int ns,
+                                                           const void* __restrict__ resid,
+                                                           void* __restrict__ out, int bf16) {
   const size_t n4 = (size_t)T * H / 4;
   for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n4;
        v += (size_t)gridDim.x * blockDim.x) {
     const size_t t = v / (H / 4), o = (v % (H / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; j++) {
-      const float4 q = *reinterpret_cast<const float4*>(r + (t * k + j) * H + o);
+      const float4 q = __ldcs(reinterpret_cast<const float4*>(r + (t * k + j) * H + o));
       acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
     }
     if (sp) {
@@ -56,6 +59,68 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       acc.w += load_act(resid, bf16, t * H + o + 3);
     }
     store_act4(out, bf16, t * H + o, acc);
+  }
+}
+
+// Eight lanes per group of 4 outputs: lane l of the octet adds the K-split
+// partials of pairs j = l, l + 8 (splits in order) and the shared-expert
+// partials s = l, l + 8, ... (in order); lane 0 then adds the eight lanes'
+// sums in lane order, so the result is the same on every run.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ r, int nr, int T,
+                                                      int k, int H, const float* __restrict__ sp,
+                                                      int ns, const void* __restrict__ resid,
+                                                      void* __restrict__ out, int bf16) {
+  const int lane = threadIdx.x & 31, l8 = lane & 7, base = lane & 24;
+  const size_t n4 = (size_t)T * H / 4;
+  const size_t rstride = (size_t)T * k * H;  // one K-split slab of pair rows
+  const size_t first = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+  const size_t step = ((size_t)gridDim.x * blockDim.x) >> 3;
+  // every lane of a warp runs the same number of iterations (shuffles below)
+  const size_t n_iter = (n4 + step - 1) / step;
+  for (size_t it = 0; it < n_iter; it++) {
+    const size_t v = first + it * step;
+    const bool live = v < n4;
+    const size_t t = live ? v / (H / 4) : 0, o = live ? (v % (H / 4)) * 4 : 0;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (live) {
+      for (int j = l8; j < k; j += 8) {
+        const float* rp = r + (t * k + j) * H + o;
+        float4 pr = *reinterpret_cast<const float4*>(rp);
+#pragma unroll 8
+        for (int q = 1; q < nr; q++) {
+          const float4 w = *reinterpret_cast<const float4*>(rp + q * rstride);
+          pr.x += w.x; pr.y += w.y; pr.z += w.z; pr.w += w.w;
+        }
+        a.x += pr.x; a.y += pr.y; a.z += pr.z; a.w += pr.w;
+      }
+      if (sp) {
+#pragma unroll 4
+        for (int s = l8; s < ns; s += 8) {
+          const float4 w = *reinterpret_cast<const float4*>(sp + ((size_t)s * T + t) * H + o);
+          b.x += w.x; b.y += w.y; b.z += w.z; b.w += w.w;
+        }
+      }
+    }
+    float4 acc = a, sh = b;
+    for (int i = 1; i < 8; i++) {
+      const int src = base + i;
+      const float ax = __shfl_sync(0xffffffffu, a.x, src), ay = __shfl_sync(0xffffffffu, a.y, src);
+      const float az = __shfl_sync(0xffffffffu, a.z, src), aw = __shfl_sync(0xffffffffu, a.w, src);
+      const float bx = __shfl_sync(0xffffffffu, b.x, src), by = __shfl_sync(0xffffffffu, b.y, src);
+      const float bz = __shfl_sync(0xffffffffu, b.z, src), bw = __shfl_sync(0xffffffffu, b.w, src);
+      acc.x += ax; acc.y += ay; acc.z += az; acc.w += aw;
+      sh.x += bx; sh.y += by; sh.z += bz; sh.w += bw;
+    }
+    if (live && l8 == 0) {
+      acc.x += sh.x; acc.y += sh.y; acc.z += sh.z; acc.w += sh.w;
+      if (resid) {
+        acc.x += load_act(resid, bf16, t * H + o + 0);
+        acc.y += load_act(resid, bf16, t * H + o + 1);
+        acc.z += load_act(resid, bf16, t * H + o + 2);
+        acc.w += load_act(resid, bf16, t * H + o + 3);
+      }
+      store_act4(out, bf16, t * H + o, acc);
+    }
   }
 }
 
@@ -87,15 +152,23 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const void* __restrict__ x
 
 }  // namespace
 
-cudaError_t launch_combine(const float* r, int T, int top_k, int H, const float* shared_part,
-                           int shared_splits, const void* residual, void* out, int out_bf16,
-                           cudaStream_t st) {
+cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H,
+                           const float* shared_part, int shared_splits, const void* residual,
+                           void* out, int out_bf16, cudaStream_t st) {
   const size_t n4 = (size_t)T * H / 4;
-  int blocks = (int)((n4 + 255) / 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks < 1) blocks = 1;
-  combine_kernel<<<blocks, 256, 0, st>>>(r, T, top_k, H, shared_part, shared_splits, residual, out,
-                                         out_bf16);
+  if (r_splits == 1) {
+    size_t blocks = (n4 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    combine_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(r, T, top_k, H, shared_part,
+                                                          shared_splits, residual, out, out_bf16);
+  } else {
+    size_t blocks = (n4 * 8 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(r, r_splits, T, top_k, H, shared_part,
+                                                     shared_splits, residual, out, out_bf16);
+  }
   note_launches(1);
   return cudaGetLastError();
 }

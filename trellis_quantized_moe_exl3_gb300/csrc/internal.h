@@ -82,13 +82,11 @@ cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int ap
 struct GemvBuffers {
   uint32_t* xs_gu;   // [group][2][H/16][8][16] fp16x2 (dup), permuted per 16-block
   float* xs_gu_inv;  // [P][2]
-  float* gu;         // [2][P][I] fp32 gate and up outputs (pair-sorted rows)
+  float* gu;         // [ns_gu][2][P][I] fp32 gate and up K-split partials (pair-sorted rows)
   uint32_t* xs_d;    // [group][I/16][8][16] fp16x2 (dup), permuted
   float* xs_d_inv;   // [P]
-  float* r;          // [P][H] fp32 rows by pair id
-  float* partial;    // K-split partial sums
-  int32_t* counters; // K-split tickets
-  size_t n_counters;
+  float* r;          // [ns_d][P][H] fp32 K-split partial rows by pair id
+  int32_t* counters; // item counters of the two launches
   int ns_gu, ns_d;   // K splits of the two launches
 };
 size_t gemv_scratch_bytes(int T, int top_k, int E, int H, int I);
@@ -107,15 +105,17 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
                             cudaStream_t st);
 
 // ---- shared expert (dense fp16)
-constexpr int kSharedKPer = 128;  // rows of W per split
 size_t shared_scratch_bytes(int T, int H, int I);
-cudaError_t launch_shared(const LayerView& L, const void* x, int x_bf16, int T, float* part_gu,
-                          float* part_d, cudaStream_t st);
+// scratch: shared_scratch_bytes(T, H, I) bytes.  *part_d / *nsplit_d receive
+// the down projection's partial sums [nsplit][T][H] that the combine adds.
+cudaError_t launch_shared(const LayerView& L, const void* x, int x_bf16, int T, void* scratch,
+                          const float** part_d, int* nsplit_d, cudaStream_t st);
 
 // ---- combine / norm
-cudaError_t launch_combine(const float* r, int T, int top_k, int H, const float* shared_part,
-                           int shared_splits, const void* residual, void* out, int out_bf16,
-                           cudaStream_t st);
+// r: [r_splits][T*top_k][H] pair rows (K-split partials, added in order).
+cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H,
+                           const float* shared_part, int shared_splits, const void* residual,
+                           void* out, int out_bf16, cudaStream_t st);
 cudaError_t launch_rmsnorm(const void* x, int bf16, int T, int H, float eps, void* out,
                            cudaStream_t st);
 

@@ -199,6 +199,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   rec(1);
 
   float* pair_rows = nullptr;
+  int pair_splits = 1;
   if (use_gemm(L, T, top_k, path)) {
     if (launch_moe_gemm(L, x, bf16, T, top_k, rb, base + f.gemv, ev, &pair_rows, st) !=
         cudaSuccess)
@@ -208,19 +209,17 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
     gemv_carve(base + f.gemv, T, top_k, L.E, L.H, L.I, &gb);
     if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
     pair_rows = gb.r;
+    pair_splits = gb.ns_d;
   }
 
   const float* sp = nullptr;
   int ns = 0;
   if (layer->has_shared) {
-    float* pgu = reinterpret_cast<float*>(base + f.shared);
-    float* pd = pgu + al((size_t)2 * (L.H / kSharedKPer) * T * L.I * 4) / 4;
-    if (launch_shared(L, x, bf16, T, pgu, pd, st) != cudaSuccess) return EXL3_ERR_CUDA;
-    sp = pd;
-    ns = L.I / kSharedKPer;
+    if (launch_shared(L, x, bf16, T, base + f.shared, &sp, &ns, st) != cudaSuccess)
+      return EXL3_ERR_CUDA;
   }
   rec(6);
-  if (launch_combine(pair_rows, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
+  if (launch_combine(pair_rows, pair_splits, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(7);
   return EXL3_OK;

@@ -309,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, c = lane & 3;
     uint8_t* ring = smem + C::kOffCode + warp * kCodeStages * C::kCodeChunk;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
-    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
+    const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
+                                                            (pj ? p.stride[1] : p.stride[0]) * e) +
                            (size_t)8 * s * 32 * K;
     const int n_my = (nks - ks0 + kPar - 1) / kPar;
     // lane-constant swizzled offsets of this lane's 8 output chunks in a block
@@ -342,7 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n < n_my) issue(n);
       cp_async_commit();
     }
-    const uint16_t* suh_e = p.suh[pj] + (size_t)e * p.in;
+    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
+    // suh of this lane's 4 inputs of a block, loaded one job ahead
+    uint32_t s2n[4];
+    auto load_suh = [&](int n) {
+      const int ks = ks0 + n * kPar;
+#pragma unroll
+      for (int q = 0; q < 4; q++) s2n[q] = __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+    };
+    if (n_my > 0) load_suh(0);
     for (int n = 0; n < n_my; n++) {
       const int ks = ks0 + n * kPar;
       const int sa = ks % kAStages;
@@ -351,10 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_l2(n + kL2Ahead);
       uint32_t s2[4];
 #pragma unroll
-      for (int q = 0; q < 4; q++) {
-        const uint32_t sb = __ldg(suh_e + ks * kKS + 16 * blk + c + 4 * (q & 1) + 8 * (q >> 1));
-        s2[q] = sb | (sb << 16);
-      }
+      for (int q = 0; q < 4; q++) s2[q] = s2n[q] | (s2n[q] << 16);
+      if (n + 1 < n_my) load_suh(n + 1);
       cp_async_wait<kCodeStages - 1>();
       __syncwarp();
       LaneWords<K> lw;
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3, half = warp >> 2;
     const int o = 128 * s + 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * kHalfN;
-    const float sv = __half2float(__ushort_as_half(p.svh[pj][(size_t)e * p.out + o]));
+    const float sv = __half2float(__ushort_as_half((pj ? p.svh[1] : p.svh[0])[(size_t)e * p.out + o]));
     const int base_n = half * kHalfN;
     for (int c0 = 0; c0 < kHalfN && base_n + c0 < cnt; c0 += 16) {
       float a0[16];
@@ -402,52 +409,131 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
+// Row kernels: one warp per position row, 16-byte vector accesses; the first
+// kRowCache chunks of 32 lanes x 8 (gather) or x 4 (swiglu) elements stay in
+// registers between the max pass and the write pass, the rest are re-read.
+constexpr int kRowWarps = 8;
+constexpr int kRowCache = 16;
+
+__device__ __forceinline__ float warp_max(float v) {
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// 8 activations (fp16 or bf16 bits) as floats.
+__device__ __forceinline__ void act8(const uint4& r, int bf16, float (&f)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+    if (bf16) {
+      f[2 * i] = __uint_as_float(lo << 16);
+      f[2 * i + 1] = __uint_as_float(hi << 16);
+    } else {
+      f[2 * i] = __half2float(__ushort_as_half((unsigned short)lo));
+      f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)hi));
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Activation rows in position order, fp16 with a power-of-two scale per row
-// chosen from its max |x| (undone in the epilogue).
-__global__ void __launch_bounds__(256) gather_rows_kernel(const void* __restrict__ x, int x_bf16,
-                                                          int H, int k, const int32_t* seg_pairs,
-                                                          uint16_t* __restrict__ xg,
-                                                          float* __restrict__ xinv) {
-  __shared__ float s_w[32];
-  const int pos = blockIdx.x;
+// chosen from its max |x| (undone in the epilogue).  H is a multiple of 128.
+__global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
+    const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
+    uint16_t* __restrict__ xg, float* __restrict__ xinv) {
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (pos >= P) return;
   const int t = seg_pairs[pos] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
+  const int nv = H / 8;  // 16-byte vectors per row
+  uint4 c[kRowCache];
   float am = 0.0f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) am = fmaxf(am, fabsf(load_act(x, x_bf16, (size_t)t * H + i)));
-  for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = am;
-  __syncthreads();
-  am = 0.0f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); w++) am = fmaxf(am, s_w[w]);
+#pragma unroll
+  for (int i = 0; i < kRowCache; i++) {
+    const int v = i * 32 + lane;
+    if (v < nv) {
+      c[i] = src[v];
+      float f[8];
+      act8(c[i], x_bf16, f);
+#pragma unroll
+      for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(f[q]));
+    }
+  }
+  for (int v = kRowCache * 32 + lane; v < nv; v += 32) {
+    float f[8];
+    act8(src[v], x_bf16, f);
+#pragma unroll
+    for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(f[q]));
+  }
+  am = warp_max(am);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
-  uint16_t* dst = xg + (size_t)pos * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    dst[i] = __half_as_ushort(__float2half_rn(load_act(x, x_bf16, (size_t)t * H + i) * sc));
-  if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -ex);
+  auto put = [&](int v, const uint4& r) {
+    float f[8];
+    act8(r, x_bf16, f);
+    dst[v] = make_uint4(pack_h2(f[0] * sc, f[1] * sc), pack_h2(f[2] * sc, f[3] * sc),
+                        pack_h2(f[4] * sc, f[5] * sc), pack_h2(f[6] * sc, f[7] * sc));
+  };
+#pragma unroll
+  for (int i = 0; i < kRowCache; i++) {
+    const int v = i * 32 + lane;
+    if (v < nv) put(v, c[i]);
+  }
+  for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, src[v]);
+  if (lane == 0) xinv[pos] = ldexpf(1.0f, -ex);
 }
 
 // h = silu(g) * u per position row, as fp16 with a power-of-two row scale
-// (suh of down is applied on the weight side by the decoder).
-__global__ void __launch_bounds__(256) swiglu_rows_kernel(const float* __restrict__ gu, size_t n_pos,
-                                                          int I, uint16_t* __restrict__ hs,
-                                                          float* __restrict__ hinv) {
-  __shared__ float s_w[32];
-  const int pos = blockIdx.x;
-  const float* gr = gu + (size_t)pos * I;
-  const float* ur = gu + (n_pos + pos) * I;
+// (suh of down is applied on the weight side by the decoder).  I is a
+// multiple of 128.
+__global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
+    const float* __restrict__ gu, size_t n_pos, int I, uint16_t* __restrict__ hs,
+    float* __restrict__ hinv) {
+  const int lane = threadIdx.x & 31;
+  const size_t pos = (size_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (pos >= n_pos) return;
+  const float4* gr = reinterpret_cast<const float4*>(gu + pos * I);
+  const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
+  uint2* dst = reinterpret_cast<uint2*>(hs + pos * I);
+  const int nv = I / 4;
+  auto h4 = [&](int v) {
+    const float4 g = __ldcs(gr + v), u = __ldcs(ur + v);
+    return make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+  };
+  auto amax4 = [](float a, const float4& h) {
+    return fmaxf(fmaxf(a, fabsf(h.x)), fmaxf(fmaxf(fabsf(h.y), fabsf(h.z)), fabsf(h.w)));
+  };
+  float4 c[kRowCache];
   float am = 0.0f;
-  for (int i = threadIdx.x; i < I; i += blockDim.x) am = fmaxf(am, fabsf(silu_f(gr[i]) * ur[i]));
-  for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = am;
-  __syncthreads();
-  am = 0.0f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); w++) am = fmaxf(am, s_w[w]);
+#pragma unroll
+  for (int i = 0; i < kRowCache; i++) {
+    const int v = i * 32 + lane;
+    if (v < nv) {
+      c[i] = h4(v);
+      am = amax4(am, c[i]);
+    }
+  }
+  for (int v = kRowCache * 32 + lane; v < nv; v += 32) am = amax4(am, h4(v));
+  am = warp_max(am);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
-  uint16_t* dst = hs + (size_t)pos * I;
-  for (int i = threadIdx.x; i < I; i += blockDim.x)
-    dst[i] = __half_as_ushort(__float2half_rn(silu_f(gr[i]) * ur[i] * sc));
-  if (threadIdx.x == 0) hinv[pos] = ldexpf(1.0f, -ex);
+  auto put = [&](int v, const float4& h) {
+    dst[v] = make_uint2(pack_h2(h.x * sc, h.y * sc), pack_h2(h.z * sc, h.w * sc));
+  };
+#pragma unroll
+  for (int i = 0; i < kRowCache; i++) {
+    const int v = i * 32 + lane;
+    if (v < nv) put(v, c[i]);
+  }
+  for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, h4(v));
+  if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex);
 }
 
 // Token tiles of <= kBN positions per expert segment (one CTA, thread per expert).
@@ -623,7 +709,9 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     return cudaErrorInvalidValue;
   cudaError_t err;
   build_tiles_kernel<<<1, 1024, 0, st>>>(L.E, rb.seg_offsets, tiles, ntiles);
-  gather_rows_kernel<<<P, 256, 0, st>>>(x, x_bf16, L.H, top_k, rb.seg_pairs, xg, xinv);
+  const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
+  gather_rows_kernel<<<row_blocks, kRowWarps * 32, 0, st>>>(x, x_bf16, L.H, top_k, P, rb.seg_pairs,
+                                                           xg, xinv);
   note_launches(2);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(2);
@@ -642,7 +730,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     return err;
   rec(3);
 
-  swiglu_rows_kernel<<<P, 256, 0, st>>>(gu_buf, (size_t)P, L.I, hs, hinv);
+  swiglu_rows_kernel<<<row_blocks, kRowWarps * 32, 0, st>>>(gu_buf, (size_t)P, L.I, hs, hinv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(4);

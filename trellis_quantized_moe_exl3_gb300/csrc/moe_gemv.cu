@@ -7,25 +7,26 @@
 // SwiGLU, down + scatter, driven by device-side segment tables.
 //
 // Work item = (token group of <= 8 positions of one expert, projection,
-// 128-output strip, K split).  A persistent grid walks the items.  Each of
-// the 8 warps of a CTA takes every 8th 16-input block of the item and runs its
-// own asynchronous-copy ring (cp.async, 16 bytes per lane, several blocks
-// ahead, across item boundaries): per block the code row of the strip (8
-// consecutive tiles, 8K bytes per lane) and the matching activation rows
-// (8 tokens x 16 inputs).  Every lane then decodes its 64 weights in
-// registers (the 16-K bit window overlap comes from the next lane of the quad
-// by shuffle) and feeds mma.m16n8k16 with the K dimension doubled: the A
-// register of weight (o, i) is the codebook's {a, b} fp16 pair itself and the
-// B register holds {x_i, x_i}, so the tensor core forms (a + b) x_i with no
-// separate add.  (The exact a + b differs from the format's fp16(a + b) by at
-// most half an fp16 ulp; with the E4M3 rule the rounded value is formed first
-// and placed as {v, 0}.)  Gate and up are separate items; SwiGLU runs in the
-// down projection's input pass.
+// 128-output strip, K split), processed by ONE warp; warps take items from a
+// device counter (an item's successor is taken while its last blocks are
+// still being copied), so the load stays balanced whatever the expert mix.
+// Each warp runs its own asynchronous-copy ring (cp.async, 16 bytes per lane,
+// several blocks ahead, across item boundaries): per 16-input block the code
+// row of the strip (8 consecutive tiles, 8K bytes per lane) and the matching
+// activation rows (8 tokens x 16 inputs).  Every lane then decodes its 64
+// weights in registers (the 16-K bit window overlap comes from the next lane
+// of the quad by shuffle) and feeds mma.m16n8k16 with the K dimension
+// doubled: the A register of weight (o, i) is the codebook's {a, b} fp16 pair
+// itself and the B register holds {x_i, x_i}, so the tensor core forms
+// (a + b) x_i with no separate add.  (The exact a + b differs from the
+// format's fp16(a + b) by at most half an fp16 ulp; with the E4M3 rule the
+// rounded value is formed first and placed as {v, 0}.)  Gate and up are
+// separate items; SwiGLU runs in the down projection's input pass.
 //
-// Partial sums of the 8 warps are added in a fixed tree order in shared
-// memory; K splits write their partials to the workspace and the CTA that
-// completes an item last (atomic ticket) adds them in split order.  The
-// result does not depend on scheduling and no atomics touch the data.
+// Every item writes its scaled partial sums to its own K-split slab; the
+// consumers (the down projection's input pass, the combine) add the slabs in
+// split order, so the result does not depend on scheduling and no atomics
+// touch the data.
 //
 // Activations enter as fp16 with a power-of-two scale per (pair, projection)
 // chosen from the row's max |x * suh| and undone in the epilogue, so the fp16
@@ -48,8 +49,7 @@ struct Cfg {
   static constexpr int kSlot = kCodeChunk + kXsChunk;
   static constexpr int kStages = K == 2 ? 6 : (K == 3 ? 5 : 4);  // per-warp ring depth
   static constexpr int kWarpRing = kStages * kSlot;
-  static constexpr int kRedOff = kCW * kWarpRing;
-  static constexpr int kSmem = kRedOff + 4 * 1024 * 4;  // tree-reduction buffer
+  static constexpr int kSmem = kCW * kWarpRing;
 };
 
 __device__ __forceinline__ float block_max(float v, float* s_tmp) {
@@ -83,6 +83,35 @@ __device__ __forceinline__ void group_of(const int32_t* seg_offsets, const int32
   *slot = l % kGroup;
 }
 
+// Both input passes below give each thread 8 consecutive inputs per step
+// (16-byte loads of x / suh, 32-byte loads of fp32 rows), keep the first
+// kPrepCache steps in registers between the max pass and the write pass, and
+// re-read the rest; one CTA per position.
+constexpr int kPrepCache = 2;
+
+__device__ __forceinline__ void f16x8(const uint4& r, float (&f)[8], int bf16) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+    if (bf16) {
+      f[2 * i] = __uint_as_float(lo << 16);
+      f[2 * i + 1] = __uint_as_float(hi << 16);
+    } else {
+      f[2 * i] = __half2float(__ushort_as_half((unsigned short)lo));
+      f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)hi));
+    }
+  }
+}
+
+// Store 8 consecutive inputs idx0..idx0+7 (idx0 a multiple of 8) of one token
+// slot into the group-interleaved layout, each value duplicated into fp16x2.
+__device__ __forceinline__ void put8(uint32_t* o, int idx0, int slot, const float (&f)[8], float sc) {
+  uint32_t* d = o + ((size_t)(idx0 >> 4) * kGroup + slot) * 16;
+#pragma unroll
+  for (int q = 0; q < 8; q++) d[perm_slot(idx0 + q)] = dup_f16(f[q] * sc);
+}
+
 // x rows of the pairs, times suh of gate and up, scaled, into the
 // group-interleaved layout [group][proj][in/16][8 tokens][16] (fp16x2).
 __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__ x, int x_bf16,
@@ -97,13 +126,44 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   const int t = p / k, e = rb.ids[p];
   int g, slot;
   group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
-  const uint16_t* sg = suh_g + (size_t)e * H;
-  const uint16_t* su = suh_u + (size_t)e * H;
+  const uint4* xv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
+  const uint4* sg = reinterpret_cast<const uint4*>(suh_g + (size_t)e * H);
+  const uint4* su = reinterpret_cast<const uint4*>(suh_u + (size_t)e * H);
+  const int nv = H / 8;
+  // products x * suh of one 8-input step
+  auto prod = [&](int v, float (&fg)[8], float (&fu)[8]) {
+    float fx[8], a[8], b[8];
+    f16x8(xv[v], fx, x_bf16);
+    f16x8(sg[v], a, 0);
+    f16x8(su[v], b, 0);
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      fg[q] = fx[q] * a[q];
+      fu[q] = fx[q] * b[q];
+    }
+  };
+  float cg[kPrepCache][8], cu[kPrepCache][8];
   float ag = 0.0f, au = 0.0f;
-  for (int idx = threadIdx.x; idx < H; idx += blockDim.x) {
-    const float xv = load_act(x, x_bf16, (size_t)t * H + idx);
-    ag = fmaxf(ag, fabsf(xv * __half2float(__ushort_as_half(sg[idx]))));
-    au = fmaxf(au, fabsf(xv * __half2float(__ushort_as_half(su[idx]))));
+#pragma unroll
+  for (int i = 0; i < kPrepCache; i++) {
+    const int v = i * blockDim.x + threadIdx.x;
+    if (v < nv) {
+      prod(v, cg[i], cu[i]);
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        ag = fmaxf(ag, fabsf(cg[i][q]));
+        au = fmaxf(au, fabsf(cu[i][q]));
+      }
+    }
+  }
+  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
+    float fg[8], fu[8];
+    prod(v, fg, fu);
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      ag = fmaxf(ag, fabsf(fg[q]));
+      au = fmaxf(au, fabsf(fu[q]));
+    }
   }
   ag = block_max(ag, s_tmp);
   au = block_max(au, s_tmp);
@@ -112,11 +172,19 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   const int nb = H / 16;
   uint32_t* og = xs + (size_t)g * 2 * nb * kXsChunk / 4;
   uint32_t* ou = og + (size_t)nb * kXsChunk / 4;
-  for (int idx = threadIdx.x; idx < H; idx += blockDim.x) {
-    const float xv = load_act(x, x_bf16, (size_t)t * H + idx);
-    const size_t dst = ((size_t)(idx >> 4) * kGroup + slot) * 16 + perm_slot(idx);
-    og[dst] = dup_f16(xv * __half2float(__ushort_as_half(sg[idx])) * scg);
-    ou[dst] = dup_f16(xv * __half2float(__ushort_as_half(su[idx])) * scu);
+#pragma unroll
+  for (int i = 0; i < kPrepCache; i++) {
+    const int v = i * blockDim.x + threadIdx.x;
+    if (v < nv) {
+      put8(og, 8 * v, slot, cg[i], scg);
+      put8(ou, 8 * v, slot, cu[i], scu);
+    }
+  }
+  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
+    float fg[8], fu[8];
+    prod(v, fg, fu);
+    put8(og, 8 * v, slot, fg, scg);
+    put8(ou, 8 * v, slot, fu, scu);
   }
   if (threadIdx.x == 0) {
     xs_inv[2 * pos] = ldexpf(1.0f, -eg);
@@ -124,10 +192,11 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   }
 }
 
-// h = silu(g) * u for each position's row, times suh of down, scaled,
+// h = silu(g) * u for each position's row (g and u summed over the gate/up
+// launch's K splits in split order), times suh of down, scaled,
 // group-interleaved (the down projection's B operand).
-__global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, size_t n_pos,
-                                                        int I, RouteBuffers rb,
+__global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, int ns,
+                                                        size_t n_pos, int I, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
@@ -136,41 +205,103 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
   const int e = rb.ids[rb.seg_pairs[pos]];
   int g, slot;
   group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
-  const uint16_t* sd = suh_d + (size_t)e * I;
-  const float* gr = gu + (size_t)pos * I;
-  const float* ur = gu + (n_pos + pos) * I;
+  const uint4* sd = reinterpret_cast<const uint4*>(suh_d + (size_t)e * I);
+  // gate / up of split q: gu + ((q * 2 + proj) * n_pos + pos) * I
+  const float4* gr = reinterpret_cast<const float4*>(gu + (size_t)pos * I);
+  const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
+  const size_t qstride = 2 * n_pos * I / 4;  // float4s per split slab
+  const int nv = I / 8;
+  auto hval = [&](int v, float (&h)[8]) {
+    float sv[8];
+    f16x8(sd[v], sv, 0);
+    float gg[8], uu[8];
+#pragma unroll
+    for (int q = 0; q < 8; q++) gg[q] = uu[q] = 0.0f;
+#pragma unroll 4
+    for (int q = 0; q < ns; q++) {  // K splits in order
+      const float4 g0 = __ldcs(gr + q * qstride + 2 * v), g1 = __ldcs(gr + q * qstride + 2 * v + 1);
+      const float4 u0 = __ldcs(ur + q * qstride + 2 * v), u1 = __ldcs(ur + q * qstride + 2 * v + 1);
+      gg[0] += g0.x; gg[1] += g0.y; gg[2] += g0.z; gg[3] += g0.w;
+      gg[4] += g1.x; gg[5] += g1.y; gg[6] += g1.z; gg[7] += g1.w;
+      uu[0] += u0.x; uu[1] += u0.y; uu[2] += u0.z; uu[3] += u0.w;
+      uu[4] += u1.x; uu[5] += u1.y; uu[6] += u1.z; uu[7] += u1.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; q++) h[q] = silu_f(gg[q]) * uu[q] * sv[q];
+  };
+  float c[kPrepCache][8];
   float am = 0.0f;
-  for (int idx = threadIdx.x; idx < I; idx += blockDim.x)
-    am = fmaxf(am, fabsf(silu_f(gr[idx]) * ur[idx] * __half2float(__ushort_as_half(sd[idx]))));
+#pragma unroll
+  for (int i = 0; i < kPrepCache; i++) {
+    const int v = i * blockDim.x + threadIdx.x;
+    if (v < nv) {
+      hval(v, c[i]);
+#pragma unroll
+      for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(c[i][q]));
+    }
+  }
+  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
+    float h[8];
+    hval(v, h);
+#pragma unroll
+    for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(h[q]));
+  }
   am = block_max(am, s_tmp);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
   uint32_t* o = xs + (size_t)g * (I / 16) * kXsChunk / 4;
-  for (int idx = threadIdx.x; idx < I; idx += blockDim.x)
-    o[((size_t)(idx >> 4) * kGroup + slot) * 16 + perm_slot(idx)] =
-        dup_f16(silu_f(gr[idx]) * ur[idx] * __half2float(__ushort_as_half(sd[idx])) * sc);
+#pragma unroll
+  for (int i = 0; i < kPrepCache; i++) {
+    const int v = i * blockDim.x + threadIdx.x;
+    if (v < nv) put8(o, 8 * v, slot, c[i], sc);
+  }
+  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
+    float h[8];
+    hval(v, h);
+    put8(o, 8 * v, slot, h, sc);
+  }
   if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex);
 }
 
+// {a, b} halves of the lane's 64 weights of one tile, fed to the MMA in row
+// groups of 8 (u = 8 r0 + 4 hf + j).  For K = 2 and 4 each 32-bit window is
+// hashed once: xp[t] holds the hash of weight 8 r0 + t's window for the 8
+// weights of this row group plus the 16/K after them (whose low halves give
+// the correction, see lane_halves); the tail is carried to the next group.
 template <int K, int FP8>
 __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& b,
                                            float (&acc)[8][4], uint32_t mult) {
   const uint32_t neg16 = opaque_u32(0xFFFF0000u);
+  constexpr int step = K == 3 ? 0 : 16 / K;
+  uint32_t xp[8 + (K == 3 ? 0 : 16 / K)];
+  if constexpr (K != 3) {
+#pragma unroll
+    for (int t = 0; t < step; t++) xp[t] = lane_window32<K>(lw, t * K) * mult;
+  }
 #pragma unroll
   for (int r0 = 0; r0 < 8; r0++) {
+    uint32_t m[8];
+    if constexpr (K == 3) {
+#pragma unroll
+      for (int t = 0; t < 8; t++) m[t] = mcg_halves(lane_state<K>(lw, 8 * r0 + t), mult);
+    } else {
+      // xp[0..step) already hold weights 8 r0 .. 8 r0 + step - 1
+#pragma unroll
+      for (int t = step; t < 8 + step; t++) xp[t] = lane_window32<K>(lw, (8 * r0 + t) * K) * mult;
+#pragma unroll
+      for (int t = 0; t < 8; t++) m[t] = ((xp[t + step] * neg16 + xp[t]) & kMcgMask) ^ kMcgXor;
+#pragma unroll
+      for (int t = 0; t < step; t++) xp[t] = xp[t + 8];
+    }
 #pragma unroll
     for (int hf = 0; hf < 2; hf++) {
-      const int u = 8 * r0 + 4 * hf;
       uint32_t a0, a1, a2, a3;
-      const uint32_t m0 = lane_halves<K>(lw, u + 0, mult, neg16);
-      const uint32_t m1 = lane_halves<K>(lw, u + 1, mult, neg16);
-      const uint32_t m2 = lane_halves<K>(lw, u + 2, mult, neg16);
-      const uint32_t m3 = lane_halves<K>(lw, u + 3, mult, neg16);
+      const uint32_t* mm = m + 4 * hf;
       if (!FP8) {
-        a0 = m0; a1 = m1; a2 = m2; a3 = m3;
+        a0 = mm[0]; a1 = mm[1]; a2 = mm[2]; a3 = mm[3];
       } else {
-        const uint32_t v01 = e4m3_round2(sum_halves2(m0, m1));
-        const uint32_t v23 = e4m3_round2(sum_halves2(m2, m3));
+        const uint32_t v01 = e4m3_round2(sum_halves2(mm[0], mm[1]));
+        const uint32_t v23 = e4m3_round2(sum_halves2(mm[2], mm[3]));
         a0 = v01 & 0xFFFFu; a1 = v01 >> 16; a2 = v23 & 0xFFFFu; a3 = v23 >> 16;
       }
       mma_f16_16816(acc[r0], a0, a1, a2, a3, hf ? b.z : b.x, hf ? b.w : b.y);
@@ -211,13 +342,11 @@ struct GemvParams {
   const int32_t* n_groups; // device scalar
   const int32_t* seg_pairs;
   const float* wts;        // router weights by pair id (down launch)
-  float* gu_out;           // gate/up launch: [proj][pos][out]
-  float* r_out;            // down launch: [pair id][out]
-  float* partial;          // [group][nproj][strip][nsplit][1024]
-  int32_t* counters;       // [group][nproj][strip], zero on entry, left zero
-  int32_t* status;
+  float* gu_out;           // gate/up launch: [split][proj][pos][out]
+  float* r_out;            // down launch: [split][pair id][out]
+  size_t n_pos;            // positions = pairs
+  int32_t* work;           // item counter, zero on entry
   int nsplit;
-  size_t n_pos;            // positions (row count of gu_out per projection)
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
@@ -230,24 +359,27 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Next item of the launch for this warp (warp-uniform).
+__device__ __forceinline__ int grab_item(int32_t* work) {
+  int it = 0;
+  if ((threadIdx.x & 31) == 0) it = atomicAdd(work, 1);
+  return __shfl_sync(0xffffffffu, it, 0);
+}
+
 template <int K, int FP8>
-__global__ void __launch_bounds__(kThreads, 3) gemv_kernel(GemvParams p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   using C = Cfg<K>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + warp * C::kWarpRing;
-  float* red = reinterpret_cast<float*>(smem + C::kRedOff);
   const int strips = p.out / 128;
   const int nblk = p.in / 16;
-  const int bps = nblk / p.nsplit;   // blocks per item
-  const int bpw = bps / kCW;         // blocks per warp per item
+  const int bps = nblk / p.nsplit;   // blocks (jobs) per item, >= kStages - 1
   const int n_items = p.n_groups[0] * p.nproj * p.nsplit * strips;
-  const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int n_jobs = my_items * bpw;  // this warp's blocks, across its items
   const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
 
   // item id -> (group, projection, split, strip); consecutive ids are
-  // neighbouring strips, so concurrent CTAs read adjacent code bytes
+  // neighbouring strips, so warps taking consecutive items read adjacent code
   auto item_of = [&](int it, int& g, int& pj, int& q, int& s) {
     s = it % strips;
     int r = it / strips;
@@ -256,134 +388,129 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_kernel(GemvParams p) {
     pj = r % p.nproj;
     g = r / p.nproj;
   };
-  // copy the data of this warp's job j into ring slot j % kStages
-  auto issue = [&](int j) {
-    const int it = blockIdx.x + (j / bpw) * gridDim.x;
+  // Producer cursor: the source addresses of the next block to copy.
+  struct Cursor {
+    int b;                  // block of the item (0..bps-1)
+    const uint8_t* cs;      // code chunk of the block
+    const uint8_t* xsrc;    // this lane's activation piece (nullptr: token slot unused)
+  } cur;
+  auto cursor_item = [&](int it) {
     int g, pj, q, s;
     item_of(it, g, pj, q, s);
     const int e = p.groups[4 * g];
-    const int blk = q * bps + (j % bpw) * kCW + warp;
-    uint8_t* slot = ring + (j % C::kStages) * C::kSlot;
-    const uint8_t* cs = reinterpret_cast<const uint8_t*>(p.codes[pj] + p.stride[pj] * e) +
-                        (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
+    const int blk = q * bps;
+    cur.b = 0;
+    cur.cs = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
+                                              (pj ? p.stride[1] : p.stride[0]) * e) +
+             (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
+    // lane l copies 16 bytes of token slot l / 4; slots the group does not
+    // fill are left alone (their MMA columns are discarded)
+    cur.xsrc = (lane >> 2) < p.groups[4 * g + 2]
+                   ? reinterpret_cast<const uint8_t*>(p.xs) +
+                         (((size_t)g * p.nproj + pj) * nblk + blk) * kXsChunk + lane * 16
+                   : nullptr;
+  };
+
+  int item = grab_item(p.work);
+  if (item >= n_items) return;
+  cursor_item(item);
+  int next_item = n_items;  // taken by the producer when it leaves `item`
+  bool p_done = false;
+  // copy the cursor's block into ring slot `slot_idx` and advance the cursor;
+  // the producer is at most kStages - 1 blocks ahead and an item has at least
+  // that many, so it is never more than one item ahead of the consumer
+  auto issue = [&](int slot_idx) {
+    uint8_t* slot = ring + slot_idx * C::kSlot;
 #pragma unroll
     for (int c = 0; c < (C::kCodeChunk + 511) / 512; c++)
-      if (c * 512 + lane * 16 < C::kCodeChunk) cp_async16(slot + c * 512 + lane * 16, cs + c * 512 + lane * 16);
-    // activation rows: lane l copies 16 bytes of token slot l / 4; slots the
-    // group does not fill are left alone (their MMA columns are discarded)
-    if ((lane >> 2) < p.groups[4 * g + 2]) {
-      const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(p.xs) +
-                            (((size_t)g * p.nproj + pj) * nblk + blk) * kXsChunk;
-      cp_async16(slot + C::kCodeChunk + lane * 16, xsrc + lane * 16);
+      if (c * 512 + lane * 16 < C::kCodeChunk) cp_async16(slot + c * 512 + lane * 16, cur.cs + c * 512 + lane * 16);
+    if (cur.xsrc) cp_async16(slot + C::kCodeChunk + lane * 16, cur.xsrc);
+    if (++cur.b < bps) {
+      cur.cs += row_bytes;
+      if (cur.xsrc) cur.xsrc += kXsChunk;
+    } else {
+      next_item = grab_item(p.work);
+      if (next_item < n_items) cursor_item(next_item);
+      else p_done = true;
     }
   };
 
+  int issue_slot = 0;
 #pragma unroll
   for (int j = 0; j < C::kStages - 1; j++) {
-    if (j < n_jobs) issue(j);
+    if (!p_done) issue(issue_slot);
+    issue_slot = issue_slot + 1 == C::kStages ? 0 : issue_slot + 1;
     cp_async_commit();
   }
+  int read_slot = 0;
 
   const int g_l = lane >> 2, c_l = lane & 3;
-  int j = 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  while (item < n_items) {
     int g, pj, q, s;
     item_of(item, g, pj, q, s);
-    const int cnt = p.groups[4 * g + 2];
+    const int e = p.groups[4 * g], pos0 = p.groups[4 * g + 1], cnt = p.groups[4 * g + 2];
+    // epilogue scalars, loaded now so their latency hides behind the blocks:
+    // this lane's 16 outputs (two runs of 8 svh values) and 2 token slots
+    const int obase = 16 * (8 * s + g_l);
+    const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + obase;
+    const uint4 sv_lo = __ldg(reinterpret_cast<const uint4*>(svh));
+    const uint4 sv_hi = __ldg(reinterpret_cast<const uint4*>(svh + 8));
+    float tok_scale[2];
+    int tok_row[2];
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+      const int n = 2 * c_l + u;
+      tok_scale[u] = 0.0f;
+      tok_row[u] = 0;
+      if (n < cnt) {
+        const int pos = pos0 + n;
+        tok_scale[u] = __ldg(p.xs_inv + (size_t)pos * p.nproj + pj);
+        if (p.gu_out) {
+          tok_row[u] = ((q * p.nproj + pj) * (int)p.n_pos + pos);
+        } else {
+          const int pid = __ldg(p.seg_pairs + pos);
+          tok_scale[u] *= __ldg(p.wts + pid);
+          tok_row[u] = q * (int)p.n_pos + pid;
+        }
+      }
+    }
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
       for (int d = 0; d < 4; d++) acc[i][d] = 0.0f;
-    for (int b = 0; b < bpw; b++, j++) {
-      if (j + C::kStages - 1 < n_jobs) issue(j + C::kStages - 1);
+    for (int b = 0; b < bps; b++) {
+      if (!p_done) issue(issue_slot);
+      issue_slot = issue_slot + 1 == C::kStages ? 0 : issue_slot + 1;
       cp_async_commit();
       cp_async_wait<C::kStages - 1>();
       __syncwarp();
-      const uint8_t* slot = ring + (j % C::kStages) * C::kSlot;
+      const uint8_t* slot = ring + read_slot * C::kSlot;
+      read_slot = read_slot + 1 == C::kStages ? 0 : read_slot + 1;
       LaneWords<K> lw;
       lds_lane_words<K>(lw, slot + lane * 8 * K);
       fetch_neighbour<K>(lw);
       const uint4 bx = g_l < cnt ? *reinterpret_cast<const uint4*>(slot + C::kCodeChunk + g_l * 64 + c_l * 16)
                                  : make_uint4(0, 0, 0, 0);
       decode_mma<K, FP8>(lw, bx, acc, p.mult);
-      __syncwarp();  // the slot is refilled by the next iteration's issue
+      __syncwarp();  // the slot is refilled by a later issue
     }
-    // fixed-order tree reduction over the 8 warps: 4+4, 2+2, 1+1
+    // this item's scaled partial sums into its split slab
+    float* dst = p.gu_out ? p.gu_out : p.r_out;
+    const uint32_t svw[8] = {sv_lo.x, sv_lo.y, sv_lo.z, sv_lo.w, sv_hi.x, sv_hi.y, sv_hi.z, sv_hi.w};
 #pragma unroll
-    for (int half = 4; half >= 1; half >>= 1) {
-      if (warp >= half && warp < 2 * half) {
-        float* dst = red + (size_t)(warp - half) * 1024;
+    for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int i = 0; i < 8; i++)
-          *reinterpret_cast<float4*>(dst + (i * 32 + lane) * 4) =
-              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      }
-      __syncthreads();
-      if (warp < half) {
-        const float* src = red + (size_t)warp * 1024;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const float4 v = *reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4);
-          acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
+      for (int d = 0; d < 4; d++) {
+        const int u = d & 1, dh = d >> 1;
+        if (2 * c_l + u < cnt) {
+          // output obase + i + 8 dh: fp16 number (i + 8 dh) of the two runs
+          const uint32_t w2 = svw[(i + 8 * dh) >> 1];
+          const float sv = __half2float(__ushort_as_half((unsigned short)(i & 1 ? w2 >> 16 : w2 & 0xFFFFu)));
+          dst[(size_t)tok_row[u] * p.out + obase + i + 8 * dh] = acc[i][d] * tok_scale[u] * sv;
         }
       }
-      __syncthreads();
-    }
-    if (warp == 0) {
-      bool do_epi = true;
-      if (p.nsplit > 1) {
-        const size_t slot = ((size_t)g * p.nproj + pj) * strips + s;
-        float* mine = p.partial + (slot * p.nsplit + q) * 1024;
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-          *reinterpret_cast<float4*>(mine + (i * 32 + lane) * 4) =
-              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&p.counters[slot], 1) == p.nsplit - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        do_epi = last;
-        if (last) {
-          __threadfence();
-#pragma unroll
-          for (int i = 0; i < 8; i++)
-#pragma unroll
-            for (int d = 0; d < 4; d++) acc[i][d] = 0.0f;
-          for (int qq = 0; qq < p.nsplit; qq++) {
-            const float* src = p.partial + (slot * p.nsplit + qq) * 1024;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4));
-              acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
-            }
-          }
-          if (lane == 0) p.counters[slot] = 0;
-        }
-      }
-      if (do_epi) {
-        const int e = p.groups[4 * g], pos0 = p.groups[4 * g + 1], cnt = p.groups[4 * g + 2];
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-#pragma unroll
-          for (int d = 0; d < 4; d++) {
-            const int o = 16 * (8 * s + g_l) + i + 8 * (d >> 1);
-            const int n = 2 * c_l + (d & 1);
-            if (n < cnt) {
-              const int pos = pos0 + n;
-              const float v = acc[i][d] * p.xs_inv[(size_t)pos * p.nproj + pj] *
-                              __half2float(__ushort_as_half(p.svh[pj][(size_t)e * p.out + o]));
-              if (p.gu_out) {
-                p.gu_out[((size_t)pj * p.n_pos + pos) * p.out + o] = v;
-              } else {
-                const int pid = p.seg_pairs[pos];
-                p.r_out[(size_t)pid * p.out + o] = v * p.wts[pid];
-              }
-            }
-          }
-      }
-    }
+    item = next_item;
   }
   cp_async_wait<0>();
 }
@@ -407,7 +534,8 @@ cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
     occ = o < 1 ? 1 : o;
   }
   int grid = sms * occ;
-  if (items_ub < grid) grid = items_ub;
+  const int cta_ub = (items_ub + kCW - 1) / kCW;
+  if (cta_ub < grid) grid = cta_ub;
   if (grid < 1) grid = 1;
   kfn<<<grid, kThreads, C::kSmem, st>>>(gp);
   note_launches(1);
@@ -425,12 +553,14 @@ cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int items_ub, cu
   return launch_gemv<4, 0>(gp, items_ub, st);
 }
 
-// K splits: double while every warp keeps >= 2 blocks per item and the upper
-// bound on items stays below ~6 per CTA slot (3 CTAs on 152 SMs).
+// K splits: the smallest power of two that gives ~8 items per resident warp
+// (2 CTAs of 8 warps on 152 SMs) for the upper bound on token groups, keeping
+// >= 8 blocks per item (more than any ring is deep) and at most 16 splits.
 int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
+  const size_t target = (size_t)8 * 152 * 2 * kCW;
   int ns = 1;
-  while (ns < 8 && nblk % (2 * ns * kCW) == 0 && nblk / (2 * ns * kCW) >= 2 &&
-         groups_ub * items_per_group * ns < (size_t)6 * 456)
+  while (ns < 16 && nblk % (2 * ns) == 0 && nblk / (2 * ns) >= 8 &&
+         groups_ub * items_per_group * ns < target)
     ns *= 2;
   return ns;
 }
@@ -438,9 +568,8 @@ int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct GemvLayout {
-  size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, partial, counters, total;
+  size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, counters, total;
   int ns_gu, ns_d;
-  size_t n_counters;
 };
 
 GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
@@ -449,18 +578,14 @@ GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
   const size_t G = max_groups(T, E, top_k);
   g.ns_gu = choose_nsplit(G, 2 * (I / 128), H / 16);
   g.ns_d = choose_nsplit(G, H / 128, I / 16);
-  const size_t part_gu = g.ns_gu > 1 ? G * 2 * (I / 128) * g.ns_gu * 1024 * 4 : 0;
-  const size_t part_d = g.ns_d > 1 ? G * (H / 128) * g.ns_d * 1024 * 4 : 0;
-  g.n_counters = G * (2 * (I / 128) > H / 128 ? 2 * (I / 128) : H / 128);
   size_t o = 0;
   g.xs_gu = o; o += al(G * 2 * (H / 16) * kXsChunk);
   g.xs_gu_inv = o; o += al(P * 2 * 4);
-  g.gu = o; o += al(2 * P * I * 4);
+  g.gu = o; o += al((size_t)g.ns_gu * 2 * P * I * 4);
   g.xs_d = o; o += al(G * (I / 16) * kXsChunk);
   g.xs_d_inv = o; o += al(P * 4);
-  g.r = o; o += al(P * H * 4);
-  g.partial = o; o += al(part_gu > part_d ? part_gu : part_d);
-  g.counters = o; o += al(g.n_counters * 4);
+  g.r = o; o += al((size_t)g.ns_d * P * H * 4);
+  g.counters = o; o += al(2 * 4);
   g.total = o;
   return g;
 }
@@ -480,9 +605,7 @@ void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb
   gb->xs_d = reinterpret_cast<uint32_t*>(q + g.xs_d);
   gb->xs_d_inv = reinterpret_cast<float*>(q + g.xs_d_inv);
   gb->r = reinterpret_cast<float*>(q + g.r);
-  gb->partial = reinterpret_cast<float*>(q + g.partial);
   gb->counters = reinterpret_cast<int32_t*>(q + g.counters);
-  gb->n_counters = g.n_counters;
   gb->ns_gu = g.ns_gu;
   gb->ns_d = g.ns_d;
 }
@@ -496,8 +619,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   const int P = T * top_k;
   const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
-  if ((err = cudaMemsetAsync(gb.counters, 0, gb.n_counters * sizeof(int32_t), st)) != cudaSuccess)
-    return err;
+  if ((err = cudaMemsetAsync(gb.counters, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return err;
   gather_xs_kernel<<<P, 256, 0, st>>>(x, x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], gb.xs_gu,
                                       gb.xs_gu_inv);
   note_launches(1);
@@ -513,14 +635,14 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   gu.xs = gb.xs_gu; gu.xs_inv = gb.xs_gu_inv;
   gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
   gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.gu_out = gb.gu; gu.n_pos = (size_t)P;
-  gu.partial = gb.partial; gu.counters = gb.counters; gu.status = rb.status;
-  gu.nsplit = gb.ns_gu;
+  gu.work = gb.counters; gu.nsplit = gb.ns_gu;
   if ((err = dispatch_gemv(L.K[0], L.fp8, gu, (int)(G * 2 * (L.I / 128) * gu.nsplit), st)) !=
       cudaSuccess)
     return err;
   rec(3);
 
-  prep_down_kernel<<<P, 256, 0, st>>>(gb.gu, (size_t)P, L.I, rb, L.suh[2], gb.xs_d, gb.xs_d_inv);
+  prep_down_kernel<<<P, 256, 0, st>>>(gb.gu, gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], gb.xs_d,
+                                      gb.xs_d_inv);
   note_launches(1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   rec(4);
@@ -531,9 +653,8 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   dn.svh[0] = L.svh[2];
   dn.xs = gb.xs_d; dn.xs_inv = gb.xs_d_inv;
   dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
-  dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r;
-  dn.partial = gb.partial; dn.counters = gb.counters; dn.status = rb.status;
-  dn.nsplit = gb.ns_d;
+  dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r; dn.n_pos = (size_t)P;
+  dn.work = gb.counters + 1; dn.nsplit = gb.ns_d;
   err = dispatch_gemv(L.K[2], L.fp8, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
   rec(5);
   return err;
