@@ -8,11 +8,13 @@ hidden 4096, intermediate 2048, K=2 codes, 4 bf16 tokens, plus an fp16 shared
 expert), synthetic seeded data.  One JSON line on rank 0.
 
 ours:      the CUDA library through its C ABI; the step is captured once in a
-           CUDA graph and replayed; L2 is flushed (512 MiB read) before every
-           timed step; per-stage CUDA events inside the graph give the dominant
-           kernel's duration.  e2e: the same forward through the public API
-           with pinned-host inputs copied in and the output copied out inside
-           the timed region.
+           CUDA graph and replayed; L2 is flushed (512 MiB written, then 512
+           MiB read, so no dirty line is left) before every timed step.  A
+           second graph of the same forward with per-stage CUDA events inside
+           gives the stage times and the dominant kernel's duration for the
+           roofline.  e2e: the same forward through the public API with
+           pinned-host inputs copied in and the output copied out inside the
+           timed region.
 reference: the CPU oracle as it stands, on this host, on a bounded sample
            (one (token, expert) pair per step).
 Under torchrun (N > 1) every rank runs its own token batch (weak scaling).
@@ -214,7 +216,7 @@ def workload_config(wl):
                          + (", + fp16 shared expert" if s.shared else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
             "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round,
-            "l2": "flushed (512 MiB read) before every timed step"}
+            "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
 
 
 # ----------------------------------------------------------------------------- ours
@@ -226,7 +228,7 @@ def run_ours(args):
 
     from trellis_quantized_moe_exl3_gb300 import _lib, synth
     from trellis_quantized_moe_exl3_gb300 import build as lib_build
-    from trellis_quantized_moe_exl3_gb300.api import Layer
+    from trellis_quantized_moe_exl3_gb300.api import Layer, route
 
     world, rank, local = dist_env()
     lib_build.build()
@@ -255,34 +257,28 @@ def run_ours(args):
     T, k = wl.T, wl.top_k
     ws = layer.workspace(T, k, dev)
     out = torch.empty_like(x)
-    # L2 flush by reading 512 MiB (4x L2): leaves clean lines, so no write-back
-    # of the flush competes with the next step
+    # L2 flush: write 512 MiB (4x L2), then read it back, so the lines left in
+    # L2 are clean and no write-back of the flush competes with the step
     flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
-    flush_l2 = lambda: flush.sum()
+
+    def flush_l2():
+        flush.fill_(1)
+        flush.sum()
+
     s = torch.cuda.Stream(device=dev)
     L = _lib.lib()
-
-    # stage events recorded inside the forward (and inside the graph)
-    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(_lib.EXL3_NUM_STAGE_EVENTS)]
-    with torch.cuda.stream(s):
-        for e in stage_ev:
-            e.record(s)
-    torch.cuda.synchronize()
-    arr = (ctypes.c_void_p * _lib.EXL3_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_ev])
-    _lib.check(L.exl3_layer_set_stage_events(layer.handle, arr, _lib.EXL3_NUM_STAGE_EVENTS),
-               "set_stage_events")
-
     with torch.cuda.stream(s):
         for _ in range(2):
             layer.forward(x, lg, k, out=out, ws=ws, stream=s)
     torch.cuda.synchronize()
 
-    # active experts of this batch (for the algorithmic bytes)
-    from trellis_quantized_moe_exl3_gb300.api import route
-    r_ids, _, r_off, _ = route(lg, k)
+    # routing of this batch (host side, outside any timing): the per-expert
+    # counts behind the algorithmic work of each kernel
+    _, _, r_off, _ = route(lg, k)
     counts = torch.diff(r_off).cpu().numpy()
     n_active = int((counts > 0).sum())
 
+    # headline graph: the forward alone
     use_graph = True
     c0 = L.exl3_launch_count()
     g = torch.cuda.CUDAGraph()
@@ -293,21 +289,37 @@ def run_ours(args):
         use_graph = False
     launches_per_step = int(L.exl3_launch_count() - c0)
 
+    # stage graph: the same forward with stage-boundary events inside
+    n_ev = _lib.EXL3_NUM_STAGE_EVENTS
+    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    with torch.cuda.stream(s):
+        for e in stage_ev:
+            e.record(s)
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in stage_ev])
+    _lib.check(L.exl3_layer_set_stage_events(layer.handle, arr, n_ev), "set_stage_events")
+    g_stage = None
+    if use_graph:
+        g_stage = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g_stage, stream=s):
+                layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+        except Exception:
+            g_stage = None
+    L.exl3_layer_set_stage_events(layer.handle, None, 0)
+
     def step():
         if use_graph:
             g.replay()
         else:
             layer.forward(x, lg, k, out=out, ws=ws, stream=s)
 
-    start_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    end_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
             flush_l2()
             step()
     torch.cuda.synchronize()
 
-    stage_ms = np.zeros(_lib.EXL3_NUM_STAGE_EVENTS - 1)
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -316,42 +328,24 @@ def run_ours(args):
         except ValueError:
             pass
     clocks = ClockSampler(gpu_index)
+    start_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    end_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    step_ms = []
-    stage_live = True
     with torch.cuda.stream(s):
         for i in range(args.steps):
             flush_l2()
             start_ev[i].record(s)
             step()
             end_ev[i].record(s)
-            end_ev[i].synchronize()
-            step_ms.append(start_ev[i].elapsed_time(end_ev[i]))
-            if stage_live:
-                try:
-                    for j in range(_lib.EXL3_NUM_STAGE_EVENTS - 1):
-                        stage_ms[j] += stage_ev[j].elapsed_time(stage_ev[j + 1])
-                except Exception:
-                    stage_live = False
-                    stage_ms[:] = 0
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    if not stage_live:
-        # events inside the graph could not be timed: time the same K steps eagerly
-        with torch.cuda.stream(s):
-            for i in range(args.steps):
-                flush_l2()
-                layer.forward(x, lg, k, out=out, ws=ws, stream=s)
-                stage_ev[-1].synchronize()
-                for j in range(_lib.EXL3_NUM_STAGE_EVENTS - 1):
-                    stage_ms[j] += stage_ev[j].elapsed_time(stage_ev[j + 1])
-    stage_ms /= args.steps
+    step_ms = [a.elapsed_time(b) for a, b in zip(start_ev, end_ev)]
     tot = float(np.sum(step_ms))
     if world > 1:
         t = torch.tensor([tot], device=dev)
@@ -359,6 +353,24 @@ def run_ours(args):
         tot = float(t.item())
     ms_per_step = tot / args.steps
     value = world * T * args.steps / (tot / 1e3)
+
+    # stage times: the stage graph (or eager forwards with the events set)
+    stage_ms = np.zeros(n_ev - 1)
+    stage_live = g_stage is not None
+    if not stage_live:
+        L.exl3_layer_set_stage_events(layer.handle, arr, n_ev)
+    with torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush_l2()
+            if stage_live:
+                g_stage.replay()
+            else:
+                layer.forward(x, lg, k, out=out, ws=ws, stream=s)
+            stage_ev[-1].synchronize()
+            for j in range(n_ev - 1):
+                stage_ms[j] += stage_ev[j].elapsed_time(stage_ev[j + 1])
+    L.exl3_layer_set_stage_events(layer.handle, None, 0)
+    stage_ms /= args.steps
 
     # e2e: public API with host buffers, copies inside the timed region
     x_host = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -368,7 +380,6 @@ def run_ours(args):
     lg_d = torch.empty_like(lg)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    L.exl3_layer_set_stage_events(layer.handle, None, 0)
     e2e_ms = []
     with torch.cuda.stream(s):
         for i in range(args.warmup + args.steps):
@@ -389,21 +400,52 @@ def run_ours(args):
         e2e_tot = float(t.item())
     e2e_value = world * T * args.steps / (e2e_tot / 1e3)
 
-    # roofline of the dominant kernel (largest stage)
+    # roofline of the dominant expert kernel (the larger of gate/up and down)
     hbm, bf16_tf, src = peaks()
     H, I = spec.hidden, spec.inter
     code_b = [H * I * spec.K[p] // 8 for p in range(3)]
     side_b = [(H + I) * 2] * 3
     stage_names = _lib.STAGE_NAMES
-    stage_bytes = {
-        "gate_up": n_active * (code_b[0] + code_b[1] + side_b[0] + side_b[1]),
-        "down": n_active * (code_b[2] + side_b[2]),
-        "shared": 3 * H * I * 2 if sw else 0,
-    }
-    dom = max(stage_bytes, key=lambda n: stage_ms[stage_names.index(n)])
+    P = T * k
+    gemm_path = P >= 16 * spec.num_experts
+    # weight decodes: every expert's weights once per token group (GEMV: <= 8
+    # tokens) or token tile (GEMM: <= 512 tokens)
+    per = 512 if gemm_path else 8
+    units = int(sum((int(c) + per - 1) // per for c in counts))
+    dec_w = {"gate_up": units * 2 * H * I, "down": units * H * I}
+    flops = {"gate_up": 2.0 * P * H * I * 2, "down": 2.0 * P * H * I}
+    code_bytes = {"gate_up": n_active * (code_b[0] + code_b[1] + side_b[0] + side_b[1]),
+                  "down": n_active * (code_b[2] + side_b[2])}
+    dom = max(("gate_up", "down"), key=lambda n: stage_ms[stage_names.index(n)])
     dom_ms = float(stage_ms[stage_names.index(dom)])
-    achieved = stage_bytes[dom] / (dom_ms / 1e3) / 1e9
-    step_bytes = sum(stage_bytes.values())
+    kdom = spec.K[0] if dom == "gate_up" else spec.K[2]
+    # issue-slot peak of the trellis decode: 128 lane-instructions per SM and
+    # clock, 152 SMs, 2070 MHz maximum clock; K = 2 and 4 need 4 integer
+    # instructions per weight (window, multiply, correction, mask-xor: two on
+    # the ALU pipe, two on the FMA pipe), K = 3 needs 3 on the 64-lane ALU pipe
+    # (window, mask, mask-xor) besides the multiply
+    sms, clk_hz = 152, 2.070e9
+    peak_wps = sms * clk_hz * (128 / 4 if kdom in (2, 4) else 64 / 3)
+    dec_rate = dec_w[dom] / (dom_ms / 1e3)
+    hbm_rate = code_bytes[dom] / (dom_ms / 1e3) / 1e9
+    if gemm_path:
+        tf = flops[dom] / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_tf,
+                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": None,
+                "algorithmic_flops": flops[dom], "ms": dom_ms,
+                "peak_source": f"{src} (bf16_tflops burst; the fp16 dense rate equals bf16)",
+                "alu_view": {"achieved": dec_rate / 1e9, "peak": peak_wps / 1e9,
+                             "unit": "Gweight/s", "frac": dec_rate / peak_wps,
+                             "weight_decodes": dec_w[dom]}}
+    else:
+        roof = {"bound": "alu", "kernel": dom, "achieved": dec_rate / 1e9,
+                "peak": peak_wps / 1e9, "unit": "Gweight/s", "frac": dec_rate / peak_wps,
+                "traffic": None, "weight_decodes": dec_w[dom], "ms": dom_ms,
+                "peak_source": "derived: 152 SMs x 2070 MHz x 128 issue slots / instructions per weight",
+                "hbm_view": {"achieved": hbm_rate, "peak": hbm, "unit": "GB/s",
+                             "frac": hbm_rate / hbm, "algorithmic_bytes": code_bytes[dom],
+                             "peak_source": f"{src} (hbm_gbs, burst)"}}
+    step_bytes = code_bytes["gate_up"] + code_bytes["down"] + (3 * H * I * 2 if sw else 0)
     line = {
         "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -412,11 +454,9 @@ def run_ours(args):
         "data": "synthetic (seeded PCG64): uniform uint16 codes, side vectors 1+0.1N(0,1), "
                 "N(0,1) activations and router logits",
         "config": {**workload_config(wl), "cuda_graph": use_graph, "n_active_experts": n_active,
-                   "stage_events": "inside the timed graph" if stage_live else "eager re-run"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
-                     "algorithmic_bytes": stage_bytes[dom], "ms": dom_ms,
-                     "peak_source": f"{src} (hbm_gbs, burst)"},
+                   "path": "gemm (tcgen05)" if gemm_path else "gemv (mma.sync)",
+                   "stage_times": "separate graph with stage events" if stage_live else "eager re-run"},
+        "roofline": roof,
         "step_roofline": {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
                           "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm,
                           "what": "code + side-vector + shared-expert bytes of one step / step time"},

@@ -77,10 +77,15 @@ typedef struct {
                                     ([p4] intro: one shared expert per MoE layer) */
 } exl3_layer_desc;
 
-/* Validate `desc` and build a handle (host allocation only).  Errors:
+/* Validate `desc` and build a handle.  A layer with a shared expert also
+ * creates one CUDA stream and two events on the current device (released by
+ * exl3_layer_destroy); the shared expert of every forward runs on that stream,
+ * forked from the caller's stream after routing and joined before the
+ * combine, so forwards on one handle must be issued by one host thread at a
+ * time.  Errors:
  * EXL3_ERR_ARG (null pointers, shared_w partly NULL), EXL3_ERR_SHAPE,
  * EXL3_ERR_K, EXL3_ERR_DEVICE (current device is not compute capability
- * 10.x). */
+ * 10.x), EXL3_ERR_CUDA (stream or event creation failed). */
 exl3_status exl3_layer_create(const exl3_layer_desc *desc, exl3_layer_t **out);
 void exl3_layer_destroy(exl3_layer_t *layer);
 
@@ -173,7 +178,8 @@ exl3_status exl3_get_device_status(const void *ws, void *stream, int32_t *status
 /* Stage-boundary profiling.  When set, every forward on this layer records
  * events[i] (cudaEvent_t, created by the caller) on its stream at these
  * boundaries: 0 start, 1 routing done, 2 gather done, 3 gate/up done,
- * 4 down input prepared, 5 down done, 6 shared expert done, 7 combine done.
+ * 4 down input prepared, 5 down done, 6 joined with the shared expert's
+ * stream, 7 combine done.
  * n_events must be EXL3_NUM_STAGE_EVENTS; events = NULL clears the hook.
  * For measurement only: not safe while another thread runs a forward on the
  * same layer. */

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restri
                                                            const float* __restrict__ sp, int ns,
                                                            const void* __restrict__ resid,
                                                            void* __restrict__ out, int bf16) {
+  pdl_wait();
   const size_t n4 = (size_t)T * H / 4;
   for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n4;
        v += (size_t)gridDim.x * blockDim.x) {
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int k, int H, const float* __restrict__ sp,
                                                       int ns, const void* __restrict__ resid,
                                                       void* __restrict__ out, int bf16) {
+  pdl_wait();
   const int lane = threadIdx.x & 31, l8 = lane & 7, base = lane & 24;
   const size_t n4 = (size_t)T * H / 4;
   const size_t rstride = (size_t)T * k * H;  // one K-split slab of pair rows
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const void* __restrict__ x, int bf16, int H,
                                                       float eps, void* __restrict__ out) {
+  pdl_wait();
   __shared__ float s_w[32];
   const size_t t = blockIdx.x;
   float ss = 0.0f;
@@ -156,29 +159,30 @@ cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H
                            const float* shared_part, int shared_splits, const void* residual,
                            void* out, int out_bf16, cudaStream_t st) {
   const size_t n4 = (size_t)T * H / 4;
+  cudaError_t err;
   if (r_splits == 1) {
     size_t blocks = (n4 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    combine_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(r, T, top_k, H, shared_part,
-                                                          shared_splits, residual, out, out_bf16);
+    err = launch_pdl(combine_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, r, T, top_k, H,
+                     shared_part, shared_splits, residual, out, out_bf16);
   } else {
     size_t blocks = (n4 * 8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(r, r_splits, T, top_k, H, shared_part,
-                                                     shared_splits, residual, out, out_bf16);
+    err = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, r, r_splits, T,
+                     top_k, H, shared_part, shared_splits, residual, out, out_bf16);
   }
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_rmsnorm(const void* x, int bf16, int T, int H, float eps, void* out,
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, 256, 0, st>>>(x, bf16, H, eps, out);
+  const cudaError_t err = launch_pdl(rmsnorm_kernel, dim3(T), dim3(256), 0, st, x, bf16, H, eps, out);
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace exl3

@@ -187,6 +187,12 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- PDL
+// Kernels of the forward chain are launched with programmatic dependent
+// launch: a kernel may become resident while its stream predecessor drains,
+// and must wait here before it touches memory the predecessor reads or writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float load_act(const void* x, int is_bf16, size_t idx) {
   const uint16_t b = reinterpret_cast<const uint16_t*>(x)[idx];

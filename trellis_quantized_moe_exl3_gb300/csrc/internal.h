@@ -22,6 +22,23 @@ inline void record_stage_event(cudaEvent_t ev, cudaStream_t st) {
     cudaEventRecord(ev, st);
 }
 
+// Launch with programmatic dependent launch allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr uint32_t kDefaultMcgMult = 0x9E3779B1u;
 constexpr int kRouteChunk = 128;   // tokens per routing CTA
 constexpr int kMaxTopK = 16;

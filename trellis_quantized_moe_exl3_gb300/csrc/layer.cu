@@ -15,6 +15,10 @@ struct exl3_layer {
   int has_shared;
   cudaEvent_t ev[EXL3_NUM_STAGE_EVENTS];
   int has_ev;
+  // the shared expert runs on a side stream, forked from and joined to the
+  // caller's stream inside each forward
+  cudaStream_t side;
+  cudaEvent_t fork, join;
 };
 
 namespace {
@@ -120,11 +124,25 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
     v.code_stride[p] = (in / 16) * (outf / 16) * 16 * (size_t)d->K[p];
   }
   L->has_shared = nshared == 3;
+  if (L->has_shared) {
+    if (cudaStreamCreateWithFlags(&L->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->join, cudaEventDisableTiming) != cudaSuccess) {
+      exl3_layer_destroy(L);
+      return EXL3_ERR_CUDA;
+    }
+  }
   *out = L;
   return EXL3_OK;
 }
 
-void exl3_layer_destroy(exl3_layer_t* layer) { free(layer); }
+void exl3_layer_destroy(exl3_layer_t* layer) {
+  if (!layer) return;
+  if (layer->side) cudaStreamDestroy(layer->side);
+  if (layer->fork) cudaEventDestroy(layer->fork);
+  if (layer->join) cudaEventDestroy(layer->join);
+  free(layer);
+}
 
 exl3_status exl3_decode_dense(const exl3_layer_t* layer, int expert, int proj, int apply_side,
                               uint16_t* out, void* stream) {
@@ -196,6 +214,19 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   rec(0);
   if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
   if (launch_route(logits, T, L.E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
+  // shared expert: forked onto the side stream once routing is done, so it
+  // overlaps the expert kernels (which take their work dynamically and do not
+  // mind SMs it occupies) instead of delaying the one-CTA routing kernel
+  const float* sp = nullptr;
+  int ns = 0;
+  if (layer->has_shared) {
+    if (cudaEventRecord(layer->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(layer->side, layer->fork, 0) != cudaSuccess)
+      return EXL3_ERR_CUDA;
+    if (launch_shared(L, x, bf16, T, base + f.shared, &sp, &ns, layer->side) != cudaSuccess)
+      return EXL3_ERR_CUDA;
+    if (cudaEventRecord(layer->join, layer->side) != cudaSuccess) return EXL3_ERR_CUDA;
+  }
   rec(1);
 
   float* pair_rows = nullptr;
@@ -212,12 +243,8 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
     pair_splits = gb.ns_d;
   }
 
-  const float* sp = nullptr;
-  int ns = 0;
-  if (layer->has_shared) {
-    if (launch_shared(L, x, bf16, T, base + f.shared, &sp, &ns, st) != cudaSuccess)
-      return EXL3_ERR_CUDA;
-  }
+  if (layer->has_shared && cudaStreamWaitEvent(st, layer->join, 0) != cudaSuccess)
+    return EXL3_ERR_CUDA;
   rec(6);
   if (launch_combine(pair_rows, pair_splits, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
     return EXL3_ERR_CUDA;

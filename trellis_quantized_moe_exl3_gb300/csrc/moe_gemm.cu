@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int s = blockIdx.x % strips;
   const int pj = (blockIdx.x / strips) % p.nproj;
   const int tile = blockIdx.x / (strips * p.nproj);
-  if (tile >= p.n_tiles[0]) return;
+  pdl_wait();
+  if (tile >= p.n_tiles[0]) return;  // the whole cluster shares the tile
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int n0 = cnt < kHalfN ? ((cnt + 15) / 16) * 16 : kHalfN;
   const int n1 = cnt > kHalfN ? ((cnt - kHalfN + 15) / 16) * 16 : 0;
@@ -446,6 +447,7 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
     const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
     uint16_t* __restrict__ xg, float* __restrict__ xinv) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (pos >= P) return;
@@ -496,6 +498,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
 __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     const float* __restrict__ gu, size_t n_pos, int I, uint16_t* __restrict__ hs,
     float* __restrict__ hinv) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const size_t pos = (size_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (pos >= n_pos) return;
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
 // Token tiles of <= kBN positions per expert segment (one CTA, thread per expert).
 __global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t* seg_offsets,
                                                            int32_t* tiles, int32_t* n_tiles) {
+  pdl_wait();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   const int cnt = e < E ? seg_offsets[e + 1] - seg_offsets[e] : 0;
@@ -620,13 +624,15 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = gp.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t err = cudaLaunchKernelEx(&cfg, kfn, tm, gp);
   note_launches(1);
   return err;
@@ -708,12 +714,14 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   if (!make_tmap(&tm_x, xg, (size_t)P, (size_t)L.H) || !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I))
     return cudaErrorInvalidValue;
   cudaError_t err;
-  build_tiles_kernel<<<1, 1024, 0, st>>>(L.E, rb.seg_offsets, tiles, ntiles);
+  if ((err = launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, st, L.E,
+                        (const int32_t*)rb.seg_offsets, tiles, ntiles)) != cudaSuccess)
+    return err;
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
-  gather_rows_kernel<<<row_blocks, kRowWarps * 32, 0, st>>>(x, x_bf16, L.H, top_k, P, rb.seg_pairs,
-                                                           xg, xinv);
+  err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H,
+                   top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
   note_launches(2);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   rec(2);
 
   GemmParams gu{};
@@ -730,9 +738,10 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     return err;
   rec(3);
 
-  swiglu_rows_kernel<<<row_blocks, kRowWarps * 32, 0, st>>>(gu_buf, (size_t)P, L.I, hs, hinv);
+  err = launch_pdl(swiglu_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
+                   (const float*)gu_buf, (size_t)P, L.I, hs, hinv);
   note_launches(1);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   rec(4);
 
   GemmParams dn{};

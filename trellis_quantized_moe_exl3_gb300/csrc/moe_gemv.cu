@@ -68,12 +68,9 @@ __device__ __forceinline__ uint32_t dup_f16(float v) {
   return b | (b << 16);
 }
 
-// Slot of input idx inside its 16-block: lane c reads slots 4c..4c+3, which
-// hold inputs c, c+4, c+8, c+12.
-__device__ __forceinline__ int perm_slot(int idx) {
-  const int r = idx & 15;
-  return 4 * (r & 3) + (r >> 2);
-}
+// Activation slots inside a 16-input block: lane c of an MMA quad reads
+// slots 4c..4c+3, which hold inputs c, c+4, c+8, c+12 (slot q holds input
+// 4 (q & 3) + (q >> 2)).
 
 // Token group and slot of a segment position.
 __device__ __forceinline__ void group_of(const int32_t* seg_offsets, const int32_t* group_off, int e,
@@ -83,13 +80,12 @@ __device__ __forceinline__ void group_of(const int32_t* seg_offsets, const int32
   *slot = l % kGroup;
 }
 
-// Both input passes below give each thread 8 consecutive inputs per step
-// (16-byte loads of x / suh, 32-byte loads of fp32 rows), keep the first
-// kPrepCache steps in registers between the max pass and the write pass, and
-// re-read the rest; one CTA per position.
-constexpr int kPrepCache = 2;
-
-__device__ __forceinline__ void f16x8(const uint4& r, float (&f)[8], int bf16) {
+// Both input passes below give each thread one 16-input block per step
+// (16-byte loads of x / suh, float4 loads of fp32 rows), keep its first block
+// in registers between the max pass and the write pass (re-reading any
+// further ones), and write the block's 16 token-slot values as four 16-byte
+// stores in the permuted slot order; one CTA per position.
+__device__ __forceinline__ void f16x8(const uint4& r, float* f, int bf16) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
   for (int i = 0; i < 4; i++) {
@@ -104,12 +100,26 @@ __device__ __forceinline__ void f16x8(const uint4& r, float (&f)[8], int bf16) {
   }
 }
 
-// Store 8 consecutive inputs idx0..idx0+7 (idx0 a multiple of 8) of one token
-// slot into the group-interleaved layout, each value duplicated into fp16x2.
-__device__ __forceinline__ void put8(uint32_t* o, int idx0, int slot, const float (&f)[8], float sc) {
-  uint32_t* d = o + ((size_t)(idx0 >> 4) * kGroup + slot) * 16;
+// Store the 16 inputs of block b of one token slot into the group-interleaved
+// layout, each value duplicated into fp16x2, in the slot order above.
+__device__ __forceinline__ void put16(uint32_t* o, int b, int slot, const float (&f)[16], float sc) {
+  uint4* d = reinterpret_cast<uint4*>(o + ((size_t)b * kGroup + slot) * 16);
 #pragma unroll
-  for (int q = 0; q < 8; q++) d[perm_slot(idx0 + q)] = dup_f16(f[q] * sc);
+  for (int v = 0; v < 4; v++) {
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int q = 4 * v + u;
+      w[u] = dup_f16(f[4 * (q & 3) + (q >> 2)] * sc);
+    }
+    d[v] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ float amax16(float a, const float (&f)[16]) {
+#pragma unroll
+  for (int q = 0; q < 16; q++) a = fmaxf(a, fabsf(f[q]));
+  return a;
 }
 
 // x rows of the pairs, times suh of gate and up, scaled, into the
@@ -120,6 +130,7 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
                                                         const uint16_t* __restrict__ suh_u,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
+  pdl_wait();
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
   const int p = rb.seg_pairs[pos];
@@ -129,62 +140,51 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   const uint4* xv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
   const uint4* sg = reinterpret_cast<const uint4*>(suh_g + (size_t)e * H);
   const uint4* su = reinterpret_cast<const uint4*>(suh_u + (size_t)e * H);
-  const int nv = H / 8;
-  // products x * suh of one 8-input step
-  auto prod = [&](int v, float (&fg)[8], float (&fu)[8]) {
-    float fx[8], a[8], b[8];
-    f16x8(xv[v], fx, x_bf16);
-    f16x8(sg[v], a, 0);
-    f16x8(su[v], b, 0);
+  const int nb = H / 16;
+  // products x * suh of block b
+  auto prod = [&](int b, float (&fg)[16], float (&fu)[16]) {
+    float fx[16], a[16], c[16];
+    f16x8(xv[2 * b], fx, x_bf16);
+    f16x8(xv[2 * b + 1], fx + 8, x_bf16);
+    f16x8(sg[2 * b], a, 0);
+    f16x8(sg[2 * b + 1], a + 8, 0);
+    f16x8(su[2 * b], c, 0);
+    f16x8(su[2 * b + 1], c + 8, 0);
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
+    for (int q = 0; q < 16; q++) {
       fg[q] = fx[q] * a[q];
-      fu[q] = fx[q] * b[q];
+      fu[q] = fx[q] * c[q];
     }
   };
-  float cg[kPrepCache][8], cu[kPrepCache][8];
+  float cg[16], cu[16];
   float ag = 0.0f, au = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kPrepCache; i++) {
-    const int v = i * blockDim.x + threadIdx.x;
-    if (v < nv) {
-      prod(v, cg[i], cu[i]);
-#pragma unroll
-      for (int q = 0; q < 8; q++) {
-        ag = fmaxf(ag, fabsf(cg[i][q]));
-        au = fmaxf(au, fabsf(cu[i][q]));
-      }
-    }
+  const int b0 = threadIdx.x;
+  if (b0 < nb) {
+    prod(b0, cg, cu);
+    ag = amax16(ag, cg);
+    au = amax16(au, cu);
   }
-  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
-    float fg[8], fu[8];
-    prod(v, fg, fu);
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      ag = fmaxf(ag, fabsf(fg[q]));
-      au = fmaxf(au, fabsf(fu[q]));
-    }
+  for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
+    float fg[16], fu[16];
+    prod(b, fg, fu);
+    ag = amax16(ag, fg);
+    au = amax16(au, fu);
   }
   ag = block_max(ag, s_tmp);
   au = block_max(au, s_tmp);
   const int eg = fp16_scale_exp(ag), eu = fp16_scale_exp(au);
   const float scg = ldexpf(1.0f, eg), scu = ldexpf(1.0f, eu);
-  const int nb = H / 16;
   uint32_t* og = xs + (size_t)g * 2 * nb * kXsChunk / 4;
   uint32_t* ou = og + (size_t)nb * kXsChunk / 4;
-#pragma unroll
-  for (int i = 0; i < kPrepCache; i++) {
-    const int v = i * blockDim.x + threadIdx.x;
-    if (v < nv) {
-      put8(og, 8 * v, slot, cg[i], scg);
-      put8(ou, 8 * v, slot, cu[i], scu);
-    }
+  if (b0 < nb) {
+    put16(og, b0, slot, cg, scg);
+    put16(ou, b0, slot, cu, scu);
   }
-  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
-    float fg[8], fu[8];
-    prod(v, fg, fu);
-    put8(og, 8 * v, slot, fg, scg);
-    put8(ou, 8 * v, slot, fu, scu);
+  for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
+    float fg[16], fu[16];
+    prod(b, fg, fu);
+    put16(og, b, slot, fg, scg);
+    put16(ou, b, slot, fu, scu);
   }
   if (threadIdx.x == 0) {
     xs_inv[2 * pos] = ldexpf(1.0f, -eg);
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
                                                         const uint16_t* __restrict__ suh_d,
                                                         uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
+  pdl_wait();
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
   const int e = rb.ids[rb.seg_pairs[pos]];
@@ -210,64 +211,52 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
   const float4* gr = reinterpret_cast<const float4*>(gu + (size_t)pos * I);
   const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
   const size_t qstride = 2 * n_pos * I / 4;  // float4s per split slab
-  const int nv = I / 8;
-  auto hval = [&](int v, float (&h)[8]) {
-    float sv[8];
-    f16x8(sd[v], sv, 0);
-    float gg[8], uu[8];
+  const int nb = I / 16;
+  auto hval = [&](int b, float (&h)[16]) {
+    float sv[16];
+    f16x8(sd[2 * b], sv, 0);
+    f16x8(sd[2 * b + 1], sv + 8, 0);
+    float gg[16], uu[16];
 #pragma unroll
-    for (int q = 0; q < 8; q++) gg[q] = uu[q] = 0.0f;
-#pragma unroll 4
+    for (int q = 0; q < 16; q++) gg[q] = uu[q] = 0.0f;
+#pragma unroll 2
     for (int q = 0; q < ns; q++) {  // K splits in order
-      const float4 g0 = __ldcs(gr + q * qstride + 2 * v), g1 = __ldcs(gr + q * qstride + 2 * v + 1);
-      const float4 u0 = __ldcs(ur + q * qstride + 2 * v), u1 = __ldcs(ur + q * qstride + 2 * v + 1);
-      gg[0] += g0.x; gg[1] += g0.y; gg[2] += g0.z; gg[3] += g0.w;
-      gg[4] += g1.x; gg[5] += g1.y; gg[6] += g1.z; gg[7] += g1.w;
-      uu[0] += u0.x; uu[1] += u0.y; uu[2] += u0.z; uu[3] += u0.w;
-      uu[4] += u1.x; uu[5] += u1.y; uu[6] += u1.z; uu[7] += u1.w;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const float4 a = __ldcs(gr + q * qstride + 4 * b + c);
+        const float4 u = __ldcs(ur + q * qstride + 4 * b + c);
+        gg[4 * c] += a.x; gg[4 * c + 1] += a.y; gg[4 * c + 2] += a.z; gg[4 * c + 3] += a.w;
+        uu[4 * c] += u.x; uu[4 * c + 1] += u.y; uu[4 * c + 2] += u.z; uu[4 * c + 3] += u.w;
+      }
     }
 #pragma unroll
-    for (int q = 0; q < 8; q++) h[q] = silu_f(gg[q]) * uu[q] * sv[q];
+    for (int q = 0; q < 16; q++) h[q] = silu_f(gg[q]) * uu[q] * sv[q];
   };
-  float c[kPrepCache][8];
+  float c[16];
   float am = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kPrepCache; i++) {
-    const int v = i * blockDim.x + threadIdx.x;
-    if (v < nv) {
-      hval(v, c[i]);
-#pragma unroll
-      for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(c[i][q]));
-    }
+  const int b0 = threadIdx.x;
+  if (b0 < nb) {
+    hval(b0, c);
+    am = amax16(am, c);
   }
-  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
-    float h[8];
-    hval(v, h);
-#pragma unroll
-    for (int q = 0; q < 8; q++) am = fmaxf(am, fabsf(h[q]));
+  for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
+    float h[16];
+    hval(b, h);
+    am = amax16(am, h);
   }
   am = block_max(am, s_tmp);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
-  uint32_t* o = xs + (size_t)g * (I / 16) * kXsChunk / 4;
-#pragma unroll
-  for (int i = 0; i < kPrepCache; i++) {
-    const int v = i * blockDim.x + threadIdx.x;
-    if (v < nv) put8(o, 8 * v, slot, c[i], sc);
-  }
-  for (int v = kPrepCache * blockDim.x + threadIdx.x; v < nv; v += blockDim.x) {
-    float h[8];
-    hval(v, h);
-    put8(o, 8 * v, slot, h, sc);
+  uint32_t* o = xs + (size_t)g * nb * kXsChunk / 4;
+  if (b0 < nb) put16(o, b0, slot, c, sc);
+  for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
+    float h[16];
+    hval(b, h);
+    put16(o, b, slot, h, sc);
   }
   if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex);
 }
 
-// {a, b} halves of the lane's 64 weights of one tile, fed to the MMA in row
-// groups of 8 (u = 8 r0 + 4 hf + j).  For K = 2 and 4 each 32-bit window is
-// hashed once: xp[t] holds the hash of weight 8 r0 + t's window for the 8
-// weights of this row group plus the 16/K after them (whose low halves give
-// the correction, see lane_halves); the tail is carried to the next group.
 template <int K, int FP8>
 __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& b,
                                            float (&acc)[8][4], uint32_t mult) {
@@ -370,6 +359,7 @@ template <int K, int FP8>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   using C = Cfg<K>;
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + warp * C::kWarpRing;
   const int strips = p.out / 128;
@@ -537,9 +527,9 @@ cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
   const int cta_ub = (items_ub + kCW - 1) / kCW;
   if (cta_ub < grid) grid = cta_ub;
   if (grid < 1) grid = 1;
-  kfn<<<grid, kThreads, C::kSmem, st>>>(gp);
+  const cudaError_t err = launch_pdl(kfn, dim3(grid), dim3(kThreads), C::kSmem, st, gp);
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int items_ub, cudaStream_t st) {
@@ -620,10 +610,10 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
   if ((err = cudaMemsetAsync(gb.counters, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return err;
-  gather_xs_kernel<<<P, 256, 0, st>>>(x, x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], gb.xs_gu,
-                                      gb.xs_gu_inv);
+  err = launch_pdl(gather_xs_kernel, dim3(P), dim3(L.H / 16 < 256 ? L.H / 16 : 256), 0, st, x, x_bf16, L.H, top_k, rb, L.suh[0],
+                   L.suh[1], gb.xs_gu, gb.xs_gu_inv);
   note_launches(1);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   rec(2);
 
   // gate and up share one launch, so they share a width (checked at create)
@@ -641,10 +631,10 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     return err;
   rec(3);
 
-  prep_down_kernel<<<P, 256, 0, st>>>(gb.gu, gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], gb.xs_d,
-                                      gb.xs_d_inv);
+  err = launch_pdl(prep_down_kernel, dim3(P), dim3(L.I / 16 < 256 ? L.I / 16 : 256), 0, st, gb.gu, gb.ns_gu, (size_t)P, L.I, rb,
+                   L.suh[2], gb.xs_d, gb.xs_d_inv);
   note_launches(1);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   rec(4);
 
   GemvParams dn{};

@@ -126,6 +126,7 @@ template <int MAXPL>
 __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restrict__ logits, int T,
                                                            int E, int k, RouteBuffers rb,
                                                            int fused) {
+  pdl_wait();
   __shared__ int s_ids[kRouteChunk * kMaxTopK];
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_warp[32];
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
 // Scan stage (one CTA): exclusive prefix over chunks per expert, offsets over
 // experts, active list.  chunk_counts becomes the base of each (chunk, e).
 __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, RouteBuffers rb) {
+  pdl_wait();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   int tot = 0;
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, Ro
 }
 
 __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, RouteBuffers rb) {
+  pdl_wait();
   const int chunk = blockIdx.x;
   const int t0 = chunk * kRouteChunk;
   const int nt = min(kRouteChunk, T - t0);
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 }
 
 __global__ void route_empty_kernel(int E, RouteBuffers rb) {
+  pdl_wait();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     rb.seg_offsets[e] = 0;
     rb.group_off[e] = 0;
@@ -254,10 +258,17 @@ __global__ void route_empty_kernel(int E, RouteBuffers rb) {
 template <int MAXPL>
 cudaError_t launch_chunks(const float* logits, int T, int E, int k, const RouteBuffers& rb,
                           int nchunks, cudaStream_t st) {
-  const int threads = nchunks == 1 ? 1024 : 512;
-  route_chunk_kernel<MAXPL><<<nchunks, threads, 0, st>>>(logits, T, E, k, rb, nchunks == 1);
+  // one chunk: the scans need a thread per expert, the top-k a warp per token
+  // (in turns); fewer warps make the CTA's barriers cheaper
+  int threads = 512;
+  if (nchunks == 1) {
+    const int need_e = (E + 31) / 32 * 32, need_t = 32 * (T < 16 ? T : 16);
+    threads = need_e > need_t ? need_e : need_t;
+  }
+  const cudaError_t err = launch_pdl(route_chunk_kernel<MAXPL>, dim3(nchunks), dim3(threads), 0, st,
+                                     logits, T, E, k, rb, (int)(nchunks == 1));
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace
@@ -300,9 +311,9 @@ void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb) {
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBuffers& rb,
                          cudaStream_t st) {
   if (T == 0) {
-    route_empty_kernel<<<1, 256, 0, st>>>(E, rb);
+    const cudaError_t e = launch_pdl(route_empty_kernel, dim3(1), dim3(256), 0, st, E, rb);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
   }
   const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
   const int pl = (E + 31) / 32;
@@ -314,12 +325,12 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBu
   else if (pl <= 16) err = launch_chunks<16>(logits, T, E, k, rb, nchunks, st);
   else err = launch_chunks<32>(logits, T, E, k, rb, nchunks, st);
   if (err != cudaSuccess || nchunks == 1) return err;
-  route_scan_kernel<<<1, 1024, 0, st>>>(E, nchunks, rb);
+  err = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, rb);
   note_launches(1);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  route_scatter_kernel<<<nchunks, 256, 0, st>>>(T, E, k, rb);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, rb);
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace exl3

@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(kSThreads, 2) shared_gemv_kernel(SharedParams 
   uint4 raw[kSBatch];
   load_rows(raw, wp, p.out, lane_ok);
 
+  // the inputs (h) and the partial sums are the predecessors' business
+  pdl_wait();
   for (int v = threadIdx.x; v < NT * kSRows; v += kSThreads) {
     const int tt = v / kSRows, kk = v % kSRows;
     float val = 0.0f;
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(kSThreads, 2) shared_gemv_kernel(SharedParams 
 // h[t][o] = silu(sum_s gate[s][t][o]) * sum_s up[s][t][o], splits in order.
 __global__ void __launch_bounds__(256) shared_h_kernel(const float* __restrict__ part, int nsplit,
                                                        int T, int I, float* __restrict__ h) {
+  pdl_wait();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)T * I) return;
   const size_t slab = (size_t)T * I;
@@ -159,9 +162,9 @@ cudaError_t launch_nt(const SharedParams& sp, dim3 grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  shared_gemv_kernel<NT><<<grid, kSThreads, smem, st>>>(sp);
+  const cudaError_t err = launch_pdl(shared_gemv_kernel<NT>, grid, dim3(kSThreads), smem, st, sp);
   note_launches(1);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_sg(const SharedParams& sp, dim3 grid, cudaStream_t st) {
@@ -206,9 +209,10 @@ cudaError_t launch_shared(const LayerView& L, const void* x, int x_bf16, int T, 
   if ((err = launch_sg(gu, dim3(chunks_i, L.H / kSRows, 2 * passes), st)) != cudaSuccess) return err;
   float* h = reinterpret_cast<float*>(b + s.h);
   const size_t nh = (size_t)T * L.I;
-  shared_h_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(gu.part, L.H / kSRows, T, L.I, h);
+  err = launch_pdl(shared_h_kernel, dim3((unsigned)((nh + 255) / 256)), dim3(256), 0, st, gu.part,
+                   L.H / kSRows, T, L.I, h);
   note_launches(1);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   SharedParams dn{};
   dn.w[0] = L.shared_w[2];
   dn.in = L.I; dn.out = L.H; dn.T = T; dn.nproj = 1;
