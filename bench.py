@@ -58,6 +58,32 @@ def dist_env():
     return world, rank, local
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the decode step's expert kernels, from one ncu capture summarised in
+# profiles/gemv_kernel_K2_decode.md; reported only while the kernel sources
+# hash to what was captured (otherwise null).
+NCU_TRAFFIC = {
+    ("decode", "gate_up"): 128.093440e6 + 4.645120e6,
+    ("decode", "down"): 63.688192e6 + 0.931328e6,
+}
+NCU_SOURCES = {
+    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "27ab4b195a7e5aa1616493edd62d84c368acc413",
+    "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "acc08b6543c6c9f48b753a60e3a7426762d31149",
+}
+
+
+def ncu_traffic(workload, kernel):
+    import hashlib
+    for rel, digest in NCU_SOURCES.items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return NCU_TRAFFIC.get((workload, kernel))
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -438,9 +464,11 @@ def run_ours(args):
                              "unit": "Gweight/s", "frac": dec_rate / peak_wps,
                              "weight_decodes": dec_w[dom]}}
     else:
+        traffic = ncu_traffic(wl.name, dom)
         roof = {"bound": "alu", "kernel": dom, "achieved": dec_rate / 1e9,
                 "peak": peak_wps / 1e9, "unit": "Gweight/s", "frac": dec_rate / peak_wps,
-                "traffic": None, "weight_decodes": dec_w[dom], "ms": dom_ms,
+                "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
+                "weight_decodes": dec_w[dom], "ms": dom_ms,
                 "peak_source": "derived: 152 SMs x 2070 MHz x 128 issue slots / instructions per weight",
                 "hbm_view": {"achieved": hbm_rate, "peak": hbm, "unit": "GB/s",
                              "frac": hbm_rate / hbm, "algorithmic_bytes": code_bytes[dom],
