@@ -13,15 +13,15 @@
 // (N = tokens, K-major, loaded by TMA with 128-byte swizzle); fp16 operands,
 // fp32 accumulators in TMEM: two 256-column accumulators, so every decoded
 // weight serves up to 512 tokens.
-//   warps 0-7  decode: each takes one 16-input block of a 64-input K step (two
-//              K steps in flight), streams its code rows with cp.async into an
-//              interleaved (bank-conflict-free) ring, hashes each 32-bit
-//              window once, sums the codebook halves into fp16 (E4M3 rule if
-//              set), applies suh and stores 16-byte chunks into the swizzled
-//              A stage;
-//   warp 8     TMA producer of the B stages, and TMEM allocator;
-//   warp 9     one thread issues tcgen05.mma and commits stage releases.
-// The epilogue (warps 0-7) reads TMEM: gate/up launch -> svh * acc per
+//   warps 0..kDec-1  decode: each takes one 16-input block of a 64-input K
+//              step (kDec/4 K steps in flight), loads its code row one job
+//              ahead into registers (pulled into L2 8 jobs ahead), hashes each
+//              32-bit window once, sums the codebook halves into fp16 (E4M3
+//              rule if set), applies suh and stores 16-byte chunks into the
+//              swizzled A stage;
+//   warp kDec  TMA producer of the B stages, and TMEM allocator;
+//   warp kDec+1  one thread issues tcgen05.mma and commits stage releases.
+// The epilogue (the decoder warps) reads TMEM: gate/up launch -> svh * acc per
 // position (SwiGLU follows in the down projection's input pass); down launch
 // -> router weight * svh * acc into the pair's own row (no atomics).
 #include <cuda.h>
@@ -38,23 +38,22 @@ namespace {
 constexpr int kHalfN = 256;           // tokens per TMEM accumulator (MMA N)
 constexpr int kBN = 2 * kHalfN;       // tokens per tile
 constexpr int kKS = 64;               // inputs per K step
-constexpr int kDec = 8;               // decoder warps
+constexpr int kDec = 12;              // decoder warps
 constexpr int kThreads = (kDec + 2) * 32;
 constexpr int kJobs = 4;              // 16-input blocks per K step
 constexpr int kPar = kDec / kJobs;    // K steps decoded in parallel
-constexpr int kAStages = 2 * kPar;
+constexpr int kAStages = 5;           // A ring: decoders up to 5 K steps ahead
 constexpr int kAStage = 128 * kKS * 2;        // 16 KB
+constexpr int kBox = 64 * kKS * 2;            // one TMA box: 64 tokens x 64 inputs, 8 KB
 constexpr int kBStages = 2;
 constexpr int kBStage = kBN * kKS * 2;        // 64 KB
-constexpr int kCodeStages = 3;
-constexpr int kMaxCluster = 4;        // strips of one tile sharing activation loads
+constexpr int kMaxCluster = 2;        // strips of one tile sharing activation loads
 
 template <int K>
 struct GCfg {
-  static constexpr int kCodeChunk = 8 * 32 * K;
+  static constexpr int kCodeChunk = 8 * 32 * K;  // code bytes of one job (8 tiles)
   static constexpr int kOffB = kAStages * kAStage;
-  static constexpr int kOffCode = kOffB + kBStages * kBStage;
-  static constexpr int kOffScal = kOffCode + kDec * kCodeStages * kCodeChunk;
+  static constexpr int kOffScal = kOffB + kBStages * kBStage;
   static constexpr int kOffBar = kOffScal + kBN * 8;  // per-token scale and pair id
   static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
@@ -78,62 +77,6 @@ struct GemmParams {
   int32_t* status;
   int cluster;              // CTAs per cluster (divides the strip count)
 };
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* smem_dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Copy one code chunk (8 tiles of a 16-input block, 8K bytes per code lane)
-// into the ring slot in an interleaved order: piece q of code lane L sits at
-// (q * 32 + L) * piece, so that the per-lane loads below are conflict-free.
-template <int K>
-__device__ __forceinline__ void copy_codes(uint8_t* dst, const uint8_t* src, int lane) {
-  if constexpr (K == 2) {
-    cp_async16(dst + lane * 16, src + lane * 16);
-  } else if constexpr (K == 3) {
-#pragma unroll
-    for (int Q = 0; Q < 3; Q++) {
-      const int u = Q * 32 + lane;  // 8-byte unit of the chunk
-      cp_async8(dst + ((u % 3) * 32 + u / 3) * 8, src + u * 8);
-    }
-  } else {
-#pragma unroll
-    for (int Q = 0; Q < 2; Q++) {
-      const int u = Q * 32 + lane;  // 16-byte unit of the chunk
-      cp_async16(dst + ((u & 1) * 32 + (u >> 1)) * 16, src + u * 16);
-    }
-  }
-}
-
-template <int K>
-__device__ __forceinline__ void load_codes(LaneWords<K>& lw, const uint8_t* slot, int lane) {
-  if constexpr (K == 2) {
-    const uint4 v = *reinterpret_cast<const uint4*>(slot + lane * 16);
-    lw.w[0] = v.x; lw.w[1] = v.y; lw.w[2] = v.z; lw.w[3] = v.w;
-  } else if constexpr (K == 3) {
-#pragma unroll
-    for (int q = 0; q < 3; q++) {
-      const uint2 v = *reinterpret_cast<const uint2*>(slot + (q * 32 + lane) * 8);
-      lw.w[2 * q] = v.x; lw.w[2 * q + 1] = v.y;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 2; q++) {
-      const uint4 v = *reinterpret_cast<const uint4*>(slot + (q * 32 + lane) * 16);
-      lw.w[4 * q] = v.x; lw.w[4 * q + 1] = v.y; lw.w[4 * q + 2] = v.z; lw.w[4 * q + 3] = v.w;
-    }
-  }
-}
 
 // {a, b} halves of lane weights u = 16 pp .. 16 pp + 15.  For K = 2 and 4 each
 // 32-bit window is hashed once (a sliding window of 16 + 16/K products whose
@@ -209,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n0 = cnt < kHalfN ? ((cnt + 15) / 16) * 16 : kHalfN;
   const int n1 = cnt > kHalfN ? ((cnt - kHalfN + 15) / 16) * 16 : 0;
   const int nbox = (n0 + n1 + 63) / 64;
+  constexpr int nbst = kBStages, nast = kAStages;
+  const int bstage = kBStage;
+  uint8_t* const b_ring = smem + C::kOffB;
   const int nks = p.in / kKS;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -221,11 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kAStages; i++) {
+    for (int i = 0; i < nast; i++) {
       mbar_init(&a_full[i], kJobs);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < kBStages; i++) {
+    for (int i = 0; i < nbst; i++) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], p.cluster);  // released by the MMA of every CTA of the cluster
     }
@@ -260,21 +206,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every CTA of the cluster computes another strip of the same tile, so the
     // activation boxes are shared: CTA r loads boxes j = r (mod cluster) and
     // multicasts them; a stage is refilled once all CTAs released it.
+    // (single-thread loops: stage index and phase advance incrementally and
+    // the descriptors are precomputed, so nothing on this critical path
+    // divides)
     if (lane == 0) {
+      int sb = 0;
+      uint32_t pb = 0;
       for (int ks = 0; ks < nks; ks++) {
-        const int sb = ks % kBStages;
-        mbar_wait_or_abort(&b_empty[sb], ((ks / kBStages) & 1) ^ 1, p.status);
-        mbar_arrive_expect_tx(&b_full[sb], nbox * 64 * kKS * 2);
-        uint8_t* dst = smem + C::kOffB + sb * kBStage;
+        mbar_wait_or_abort(&b_empty[sb], pb ^ 1, p.status);
+        mbar_arrive_expect_tx(&b_full[sb], nbox * kBox);
+        uint8_t* dst = b_ring + sb * bstage;
         for (int j = crank; j < nbox; j += p.cluster)
-          tma_load_2d_multicast(dst + j * 64 * kKS * 2, &tmap_b, ks * kKS, pos0 + 64 * j,
-                                &b_full[sb], cmask);
+          tma_load_2d_multicast(dst + j * kBox, &tmap_b, ks * kKS, pos0 + 64 * j, &b_full[sb],
+                                cmask);
+        if (++sb == nbst) {
+          sb = 0;
+          pb ^= 1;
+        }
       }
       // before leaving: all boxes for this CTA have landed, and every CTA of
       // the cluster has released the last stages (their release arrives here)
-      for (int ks = nks - kBStages < 0 ? 0 : nks - kBStages; ks < nks; ks++) {
-        mbar_wait_or_abort(&b_full[ks % kBStages], (ks / kBStages) & 1, p.status);
-        mbar_wait_or_abort(&b_empty[ks % kBStages], (ks / kBStages) & 1, p.status);
+      for (int ks = nks - nbst < 0 ? 0 : nks - nbst; ks < nks; ks++) {
+        mbar_wait_or_abort(&b_full[ks % nbst], (ks / nbst) & 1, p.status);
+        mbar_wait_or_abort(&b_empty[ks % nbst], (ks / nbst) & 1, p.status);
       }
     }
   } else if (warp == kDec + 1) {
@@ -282,24 +236,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id0 = umma_idesc_f16(128, n0, 1, 0);
       const uint32_t id1 = umma_idesc_f16(128, n1 > 0 ? n1 : 16, 1, 0);
+      // descriptor address fields are byte addresses >> 4 (no carry below
+      // 256 KB), so stage and K-slice offsets are plain additions
+      const uint64_t a_desc0 = umma_desc(smem_u32(smem), 1024, 2048);
+      const uint64_t b_desc0 = umma_desc(smem_u32(b_ring), 16, 1024);
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
       for (int ks = 0; ks < nks; ks++) {
-        const int sa = ks % kAStages, sb = ks % kBStages;
-        mbar_wait_or_abort(&a_full[sa], (ks / kAStages) & 1, p.status);
-        mbar_wait_or_abort(&b_full[sb], (ks / kBStages) & 1, p.status);
+        mbar_wait_or_abort(&a_full[sa], pa, p.status);
+        mbar_wait_or_abort(&b_full[sb], pb, p.status);
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + sa * kAStage);
-        const uint32_t b_base = smem_u32(smem + C::kOffB + sb * kBStage);
+        const uint64_t ad = a_desc0 + (uint64_t)(sa * (kAStage >> 4));
+        const uint64_t bd = b_desc0 + (uint64_t)(sb * (bstage >> 4));
 #pragma unroll
         for (int kk = 0; kk < kKS / 16; kk++) {
-          const uint64_t adesc = umma_desc(a_base + kk * 4096, 1024, 2048);
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
-          umma_f16(tmem, adesc, umma_desc(b_base + kk * 32, 16, 1024), id0, acc);
+          umma_f16(tmem, ad + kk * (4096 >> 4), bd + kk * (32 >> 4), id0, acc);
           if (n1 > 0)
-            umma_f16(tmem + kHalfN, adesc, umma_desc(b_base + kHalfN * 128 + kk * 32, 16, 1024),
-                     id1, acc);
+            umma_f16(tmem + kHalfN, ad + kk * (4096 >> 4),
+                     bd + ((kHalfN * 128) >> 4) + kk * (32 >> 4), id1, acc);
         }
         umma_commit(&a_empty[sa]);
         umma_commit_multicast(&b_empty[sb], cmask);
+        if (++sa == nast) {
+          sa = 0;
+          pa ^= 1;
+        }
+        if (++sb == nbst) {
+          sb = 0;
+          pb ^= 1;
+        }
       }
       umma_commit(acc_full);
     }
@@ -308,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int blk = warp % kJobs;
     const int ks0 = warp / kJobs;
     const int g = lane >> 2, c = lane & 3;
-    uint8_t* ring = smem + C::kOffCode + warp * kCodeStages * C::kCodeChunk;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
                                                             (pj ? p.stride[1] : p.stride[0]) * e) +
@@ -323,13 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       off[idx] = (g >> 2) * 1024 + hf * 2048 + kr * 128 + (((2 * (g & 3) + jl) ^ kr) << 4);
     }
     const uint32_t neg16 = opaque_u32(0xFFFF0000u);
-    auto issue = [&](int n) {
+    // this lane's 8K code bytes of job n (code lane `lane` of the 8-tile chunk)
+    auto lane_codes = [&](int n) {
       const int ks = ks0 + n * kPar;
-      copy_codes<K>(ring + (n % kCodeStages) * C::kCodeChunk,
-                    cbase + (size_t)(ks * 4 + blk) * row_bytes, lane);
+      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
+             lane * 4 * K;
     };
-    // The shared ring is only a few jobs deep, so code rows are also pulled
-    // into L2 kL2Ahead jobs ahead: the ring's copies then hit L2.
+    // code rows are pulled into L2 kL2Ahead jobs ahead, so the register
+    // prefetch one job ahead hits L2
     constexpr int kL2Ahead = 8;
     auto prefetch_l2 = [&](int n) {
       if (n < n_my && lane * 128 < C::kCodeChunk) {
@@ -339,11 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
-#pragma unroll
-    for (int n = 0; n < kCodeStages - 1; n++) {
-      if (n < n_my) issue(n);
-      cp_async_commit();
-    }
     const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
     // suh of this lane's 4 inputs of a block, loaded one job ahead
     uint32_t s2n[4];
@@ -352,45 +313,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; q++) s2n[q] = __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
     };
-    if (n_my > 0) load_suh(0);
+    LaneWords<K> nxt;
+    if (n_my > 0) {
+      load_suh(0);
+      load_lane_words<K>(nxt, lane_codes(0));
+    }
+    // this warp's A stage and phase advance by kPar stages per job (kPar < nast)
+    int sa = ks0;
+    uint32_t pa = 0;
     for (int n = 0; n < n_my; n++) {
-      const int ks = ks0 + n * kPar;
-      const int sa = ks % kAStages;
-      if (n + kCodeStages - 1 < n_my) issue(n + kCodeStages - 1);
-      cp_async_commit();
+      LaneWords<K> lw = nxt;
+      if (n + 1 < n_my) load_lane_words<K>(nxt, lane_codes(n + 1));
       prefetch_l2(n + kL2Ahead);
       uint32_t s2[4];
 #pragma unroll
       for (int q = 0; q < 4; q++) s2[q] = s2n[q] | (s2n[q] << 16);
       if (n + 1 < n_my) load_suh(n + 1);
-      cp_async_wait<kCodeStages - 1>();
-      __syncwarp();
-      LaneWords<K> lw;
-      load_codes<K>(lw, ring + (n % kCodeStages) * C::kCodeChunk, lane);
       fetch_neighbour<K>(lw);
-      mbar_wait_or_abort(&a_empty[sa], ((ks / kAStages) & 1) ^ 1, p.status);
+      mbar_wait_or_abort(&a_empty[sa], pa ^ 1, p.status);
       decode_store<K, FP8>(lw, p.mult, neg16, smem + sa * kAStage + blk * 4096, off, s2);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
+      sa += kPar;
+      if (sa >= nast) {
+        sa -= nast;
+        pa ^= 1;
+      }
     }
-    cp_async_wait<0>();
 
     // ------------------------------------------------------------- epilogue
     mbar_wait_or_abort(acc_full, 0, p.status);
     tc_fence_after();
-    const int q4 = warp & 3, half = warp >> 2;
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its access quarter) and
+    // every (kDec/4)-th chunk of 16 token columns (column n = token n: the
+    // second accumulator starts at column kHalfN)
+    const int q4 = warp & 3, cgrp = warp >> 2;
     const int o = 128 * s + 32 * q4 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * kHalfN;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float sv = __half2float(__ushort_as_half((pj ? p.svh[1] : p.svh[0])[(size_t)e * p.out + o]));
-    const int base_n = half * kHalfN;
-    for (int c0 = 0; c0 < kHalfN && base_n + c0 < cnt; c0 += 16) {
+    for (int c0 = 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 16; i++) {
-        const int n = base_n + c0 + i;
+        const int n = c0 + i;
         if (n < cnt) {
           const float v = a0[i] * s_scale[n] * sv;
           if (p.gu_out)

@@ -46,21 +46,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait that lets the hardware suspend the warp (up to ~0.1 ms) until the
-// phase completes, instead of returning at once: waiting warps leave the
-// issue slots to the working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for the phase with the given parity; false when the budget ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -73,16 +58,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 
 // Bounded wait that also gives up as soon as any CTA has recorded a timeout
 // in the device status word (bit 4), so a stuck pipeline ends the whole grid
-// quickly instead of every CTA spending its own budget.
+// quickly instead of every CTA spending its own budget.  The status word (a
+// global load) is read only every kStatusPollCycles, so a wait that needs
+// a few retries is not slowed by memory round trips.
+constexpr long long kStatusPollCycles = 20000;  // ~10 us
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
                                                    int32_t* status) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity)) {
-    if (*reinterpret_cast<volatile int32_t*>(status) & 4) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
-      atomicOr(status, 4);
-      return false;
+  long long next_poll = t0 + kStatusPollCycles;
+  while (!mbar_try_wait(bar, parity)) {
+    const long long now = clock64();
+    if (now >= next_poll) {
+      if (*reinterpret_cast<volatile int32_t*>(status) & 4) return false;
+      if (now - t0 > kWaitBudgetCycles) {
+        atomicOr(status, 4);
+        return false;
+      }
+      next_poll = now + kStatusPollCycles;
     }
   }
   return true;
