@@ -122,11 +122,11 @@ def test_route_empty():
 # ------------------------------------------------------------------ layer
 
 
-def _run_small(spec, T, top_k, act, path=0, residual=False, seed=50):
+def _run_small(spec, T, top_k, act, path=0, residual=False, seed=50, routing="normal"):
     hl = HostLayer(spec)
     layer = hl.device()
     x = synth.activations(seed, T, spec.hidden, act)
-    logits = synth.router_logits(seed, T, spec.num_experts, "normal")
+    logits = synth.router_logits(seed, T, spec.num_experts, routing)
     xt = _act(x, act)
     res = _act(synth.activations(seed + 1, T, spec.hidden, act), act) if residual else None
     out = layer.forward(xt, torch.from_numpy(logits).cuda(), top_k, residual=res, path=path)
@@ -176,6 +176,21 @@ def test_forward_gemm_multi_tile(fp8):
         out, ref, layer = _run_small(spec, 300, 4, "bf16", path=path)
         assert_layer_close(out, ref)
         assert device_status(layer.workspace(300, 4)) == 0
+
+
+@pytest.mark.parametrize("T,k,routing,fp8", [
+    (40, 4, "normal", False),    # every expert segment <= 64 tokens: small-tile kernel only
+    (40, 4, "normal", True),
+    (700, 4, "zipf", True),      # skewed: big tiles, ragged remainders, small tiles together
+])
+def test_forward_gemm_small_tiles(T, k, routing, fp8):
+    """Tensor-core path on a shape whose H and I are multiples of 256, where
+    segments (or their last tile) of <= 64 tokens take the swapped-operand
+    small-tile kernel."""
+    spec = synth.LayerSpec(seed=77, num_experts=8, hidden=512, inter=256, K=(3, 3, 4), fp8_round=fp8)
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=2, routing=routing)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
 
 
 def test_forward_residual():

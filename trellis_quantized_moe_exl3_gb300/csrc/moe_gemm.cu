@@ -378,6 +378,263 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
+// ---------------------------------------------------------------------------
+// Small-tile variant (tiles of <= 64 tokens).  The tensor core's cost per
+// instruction is nearly flat up to N = 128, so for a tile this small the
+// operands are swapped: D[token][output] = sum_i x[token][i] W[i][output] with
+// A = the activation rows (M = 64 tokens, K-major, TMA) and B = the decoded
+// weights (N = 256 outputs, MN-major), one instruction covering twice the
+// weights of the M = 128 / N = 64 form.  One CTA = (tile, projection, 256
+// outputs = two code strips); 16 decoder warps (two K steps in flight), one
+// TMA warp, one MMA warp; the accumulator holds token 16q + i in TMEM lane
+// 32q + i (q = 0..3), column = output.
+constexpr int kSN = 256;                       // outputs per CTA (MMA N)
+constexpr int kSM = 64;                        // tokens (MMA M)
+constexpr int kSDec = 16;                      // decoder warps
+constexpr int kSThreads = (kSDec + 2) * 32;
+constexpr int kSJobs = 8;                      // jobs per K step: 4 blocks x 2 strips
+constexpr int kSPar = kSDec / kSJobs;          // K steps decoded in parallel
+constexpr int kSWStages = 5;                   // decoded-weight stages
+constexpr int kSWStage = kSN * kKS * 2;        // 32 KB
+constexpr int kSXStages = 4;                   // activation stages
+constexpr int kSXStage = kSM * kKS * 2;        // 8 KB
+
+struct SCfg {
+  static constexpr int kOffX = kSWStages * kSWStage;
+  static constexpr int kOffScal = kOffX + kSXStages * kSXStage;
+  static constexpr int kOffBar = kOffScal + kSM * 8;
+  static constexpr int kNumBars = 2 * kSWStages + 2 * kSXStages + 1;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
+};
+
+template <int K, int FP8>
+__global__ void __launch_bounds__(kSThreads, 1)
+    gemm64_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const int chunks = p.out / kSN;
+  const int s = blockIdx.x % chunks;
+  const int pj = (blockIdx.x / chunks) % p.nproj;
+  const int tile = blockIdx.x / (chunks * p.nproj);
+  pdl_wait();
+  if (tile >= p.n_tiles[0]) return;  // the whole cluster shares the tile
+  const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
+  const int nks = p.in / kKS;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SCfg::kOffBar);
+  uint64_t* w_full = bars;
+  uint64_t* w_empty = w_full + kSWStages;
+  uint64_t* x_full = w_empty + kSWStages;
+  uint64_t* x_empty = x_full + kSXStages;
+  uint64_t* acc_full = x_empty + kSXStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint8_t* const x_ring = smem + SCfg::kOffX;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSWStages; i++) {
+      mbar_init(&w_full[i], kSJobs);
+      mbar_init(&w_empty[i], 1);
+    }
+    for (int i = 0; i < kSXStages; i++) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], p.cluster);  // released by the MMA of every CTA of the cluster
+    }
+    mbar_init(acc_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == kSDec) tmem_alloc(tmem_slot, kSN);
+  float* s_scale = reinterpret_cast<float*>(smem + SCfg::kOffScal);
+  int32_t* s_pid = reinterpret_cast<int32_t*>(s_scale + kSM);
+  for (int n = threadIdx.x; n < cnt; n += blockDim.x) {
+    const int pos = pos0 + n;
+    float sc = p.xinv[pos];
+    int pid = 0;
+    if (!p.gu_out) {
+      pid = p.seg_pairs[pos];
+      sc *= p.wts[pid];
+    }
+    s_scale[n] = sc;
+    s_pid[n] = pid;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peers may multicast into this CTA only after its barriers exist
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1);
+  const int crank = (int)cluster_ctarank();
+
+  if (warp == kSDec) {
+    // ---------------------------------------------------------------- TMA
+    // one 64-token box per K step, loaded by the cluster's first CTA and
+    // multicast to every CTA of the cluster (each computes other outputs)
+    if (lane == 0) {
+      int sx = 0;
+      uint32_t px = 0;
+      for (int ks = 0; ks < nks; ks++) {
+        mbar_wait_or_abort(&x_empty[sx], px ^ 1, p.status);
+        mbar_arrive_expect_tx(&x_full[sx], kSXStage);
+        if (crank == 0)
+          tma_load_2d_multicast(x_ring + sx * kSXStage, &tmap_x, ks * kKS, pos0, &x_full[sx], cmask);
+        if (++sx == kSXStages) {
+          sx = 0;
+          px ^= 1;
+        }
+      }
+      for (int ks = nks - kSXStages < 0 ? 0 : nks - kSXStages; ks < nks; ks++) {
+        mbar_wait_or_abort(&x_full[ks % kSXStages], (ks / kSXStages) & 1, p.status);
+        mbar_wait_or_abort(&x_empty[ks % kSXStages], (ks / kSXStages) & 1, p.status);
+      }
+    }
+  } else if (warp == kSDec + 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      // A: activations K-major (8-row atoms 1024 B apart, K slice +32 B);
+      // B: decoded weights MN-major (64-output atoms 1024 B apart, 8-input
+      // groups 4096 B apart, K slice of 16 = +8192 B)
+      const uint32_t idesc = umma_idesc_f16(kSM, kSN, 0, 1);
+      const uint64_t x_desc0 = umma_desc(smem_u32(x_ring), 16, 1024);
+      const uint64_t w_desc0 = umma_desc(smem_u32(smem), 1024, 4096);
+      int sw = 0, sx = 0;
+      uint32_t pw = 0, px = 0;
+      for (int ks = 0; ks < nks; ks++) {
+        mbar_wait_or_abort(&w_full[sw], pw, p.status);
+        mbar_wait_or_abort(&x_full[sx], px, p.status);
+        tc_fence_after();
+        const uint64_t xd = x_desc0 + (uint64_t)(sx * (kSXStage >> 4));
+        const uint64_t wd = w_desc0 + (uint64_t)(sw * (kSWStage >> 4));
+#pragma unroll
+        for (int kk = 0; kk < kKS / 16; kk++)
+          umma_f16(tmem, xd + kk * (32 >> 4), wd + kk * (8192 >> 4), idesc,
+                   (ks > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&w_empty[sw]);
+        umma_commit_multicast(&x_empty[sx], cmask);
+        if (++sw == kSWStages) {
+          sw = 0;
+          pw ^= 1;
+        }
+        if (++sx == kSXStages) {
+          sx = 0;
+          px ^= 1;
+        }
+      }
+      umma_commit(acc_full);
+    }
+  } else {
+    // ---------------------------------------------------------------- decode
+    // warp w: 16-input block w % 4 of code strip 2s + (w / 4) % 2, K steps
+    // ks = w / 8 (mod 2)
+    const int blk = warp % 4;
+    const int half = (warp / 4) % 2;
+    const int ks0 = warp / kSJobs;
+    const int g = lane >> 2, c = lane & 3;
+    const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
+    const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
+                                                            (pj ? p.stride[1] : p.stride[0]) * e) +
+                           (size_t)8 * (2 * s + half) * 32 * K;
+    const int n_my = (nks - ks0 + kSPar - 1) / kSPar;
+    int off[8];
+#pragma unroll
+    for (int idx = 0; idx < 8; idx++) {
+      const int hf = idx >> 2, jh = (idx >> 1) & 1, jl = idx & 1;
+      const int kr = c + 4 * jh;
+      off[idx] = (g >> 2) * 1024 + hf * 4096 + kr * 128 + (((2 * (g & 3) + jl) ^ kr) << 4);
+    }
+    const int job_off = blk * 8192 + half * 2048;
+    const uint32_t neg16 = opaque_u32(0xFFFF0000u);
+    auto lane_codes = [&](int n) {
+      const int ks = ks0 + n * kSPar;
+      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
+             lane * 4 * K;
+    };
+    constexpr int kL2Ahead = 8;
+    auto prefetch_l2 = [&](int n) {
+      if (n < n_my && lane * 128 < 8 * 32 * K) {
+        const int ks = ks0 + n * kSPar;
+        const uint8_t* a = cbase + (size_t)(ks * 4 + blk) * row_bytes + lane * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      }
+    };
+    for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
+    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
+    uint32_t s2n[4];
+    auto load_suh = [&](int n) {
+      const int ks = ks0 + n * kSPar;
+#pragma unroll
+      for (int q = 0; q < 4; q++) s2n[q] = __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+    };
+    LaneWords<K> nxt;
+    if (n_my > 0) {
+      load_suh(0);
+      load_lane_words<K>(nxt, lane_codes(0));
+    }
+    int sw = ks0;
+    uint32_t pw = 0;
+    for (int n = 0; n < n_my; n++) {
+      LaneWords<K> lw = nxt;
+      if (n + 1 < n_my) load_lane_words<K>(nxt, lane_codes(n + 1));
+      prefetch_l2(n + kL2Ahead);
+      uint32_t s2[4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) s2[q] = s2n[q] | (s2n[q] << 16);
+      if (n + 1 < n_my) load_suh(n + 1);
+      fetch_neighbour<K>(lw);
+      mbar_wait_or_abort(&w_empty[sw], pw ^ 1, p.status);
+      decode_store<K, FP8>(lw, p.mult, neg16, smem + sw * kSWStage + job_off, off, s2);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&w_full[sw]);
+      sw += kSPar;
+      if (sw >= kSWStages) {
+        sw -= kSWStages;
+        pw ^= 1;
+      }
+    }
+
+    // ------------------------------------------------------------- epilogue
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31: lanes 0..15 hold tokens
+    // 16 (w % 4) + lane; it takes output columns 64 (w / 4) .. + 63
+    mbar_wait_or_abort(acc_full, 0, p.status);
+    tc_fence_after();
+    const int q4 = warp & 3, cg = warp >> 2;
+    const int n = 16 * q4 + lane;  // token of this lane (lane < 16)
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + kSN * s;
+    for (int c0 = 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
+      float a0[16];
+      tmem_ld16(trow + c0, a0);
+      tmem_ld_wait();
+      if (lane < 16 && n < cnt) {
+        const uint4 sva = __ldg(reinterpret_cast<const uint4*>(svh + c0));
+        const uint4 svb = __ldg(reinterpret_cast<const uint4*>(svh + c0 + 8));
+        const uint32_t sw8[8] = {sva.x, sva.y, sva.z, sva.w, svb.x, svb.y, svb.z, svb.w};
+        const float sc = s_scale[n];
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+          const uint32_t w2 = sw8[j >> 1];
+          const float sv = __half2float(__ushort_as_half((unsigned short)(j & 1 ? w2 >> 16 : w2 & 0xFFFFu)));
+          v[j] = a0[j] * sc * sv;
+        }
+        float* dst = p.gu_out ? p.gu_out + ((size_t)pj * p.n_pos + pos0 + n) * p.out
+                              : p.r_out + (size_t)s_pid[n] * p.out;
+        float4* d4 = reinterpret_cast<float4*>(dst + kSN * s + c0);
+#pragma unroll
+        for (int q = 0; q < 4; q++) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kSDec) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kSN);
+  }
+  cluster_sync();  // no CTA leaves while a peer may still signal its barriers
+}
+
 // Row kernels: one warp per position row, 16-byte vector accesses; the first
 // kRowCache chunks of 32 lanes x 8 (gather) or x 4 (swiglu) elements stay in
 // registers between the max pass and the write pass, the rest are re-read.
@@ -507,16 +764,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
   if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex);
 }
 
-// Token tiles of <= kBN positions per expert segment (one CTA, thread per expert).
-__global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t* seg_offsets,
-                                                           int32_t* tiles, int32_t* n_tiles) {
-  pdl_wait();
-  __shared__ int s_warp[32];
-  const int e = threadIdx.x;
-  const int cnt = e < E ? seg_offsets[e + 1] - seg_offsets[e] : 0;
-  const int nt = (cnt + kBN - 1) / kBN;
-  const int lane = e & 31, wid = e >> 5, nw = blockDim.x >> 5;
-  int x = nt;
+// Token tiles per expert segment (one CTA, thread per expert): tiles of
+// <= kBN positions in `tiles`; an expert's last tile (or its only one) goes
+// to `tiles_s` instead when it holds <= kSM positions and use_small is set
+// (the small-tile kernel).
+// n_tiles[0] / n_tiles[1] receive the two counts.
+__device__ int block_excl_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
   for (int off = 1; off < 32; off <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, off);
     if (lane >= off) x += y;
@@ -524,26 +779,55 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t*
   if (lane == 31) s_warp[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int v = lane < nw ? s_warp[lane] : 0;
+    int u = lane < nw ? s_warp[lane] : 0;
     for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, v, off);
-      if (lane >= off) v += y;
+      const int y = __shfl_up_sync(0xffffffffu, u, off);
+      if (lane >= off) u += y;
     }
-    if (lane < nw) s_warp[lane] = v;
+    if (lane < nw) s_warp[lane] = u;
   }
   __syncthreads();
-  const int base = (wid > 0 ? s_warp[wid - 1] : 0) + x - nt;
+  const int r = (wid > 0 ? s_warp[wid - 1] : 0) + x - v;
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t* seg_offsets,
+                                                           int use_small, int32_t* tiles,
+                                                           int32_t* tiles_s, int32_t* n_tiles) {
+  pdl_wait();
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  const int cnt = e < E ? seg_offsets[e + 1] - seg_offsets[e] : 0;
+  const int nt = (cnt + kBN - 1) / kBN;
+  const int last = nt > 0 ? cnt - (nt - 1) * kBN : 0;
+  const int small = use_small && nt > 0 && last <= kSM ? 1 : 0;
+  const int nbig = nt - small;
+  int tot_b = 0, tot_s = 0;
+  const int base_b = block_excl_scan(nbig, s_warp, &tot_b);
+  const int base_s = block_excl_scan(small, s_warp, &tot_s);
   if (e < E) {
     const int off = seg_offsets[e];
-    for (int j = 0; j < nt; j++) {
-      int32_t* t = tiles + (size_t)(base + j) * 4;
+    for (int j = 0; j < nbig; j++) {
+      int32_t* t = tiles + (size_t)(base_b + j) * 4;
       t[0] = e;
       t[1] = off + j * kBN;
       t[2] = min(kBN, cnt - j * kBN);
       t[3] = 0;
     }
+    if (small) {
+      int32_t* t = tiles_s + (size_t)base_s * 4;
+      t[0] = e;
+      t[1] = off + nbig * kBN;
+      t[2] = last;
+      t[3] = 0;
+    }
   }
-  if (threadIdx.x == 0) n_tiles[0] = s_warp[nw - 1];
+  if (threadIdx.x == 0) {
+    n_tiles[0] = tot_b;
+    n_tiles[1] = tot_s;
+  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -606,6 +890,46 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   return err;
 }
 
+template <int K, int FP8>
+cudaError_t launch_gemm64(const CUtensorMap& tm, const GemmParams& gp, int grid, cudaStream_t st) {
+  static bool init = false;
+  auto kfn = gemm64_kernel<K, FP8>;
+  if (!init) {
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg::kSmem);
+    if (e != cudaSuccess) return e;
+    init = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.dynamicSmemBytes = SCfg::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = gp.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kfn, tm, gp);
+  note_launches(1);
+  return err;
+}
+
+cudaError_t dispatch_gemm64(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
+                            cudaStream_t st) {
+  if (fp8) {
+    if (K == 2) return launch_gemm64<2, 1>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm64<3, 1>(tm, gp, grid, st);
+    return launch_gemm64<4, 1>(tm, gp, grid, st);
+  }
+  if (K == 2) return launch_gemm64<2, 0>(tm, gp, grid, st);
+  if (K == 3) return launch_gemm64<3, 0>(tm, gp, grid, st);
+  return launch_gemm64<4, 0>(tm, gp, grid, st);
+}
+
 cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
                           cudaStream_t st) {
   if (fp8) {
@@ -634,7 +958,7 @@ size_t max_tiles(int T, int E, int top_k) {
 }
 
 struct GemmLayout {
-  size_t xg, xinv, gu, hs, hinv, r, tiles, ntiles, total;
+  size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, total;
 };
 
 GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
@@ -648,6 +972,7 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
   g.hinv = o; o += al(P * 4);
   g.r = o; o += al(P * H * 4);
   g.tiles = o; o += al(max_tiles(T, E, top_k) * 16);
+  g.tiles_s = o; o += al((size_t)E * 16);
   g.ntiles = o; o += al(16);
   g.total = o;
   return g;
@@ -674,6 +999,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   float* hinv = reinterpret_cast<float*>(base + g.hinv);
   float* r = reinterpret_cast<float*>(base + g.r);
   int32_t* tiles = reinterpret_cast<int32_t*>(base + g.tiles);
+  int32_t* tiles_s = reinterpret_cast<int32_t*>(base + g.tiles_s);
   int32_t* ntiles = reinterpret_cast<int32_t*>(base + g.ntiles);
   *r_out = r;
   const int P = T * top_k;
@@ -682,8 +1008,13 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   if (!make_tmap(&tm_x, xg, (size_t)P, (size_t)L.H) || !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I))
     return cudaErrorInvalidValue;
   cudaError_t err;
+  // grids: big tiles on 128-output strips, small tiles on 256-output chunks
+  // (the small-tile kernel needs H and I to be multiples of 256; otherwise
+  // every tile takes the big-tile kernel)
+  const bool small_ok = L.H % kSN == 0 && L.I % kSN == 0;
   if ((err = launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, st, L.E,
-                        (const int32_t*)rb.seg_offsets, tiles, ntiles)) != cudaSuccess)
+                        (const int32_t*)rb.seg_offsets, (int)small_ok, tiles, tiles_s, ntiles)) !=
+      cudaSuccess)
     return err;
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
   err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H,
@@ -704,6 +1035,14 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   // gate and up share one launch, so they share a width (checked at create)
   if ((err = dispatch_gemm(L.K[0], L.fp8, tm_x, gu, mt * 2 * (L.I / 128), st)) != cudaSuccess)
     return err;
+  if (small_ok) {
+    GemmParams gs = gu;
+    gs.tiles = tiles_s;
+    gs.n_tiles = ntiles + 1;
+    gs.cluster = cluster_for(L.I / kSN);
+    if ((err = dispatch_gemm64(L.K[0], L.fp8, tm_x, gs, L.E * 2 * (L.I / kSN), st)) != cudaSuccess)
+      return err;
+  }
   rec(3);
 
   err = launch_pdl(swiglu_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
@@ -720,6 +1059,13 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
   dn.cluster = cluster_for(L.H / 128);
   err = dispatch_gemm(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
+  if (err == cudaSuccess && small_ok) {
+    GemmParams ds = dn;
+    ds.tiles = tiles_s;
+    ds.n_tiles = ntiles + 1;
+    ds.cluster = cluster_for(L.H / kSN);
+    err = dispatch_gemm64(L.K[2], L.fp8, tm_h, ds, L.E * (L.H / kSN), st);
+  }
   rec(5);
   return err;
 }
