@@ -181,11 +181,12 @@ def test_forward_gemm_multi_tile(fp8):
 @pytest.mark.parametrize("T,k,routing,fp8", [
     (40, 4, "normal", False),    # every expert segment <= 64 tokens: small-tile kernel only
     (40, 4, "normal", True),
+    (120, 4, "normal", False),   # segments of ~40-80 tokens: both small-tile widths (M 64, 128)
     (700, 4, "zipf", True),      # skewed: big tiles, ragged remainders, small tiles together
 ])
 def test_forward_gemm_small_tiles(T, k, routing, fp8):
     """Tensor-core path on a shape whose H and I are multiples of 256, where
-    segments (or their last tile) of <= 64 tokens take the swapped-operand
+    segments (or their last tile) of <= 128 tokens take the swapped-operand
     small-tile kernel."""
     spec = synth.LayerSpec(seed=77, num_experts=8, hidden=512, inter=256, K=(3, 3, 4), fp8_round=fp8)
     out, ref, layer = _run_small(spec, T, k, "bf16", path=2, routing=routing)

@@ -379,17 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Small-tile variant (tiles of <= 64 tokens).  The tensor core's cost per
+// Small-tile variant (tiles of <= 128 tokens).  The tensor core's cost per
 // instruction is nearly flat up to N = 128, so for a tile this small the
 // operands are swapped: D[token][output] = sum_i x[token][i] W[i][output] with
-// A = the activation rows (M = 64 tokens, K-major, TMA) and B = the decoded
-// weights (N = 256 outputs, MN-major), one instruction covering twice the
-// weights of the M = 128 / N = 64 form.  One CTA = (tile, projection, 256
-// outputs = two code strips); 16 decoder warps (two K steps in flight), one
-// TMA warp, one MMA warp; the accumulator holds token 16q + i in TMEM lane
-// 32q + i (q = 0..3), column = output.
+// A = the activation rows (M = 64 or 128 tokens, K-major, TMA) and B = the
+// decoded weights (N = 256 outputs, MN-major): one instruction covers 2x (M 64)
+// or 4x (M 128) the weights of the M = 128 / N = 64 form.  One CTA = (tile,
+// projection, 256 outputs = two code strips); 16 decoder warps (two K steps
+// in flight), one TMA warp, one MMA warp.  The accumulator holds, per TMEM
+// lane quarter q, tokens 16q + i (M 64, lanes 32q + i, i < 16) or 32q + i
+// (M 128); column = output.
 constexpr int kSN = 256;                       // outputs per CTA (MMA N)
-constexpr int kSM = 64;                        // tokens (MMA M)
+constexpr int kSM = 128;                       // tokens at most (MMA M 64 or 128)
 constexpr int kSDec = 16;                      // decoder warps
 constexpr int kSThreads = (kSDec + 2) * 32;
 constexpr int kSJobs = 8;                      // jobs per K step: 4 blocks x 2 strips
@@ -397,7 +398,7 @@ constexpr int kSPar = kSDec / kSJobs;          // K steps decoded in parallel
 constexpr int kSWStages = 5;                   // decoded-weight stages
 constexpr int kSWStage = kSN * kKS * 2;        // 32 KB
 constexpr int kSXStages = 4;                   // activation stages
-constexpr int kSXStage = kSM * kKS * 2;        // 8 KB
+constexpr int kSXStage = kSM * kKS * 2;        // 16 KB (M 64 uses the first half)
 
 struct SCfg {
   static constexpr int kOffX = kSWStages * kSWStage;
@@ -406,6 +407,7 @@ struct SCfg {
   static constexpr int kNumBars = 2 * kSWStages + 2 * kSXStages + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
 };
+static_assert(SCfg::kSmem <= 227 * 1024, "small-tile kernel shared memory");
 
 template <int K, int FP8>
 __global__ void __launch_bounds__(kSThreads, 1)
@@ -421,6 +423,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (tile >= p.n_tiles[0]) return;  // the whole cluster shares the tile
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int nks = p.in / kKS;
+  const int tm = cnt <= 64 ? 64 : 128;  // MMA M
+  const int nxbox = tm / 64;            // 64-token boxes per activation stage
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SCfg::kOffBar);
   uint64_t* w_full = bars;
@@ -468,16 +472,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   if (warp == kSDec) {
     // ---------------------------------------------------------------- TMA
-    // one 64-token box per K step, loaded by the cluster's first CTA and
-    // multicast to every CTA of the cluster (each computes other outputs)
+    // one or two 64-token boxes per K step; CTA r of the cluster loads boxes
+    // j = r (mod cluster) and multicasts them (every CTA computes other outputs)
     if (lane == 0) {
       int sx = 0;
       uint32_t px = 0;
       for (int ks = 0; ks < nks; ks++) {
         mbar_wait_or_abort(&x_empty[sx], px ^ 1, p.status);
-        mbar_arrive_expect_tx(&x_full[sx], kSXStage);
-        if (crank == 0)
-          tma_load_2d_multicast(x_ring + sx * kSXStage, &tmap_x, ks * kKS, pos0, &x_full[sx], cmask);
+        mbar_arrive_expect_tx(&x_full[sx], nxbox * kBox);
+        for (int j = crank; j < nxbox; j += p.cluster)
+          tma_load_2d_multicast(x_ring + sx * kSXStage + j * kBox, &tmap_x, ks * kKS, pos0 + 64 * j,
+                                &x_full[sx], cmask);
         if (++sx == kSXStages) {
           sx = 0;
           px ^= 1;
@@ -494,7 +499,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // A: activations K-major (8-row atoms 1024 B apart, K slice +32 B);
       // B: decoded weights MN-major (64-output atoms 1024 B apart, 8-input
       // groups 4096 B apart, K slice of 16 = +8192 B)
-      const uint32_t idesc = umma_idesc_f16(kSM, kSN, 0, 1);
+      const uint32_t idesc = umma_idesc_f16(tm, kSN, 0, 1);
       const uint64_t x_desc0 = umma_desc(smem_u32(x_ring), 16, 1024);
       const uint64_t w_desc0 = umma_desc(smem_u32(smem), 1024, 4096);
       int sw = 0, sx = 0;
@@ -594,19 +599,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
 
     // ------------------------------------------------------------- epilogue
-    // warp w reads TMEM lanes 32 (w % 4) .. + 31: lanes 0..15 hold tokens
-    // 16 (w % 4) + lane; it takes output columns 64 (w / 4) .. + 63
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31, which hold tokens
+    // 16 (w % 4) + lane, lane < 16 (M 64) or 32 (w % 4) + lane (M 128); it
+    // takes output columns 64 (w / 4) .. + 63
     mbar_wait_or_abort(acc_full, 0, p.status);
     tc_fence_after();
     const int q4 = warp & 3, cg = warp >> 2;
-    const int n = 16 * q4 + lane;  // token of this lane (lane < 16)
+    const bool lane_live = tm == 128 || lane < 16;
+    const int n = (tm == 128 ? 32 : 16) * q4 + lane;  // token of this lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + kSN * s;
     for (int c0 = 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait();
-      if (lane < 16 && n < cnt) {
+      if (lane_live && n < cnt) {
         const uint4 sva = __ldg(reinterpret_cast<const uint4*>(svh + c0));
         const uint4 svb = __ldg(reinterpret_cast<const uint4*>(svh + c0 + 8));
         const uint32_t sw8[8] = {sva.x, sva.y, sva.z, sva.w, svb.x, svb.y, svb.z, svb.w};
