@@ -58,6 +58,27 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's own token batch (weak scaling: every rank runs its own)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(value: float, device, world: int) -> float:
+    """The largest of the ranks' values (the job's wall time is its slowest rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the (max) time."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # the decode step's expert kernels, from one ncu capture summarised in
 # profiles/gemv_kernel_K2_decode.md; reported only while the kernel sources
@@ -168,8 +189,10 @@ def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
         ol.shared_row(x[0], wl.act == "bf16")
     t_shared = time.perf_counter() - t1
     per_token = wl.top_k * t_pairs + t_shared
-    sample = (f"{n_pairs} (token, expert) pair(s) of the {wl.T}-token decode step + the shared "
-              f"expert of one token; tokens/s = 1 / ({wl.top_k} x pair time + shared time)")
+    sample = (f"{n_pairs} (token, expert) pair(s) of the {wl.T}-token {wl.name} workload"
+              + (" + the shared expert of one token" if shared_w is not None else "")
+              + f"; tokens/s = 1 / ({wl.top_k} x pair time"
+              + (" + shared time)" if shared_w is not None else ")"))
     return 1.0 / per_token, time.perf_counter() - t0, sample
 
 
@@ -182,31 +205,34 @@ def run_reference(args):
 
     import oracle
     from trellis_quantized_moe_exl3_gb300 import synth
-    wl = synth.WORKLOADS[WORKLOAD]
-    spec = wl.layers[0]
-    x, logits = synth.workload_inputs(wl)
+    wl, spec = pick_workload(args)
+    x = synth.activations(wl.seed, wl.T, spec.hidden, wl.act)
+    logits = synth.router_logits(spec.seed, wl.T, spec.num_experts, wl.routing)
     codes = [synth.layer_codes(spec, p) for p in range(3)]
     sides = [synth.side_vectors(spec, p) for p in range(3)]
-    sw = synth.shared_weights(spec)
+    sw = synth.shared_weights(spec) if spec.shared else None
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
-                      [s[0] for s in sides], [s[1] for s in sides], shared_w=sw)
+                      [s[0] for s in sides], [s[1] for s in sides], shared_w=sw,
+                      fp8_round=spec.fp8_round)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
     for s in range(args.warmup):
         t, j = pairs[s % len(pairs)]
-        ol.expert_pair(x[t], True, int(ids[t, j]), float(w[t, j]))
+        ol.expert_pair(x[t], wl.act == "bf16", int(ids[t, j]), float(w[t, j]))
     ts = time.perf_counter()
-    ol.shared_row(x[0], True)
+    if sw is not None:
+        ol.shared_row(x[0], wl.act == "bf16")
     t_shared = time.perf_counter() - ts
     t0 = time.perf_counter()
     for s in range(args.steps):
         t, j = pairs[(args.warmup + s) % len(pairs)]
-        ol.expert_pair(x[t], True, int(ids[t, j]), float(w[t, j]))
+        ol.expert_pair(x[t], wl.act == "bf16", int(ids[t, j]), float(w[t, j]))
     t_pair = (time.perf_counter() - t0) / args.steps
     per_token = wl.top_k * t_pair + t_shared
     value = 1.0 / per_token
-    sample = (f"one (token, expert) pair of the {wl.T}-token decode step per step; tokens/s = "
-              f"1 / ({wl.top_k} x mean pair time + shared-expert time of one token)")
+    sample = (f"one (token, expert) pair of the {wl.T}-token {wl.name} workload per step; tokens/s = "
+              f"1 / ({wl.top_k} x mean pair time"
+              + (" + shared-expert time of one token)" if sw is not None else ")"))
     line = {
         "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -269,8 +295,8 @@ def run_ours(args):
     sides = [synth.side_vectors(spec, p) for p in range(3)]
     sw = synth.shared_weights(spec) if spec.shared else None
     # every rank runs its own token batch (weak scaling)
-    x_np = synth.activations(wl.seed + 1000 * rank, wl.T, spec.hidden, wl.act)
-    lg_np = synth.router_logits(spec.seed + 1000 * rank, wl.T, spec.num_experts, wl.routing)
+    x_np = synth.activations(rank_seed(wl.seed, rank), wl.T, spec.hidden, wl.act)
+    lg_np = synth.router_logits(rank_seed(spec.seed, rank), wl.T, spec.num_experts, wl.routing)
 
     t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
     d_codes = [t16(c) for c in codes]
@@ -372,13 +398,9 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in zip(start_ev, end_ev)]
-    tot = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([tot], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot = float(t.item())
+    tot = max_over_ranks(float(np.sum(step_ms)), dev, world)
     ms_per_step = tot / args.steps
-    value = world * T * args.steps / (tot / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, tot)
 
     # stage times: the stage graph (or eager forwards with the events set)
     stage_ms = np.zeros(n_ev - 1)
@@ -419,12 +441,8 @@ def run_ours(args):
             e1.synchronize()
             if i >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
-    e2e_tot = float(np.sum(e2e_ms))
-    if world > 1:
-        t = torch.tensor([e2e_tot], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_tot = float(t.item())
-    e2e_value = world * T * args.steps / (e2e_tot / 1e3)
+    e2e_tot = max_over_ranks(float(np.sum(e2e_ms)), dev, world)
+    e2e_value = job_tokens_per_s(world, T, args.steps, e2e_tot)
 
     # roofline of the dominant expert kernel (the larger of gate/up and down)
     hbm, bf16_tf, src = peaks()

@@ -1,0 +1,51 @@
+"""Host logic of bench.py's multi-GPU path (one replica per rank, weak
+scaling), run as two gloo ranks on the CPU: every rank gets its own token
+batch, the job time is the slowest rank's, and the job throughput counts the
+tokens of all ranks."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r pretends its timed steps took 10 + r ms
+        mine = 10.0 + rank
+        got = bench.max_over_ranks(mine, torch.device("cpu"), world)
+        out[rank] = (got, bench.rank_seed(7, rank))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True,
+                           start_method="spawn")
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 11.0          # both ranks report the max
+    assert res[0][1] != res[1][1]                  # distinct token batches
+
+
+def test_job_throughput_counts_every_rank():
+    # 2 ranks x 4 tokens x 10 steps in 5 ms = 16,000 tokens/s
+    assert bench.job_tokens_per_s(2, 4, 10, 5.0) == pytest.approx(16000.0)
+    assert bench.max_over_ranks(3.0, torch.device("cpu"), 1) == 3.0
