@@ -745,13 +745,23 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
   auto amax4 = [](float a, const float4& h) {
     return fmaxf(fmaxf(a, fabsf(h.x)), fmaxf(fmaxf(fabsf(h.y), fabsf(h.z)), fabsf(h.w)));
   };
-  float4 c[kRowCache];
+  // the row's first chunks: every load issued before the first SiLU
+  float4 c[kRowCache], cu[kRowCache];
   float am = 0.0f;
 #pragma unroll
   for (int i = 0; i < kRowCache; i++) {
     const int v = i * 32 + lane;
     if (v < nv) {
-      c[i] = h4(v);
+      c[i] = __ldcs(gr + v);
+      cu[i] = __ldcs(ur + v);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kRowCache; i++) {
+    const int v = i * 32 + lane;
+    if (v < nv) {
+      c[i] = make_float4(silu_f(c[i].x) * cu[i].x, silu_f(c[i].y) * cu[i].y,
+                         silu_f(c[i].z) * cu[i].z, silu_f(c[i].w) * cu[i].w);
       am = amax4(am, c[i]);
     }
   }
