@@ -11,9 +11,9 @@
 // device counter (an item's successor is taken while its last blocks are
 // still being copied), so the load stays balanced whatever the expert mix.
 // Each warp runs its own asynchronous-copy ring (cp.async, 16 bytes per lane,
-// several blocks ahead, across item boundaries): per 16-input block the code
-// row of the strip (8 consecutive tiles, 8K bytes per lane) and the matching
-// activation rows (8 tokens x 16 inputs).  Every lane then decodes its 64
+// several jobs of two 16-input blocks ahead, across item boundaries): per
+// block the code row of the strip (8 consecutive tiles, 8K bytes per lane) and
+// the matching activation rows (8 tokens x 16 inputs).  Every lane then decodes its 64
 // weights in registers (the 16-K bit window overlap comes from the next lane
 // of the quad by shuffle) and feeds mma.m16n8k16 with the K dimension
 // doubled: the A register of weight (o, i) is the codebook's {a, b} fp16 pair
@@ -42,12 +42,16 @@ namespace {
 constexpr int kCW = 8;                     // warps per CTA
 constexpr int kThreads = kCW * 32;
 constexpr int kXsChunk = kGroup * 16 * 4;  // 8 tokens x 16 inputs x fp16x2
+constexpr int kJobBlocks = 2;              // 16-input blocks per ring job
 
 template <int K>
 struct Cfg {
   static constexpr int kCodeChunk = 8 * 32 * K;  // 8 tiles of one 16-input block
-  static constexpr int kSlot = kCodeChunk + kXsChunk;
-  static constexpr int kStages = K == 2 ? 6 : (K == 3 ? 5 : 4);  // per-warp ring depth
+  static constexpr int kBlkBytes = kCodeChunk + kXsChunk;
+  static constexpr int kSlot = kJobBlocks * kBlkBytes;              // one job: 2 blocks
+  // per-warp ring depth in jobs; at most 4, the fewest jobs of an item
+  // (8 blocks), which keeps the producer within one item of the consumer
+  static constexpr int kStages = K == 4 ? 3 : 4;
   static constexpr int kWarpRing = kStages * kSlot;
   static constexpr int kSmem = kCW * kWarpRing;
 };
@@ -406,18 +410,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   cursor_item(item);
   int next_item = n_items;  // taken by the producer when it leaves `item`
   bool p_done = false;
-  // copy the cursor's block into ring slot `slot_idx` and advance the cursor;
-  // the producer is at most kStages - 1 blocks ahead and an item has at least
-  // that many, so it is never more than one item ahead of the consumer
+  // copy the cursor's next job (two blocks) into ring slot `slot_idx` and
+  // advance the cursor.  The producer runs kStages - 1 jobs ahead of the
+  // consumer; since an item has at least kStages jobs (bps >= 8 blocks), it
+  // finishes issuing the next item only after the consumer has left the
+  // current one, so next_item is never overwritten too early
   auto issue = [&](int slot_idx) {
     uint8_t* slot = ring + slot_idx * C::kSlot;
 #pragma unroll
-    for (int c = 0; c < (C::kCodeChunk + 511) / 512; c++)
-      if (c * 512 + lane * 16 < C::kCodeChunk) cp_async16(slot + c * 512 + lane * 16, cur.cs + c * 512 + lane * 16);
-    if (cur.xsrc) cp_async16(slot + C::kCodeChunk + lane * 16, cur.xsrc);
-    if (++cur.b < bps) {
-      cur.cs += row_bytes;
-      if (cur.xsrc) cur.xsrc += kXsChunk;
+    for (int q = 0; q < kJobBlocks; q++) {
+      uint8_t* dst = slot + q * C::kBlkBytes;
+      const uint8_t* cs = cur.cs + q * row_bytes;
+#pragma unroll
+      for (int c = 0; c < (C::kCodeChunk + 511) / 512; c++)
+        if (c * 512 + lane * 16 < C::kCodeChunk) cp_async16(dst + c * 512 + lane * 16, cs + c * 512 + lane * 16);
+      if (cur.xsrc) cp_async16(dst + C::kCodeChunk + lane * 16, cur.xsrc + q * kXsChunk);
+    }
+    if ((cur.b += kJobBlocks) < bps) {
+      cur.cs += kJobBlocks * row_bytes;
+      if (cur.xsrc) cur.xsrc += kJobBlocks * kXsChunk;
     } else {
       next_item = grab_item(p.work);
       if (next_item < n_items) cursor_item(next_item);
@@ -469,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
     for (int i = 0; i < 8; i++)
 #pragma unroll
       for (int d = 0; d < 4; d++) acc[i][d] = 0.0f;
-    for (int b = 0; b < bps; b++) {
+    for (int b = 0; b < bps; b += kJobBlocks) {
       if (!p_done) issue(issue_slot);
       issue_slot = issue_slot + 1 == C::kStages ? 0 : issue_slot + 1;
       cp_async_commit();
@@ -477,12 +488,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
       __syncwarp();
       const uint8_t* slot = ring + read_slot * C::kSlot;
       read_slot = read_slot + 1 == C::kStages ? 0 : read_slot + 1;
-      LaneWords<K> lw;
-      lds_lane_words<K>(lw, slot + lane * 8 * K);
-      fetch_neighbour<K>(lw);
-      const uint4 bx = g_l < cnt ? *reinterpret_cast<const uint4*>(slot + C::kCodeChunk + g_l * 64 + c_l * 16)
-                                 : make_uint4(0, 0, 0, 0);
-      decode_mma<K, FP8>(lw, bx, acc, p.mult);
+#pragma unroll
+      for (int q = 0; q < kJobBlocks; q++) {
+        const uint8_t* blk = slot + q * C::kBlkBytes;
+        LaneWords<K> lw;
+        lds_lane_words<K>(lw, blk + lane * 8 * K);
+        fetch_neighbour<K>(lw);
+        const uint4 bx = g_l < cnt ? *reinterpret_cast<const uint4*>(blk + C::kCodeChunk + g_l * 64 + c_l * 16)
+                                   : make_uint4(0, 0, 0, 0);
+        decode_mma<K, FP8>(lw, bx, acc, p.mult);
+      }
       __syncwarp();  // the slot is refilled by a later issue
     }
     // this item's scaled partial sums into its split slab
