@@ -47,6 +47,7 @@ class OracleLayer(ctypes.Structure):
         ("K", ctypes.c_int * 3), ("fp8_round", ctypes.c_int), ("mult", ctypes.c_uint32),
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
+        ("hadamard", ctypes.c_int),
     ]
 
 
@@ -100,6 +101,10 @@ def lib():
             L.oracle_shared_row.restype = None
             L.oracle_rmsnorm_row.argtypes = [u16p, ctypes.c_int, ctypes.c_double, u16p]
             L.oracle_rmsnorm_row.restype = None
+            L.oracle_hadamard128_entry.argtypes = [ctypes.c_int, ctypes.c_int]
+            L.oracle_hadamard128_entry.restype = ctypes.c_double
+            L.oracle_hadamard_blocks.argtypes = [u16p, ctypes.c_int]
+            L.oracle_hadamard_blocks.restype = None
             _lib = L
     return _lib
 
@@ -184,6 +189,19 @@ def decode_dense(codes: np.ndarray, in_f: int, out_f: int, K: int,
     return out
 
 
+# ---------------------------------------------------------------- rotation
+def hadamard128_entry(i: int, j: int) -> float:
+    return lib().oracle_hadamard128_entry(int(i), int(j))
+
+
+def hadamard_blocks(v: np.ndarray) -> np.ndarray:
+    """v . Hb for a vector whose length is a multiple of 128 (a copy)."""
+    v = np.array(v, dtype=np.float64, copy=True)
+    assert v.ndim == 1 and v.size % 128 == 0
+    lib().oracle_hadamard_blocks(_ptr(v), v.size)
+    return v
+
+
 # ---------------------------------------------------------------- routing
 def route(logits: np.ndarray, top_k: int):
     """ids [T,k] int32, w [T,k] f32, seg_offsets [E+1] int32, seg_pairs [T*k] int32."""
@@ -202,7 +220,7 @@ class Layer:
     """Holds numpy arrays of one layer (host copies) and its oracle view."""
 
     def __init__(self, num_experts, hidden, inter, K, codes, suh, svh, fp8_round=False,
-                 mult=DEFAULT_MCG_MULT, shared_w=None):
+                 mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False):
         self.arrays = []
         st = OracleLayer()
         st.num_experts, st.hidden, st.inter = num_experts, hidden, inter
@@ -210,6 +228,7 @@ class Layer:
             st.K[p] = int(K[p])
         st.fp8_round = int(bool(fp8_round))
         st.mult = mult
+        st.hadamard = int(bool(hadamard))
         for p in range(3):
             c = np.ascontiguousarray(codes[p], dtype=np.uint16)
             a = np.ascontiguousarray(suh[p], dtype=np.uint16)

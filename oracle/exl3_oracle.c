@@ -13,8 +13,9 @@
  *   - "GLM-5.3-Flash · exlr8 (K2/K3/K4)", intro: every codebook output is
  *     rounded to FP8 E4M3 (nearest-even, saturating) before the side vectors;
  *     section Loading: a 16x16 tile (k16 index), a half of 4096x128 at width
- *     K is 65,536*K bytes; section Calibration: the mcg codebook and the tile
- *     packing order are format primitives.
+ *     K is 65,536*K bytes; section Calibration: the mcg codebook, the 128x128
+ *     Hadamard matrix and the tile packing order are format primitives (the
+ *     Hadamard rotation is the optional format v2 here).
  *   - "GLM-5.3 Flash EXL3 for 2x DGX Sparks", section What runs: experts are
  *     trellis + suh + svh + mcg; section Cold prefill (E3): gather, gate/up +
  *     SwiGLU, down + scatter from device-side segment tables.
@@ -27,7 +28,8 @@
  *
  * Parity status: every function here is pinned by tests/test_oracle_pins.py
  * (closed forms, exhaustive states, library converters, brute force, dense
- * reference).  Compatibility with real EXL3/exlr8 checkpoints is unpinned: no
+ * reference; the Hadamard matrix against scipy's Sylvester construction and a
+ * closed-form rotated layer).  Compatibility with real EXL3/exlr8 checkpoints is unpinned: no
  * checkpoint or test vector exists for this build.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (contraction off so
@@ -353,9 +355,54 @@ typedef struct {
     const uint16_t *suh[3];   /* [E][in] fp16 */
     const uint16_t *svh[3];   /* [E][out] fp16 */
     const uint16_t *shared_w[3]; /* dense fp16 [in][out] or NULL */
+    int hadamard;      /* 1: format v2, the 128-point rotation on both sides */
 } oracle_layer;
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ------------------------------------------------------------------------ */
+/* Hadamard rotation (format v2)                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Entry (i, j), 0 <= i, j < 128, of the normalized 128x128 Hadamard matrix
+ * of Sylvester's construction: (-1)^popcount(i & j) / sqrt(128).
+ * reading: page "GLM-5.3-Flash · exlr8 (K2/K3/K4)", section Calibration,
+ * names "the 128x128 Hadamard matrix" as one of the format's primitives
+ * without printing it; the Sylvester matrix (the 2x2 [[1, 1], [1, -1]]
+ * raised to the 7th Kronecker power) is the plain 128x128 one, and its
+ * normalization makes it orthogonal and its own inverse. */
+double oracle_hadamard128_entry(int i, int j)
+{
+    int bits = i & j, par = 0;
+    while (bits) {
+        par ^= bits & 1;
+        bits >>= 1;
+    }
+    return (par ? -1.0 : 1.0) / sqrt(128.0);
+}
+
+/* v <- v . Hb for a row vector of n values (n a multiple of 128), where Hb is
+ * block diagonal with n/128 copies of the 128x128 matrix above.  Plain
+ * matrix-vector products from the entries (no fast transform). */
+void oracle_hadamard_blocks(double *v, int n)
+{
+    double tmp[128];
+    double *Hm = (double *)malloc(128 * 128 * sizeof(double));
+    for (int i = 0; i < 128; i++)
+        for (int j = 0; j < 128; j++)
+            Hm[i * 128 + j] = oracle_hadamard128_entry(i, j);
+    for (int b = 0; b < n; b += 128) {
+        for (int j = 0; j < 128; j++) {
+            double acc = 0.0;
+            for (int i = 0; i < 128; i++)
+                acc += v[b + i] * Hm[i * 128 + j];
+            tmp[j] = acc;
+        }
+        for (int j = 0; j < 128; j++)
+            v[b + j] = tmp[j];
+    }
+    free(Hm);
+}
 
 /* Decode projection p of expert e to doubles [in][out] (codebook values,
  * side vectors not applied). */
@@ -376,43 +423,55 @@ static void decode_proj_double(const oracle_layer *L, int p, int e, double *dst)
 /* One routed expert applied to one activation row (fp64), times router weight.
  * g = svh_g * ((x * suh_g) . Vg), u likewise, h = silu(g) * u,
  * r = w * svh_d * ((h * suh_d) . Vd).  Page "GLM-5.3 Flash EXL3 for 2x DGX
- * Sparks", section Cold prefill (E3): gate/up + SwiGLU, then down + scatter. */
+ * Sparks", section Cold prefill (E3): gate/up + SwiGLU, then down + scatter.
+ * With the Hadamard rotation (format v2) every projection becomes
+ * svh * ((((in * suh) . Hb) . V) . Hb), i.e. the effective weight matrix is
+ * diag(suh) Hb V Hb diag(svh).
+ * reading: the pages name the matrix but not where it acts; the input is
+ * scaled by suh and then rotated, the product rotated and then scaled by svh,
+ * so that with Hb = identity this is format v1. */
+static void project(const oracle_layer *L, const double *in, int n_in, const uint16_t *suh,
+                    const double *V, int n_out, double *out)
+{
+    double *a = (double *)malloc((size_t)n_in * sizeof(double));
+    for (int i = 0; i < n_in; i++)
+        a[i] = in[i] * oracle_f16_to_double(suh[i]);
+    if (L->hadamard)
+        oracle_hadamard_blocks(a, n_in);
+    for (int o = 0; o < n_out; o++)
+        out[o] = 0.0;
+    for (int i = 0; i < n_in; i++) {
+        const double *vr = V + (size_t)i * n_out;
+        for (int o = 0; o < n_out; o++)
+            out[o] += a[i] * vr[o];
+    }
+    if (L->hadamard)
+        oracle_hadamard_blocks(out, n_out);
+    free(a);
+}
+
 static void expert_row(const oracle_layer *L, int e, const double *Vg, const double *Vu,
                        const double *Vd, const double *x, double wgt, double *r)
 {
     int H = L->hidden, I = L->inter;
-    const uint16_t *suh_g = L->suh[0] + (size_t)e * H, *suh_u = L->suh[1] + (size_t)e * H;
     const uint16_t *svh_g = L->svh[0] + (size_t)e * I, *svh_u = L->svh[1] + (size_t)e * I;
-    const uint16_t *suh_d = L->suh[2] + (size_t)e * I, *svh_d = L->svh[2] + (size_t)e * H;
-    double *g = (double *)calloc((size_t)I, sizeof(double));
-    double *u = (double *)calloc((size_t)I, sizeof(double));
-    double *hd = (double *)calloc((size_t)I, sizeof(double));
-    for (int i = 0; i < H; i++) {
-        double xg = x[i] * oracle_f16_to_double(suh_g[i]);
-        double xu = x[i] * oracle_f16_to_double(suh_u[i]);
-        const double *vg = Vg + (size_t)i * I, *vu = Vu + (size_t)i * I;
-        for (int o = 0; o < I; o++) {
-            g[o] += xg * vg[o];
-            u[o] += xu * vu[o];
-        }
-    }
+    const uint16_t *svh_d = L->svh[2] + (size_t)e * H;
+    double *g = (double *)malloc((size_t)I * sizeof(double));
+    double *u = (double *)malloc((size_t)I * sizeof(double));
+    double *h = (double *)malloc((size_t)I * sizeof(double));
+    project(L, x, H, L->suh[0] + (size_t)e * H, Vg, I, g);
+    project(L, x, H, L->suh[1] + (size_t)e * H, Vu, I, u);
     for (int o = 0; o < I; o++) {
         double gg = g[o] * oracle_f16_to_double(svh_g[o]);
         double uu = u[o] * oracle_f16_to_double(svh_u[o]);
-        hd[o] = silu(gg) * uu * oracle_f16_to_double(suh_d[o]);
+        h[o] = silu(gg) * uu;
     }
-    for (int o = 0; o < H; o++)
-        r[o] = 0.0;
-    for (int i = 0; i < I; i++) {
-        const double *vd = Vd + (size_t)i * H;
-        for (int o = 0; o < H; o++)
-            r[o] += hd[i] * vd[o];
-    }
+    project(L, h, I, L->suh[2] + (size_t)e * I, Vd, H, r);
     for (int o = 0; o < H; o++)
         r[o] *= wgt * oracle_f16_to_double(svh_d[o]);
     free(g);
     free(u);
-    free(hd);
+    free(h);
 }
 
 /* Shared expert: unquantized fp16 SwiGLU MLP of the same shape, weight 1

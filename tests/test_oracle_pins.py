@@ -409,3 +409,94 @@ def test_rmsnorm_closed_form():
     x = np.full(64, 3.0)
     out = oracle.rmsnorm_row(x, 1e-6)
     assert np.allclose(out, 3.0 / math.sqrt(9.0 + 1e-6), rtol=1e-15)
+
+
+# ------------------------------------------------------------ Hadamard (format v2)
+
+
+def _sylvester128():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    return scipy_linalg.hadamard(128).astype(np.float64) / math.sqrt(128.0)
+
+
+def test_hadamard128_vs_scipy_and_invariants():
+    """The 128x128 matrix equals scipy's Sylvester Hadamard matrix divided by
+    sqrt(128); it is symmetric, orthogonal (so its own inverse) and maps the
+    all-ones vector to sqrt(128) e_0."""
+    ref = _sylvester128()
+    got = np.array([[oracle.hadamard128_entry(i, j) for j in range(128)] for i in range(128)])
+    assert np.allclose(got, ref, rtol=0, atol=1e-16)
+    assert np.array_equal(got, got.T)
+    assert np.allclose(got @ got, np.eye(128), rtol=0, atol=1e-14)
+    ones = got @ np.ones(128)
+    assert abs(ones[0] - math.sqrt(128.0)) < 1e-13 and np.abs(ones[1:]).max() < 1e-13
+
+
+def test_hadamard_blocks_vs_numpy():
+    """v . Hb on three 128-blocks equals numpy's block-by-block product with
+    the scipy matrix, and preserves the Euclidean norm."""
+    ref = _sylvester128()
+    v = np.random.default_rng(11).standard_normal(384)
+    got = oracle.hadamard_blocks(v)
+    want = (v.reshape(3, 128) @ ref).ravel()
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+    assert abs(np.linalg.norm(got) - np.linalg.norm(v)) < 1e-12 * np.linalg.norm(v)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_layer_hadamard_vs_numpy_dense_reference(fp8):
+    """Format v2 layer == numpy matmul with the effective weights
+    diag(suh) Hb V Hb diag(svh), Hb built from scipy's Sylvester matrix."""
+    E, H, I, K, T, k = 4, 256, 128, (2, 3, 4), 3, 2
+    _, codes, suh, svh, _ = _small_layer(5, E, H, I, K, fp8, False)
+    L = oracle.Layer(E, H, I, K, codes, suh, svh, fp8_round=fp8, hadamard=True)
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x, False, logits, k)
+    ids, w, _, _ = oracle.route(logits, k)
+    xf = x.view(np.float16).astype(np.float64)
+    f = lambda a: a.view(np.float16).astype(np.float64)
+    Hs = _sylvester128()
+    hb = lambda n: np.kron(np.eye(n // 128), Hs)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            W = []
+            for p in range(3):
+                fi, fo = (I, H) if p == 2 else (H, I)
+                V = f(oracle.decode_dense(codes[p][e], fi, fo, K[p], fp8_round=fp8))
+                W.append(np.diag(f(suh[p][e])) @ hb(fi) @ V @ hb(fo) @ np.diag(f(svh[p][e])))
+            g = xf[t] @ W[0]
+            u = xf[t] @ W[1]
+            h = g / (1 + np.exp(-g)) * u
+            ref[t] += float(w[t, j]) * (h @ W[2])
+    assert np.allclose(y, ref, rtol=1e-10, atol=1e-9 * np.abs(ref).max())
+
+
+def test_layer_hadamard_closed_form_zero_codes():
+    """Zero codes (every weight c = 1.84375), unit side vectors, top_k = 1.
+    The rotation concentrates a constant row on the first entry of each
+    128-block (Hb 1 = sqrt(128) e_0 per block), so g_o = u_o = G = 128 c S
+    with S = sum_b x[128 b] when o = 0 (mod 128) and 0 otherwise; the down
+    input h . Hb is then constant (h_0 / sqrt(128)), and y_o = c I silu(G) G
+    when o = 0 (mod 128), 0 otherwise."""
+    E, H, I, T = 2, 256, 256, 3
+    c = 1.84375
+    codes = [np.zeros((E, (I if p == 2 else H) // 16, (H if p == 2 else I) // 16, 32), np.uint16)
+             for p in range(3)]
+    one = np.uint16(0x3C00)
+    suh = [np.full((E, I if p == 2 else H), one, np.uint16) for p in range(3)]
+    svh = [np.full((E, H if p == 2 else I), one, np.uint16) for p in range(3)]
+    L = oracle.Layer(E, H, I, (2, 2, 2), codes, suh, svh, hadamard=True)
+    rng = np.random.default_rng(7)
+    x = (0.05 * rng.standard_normal((T, H))).astype(np.float16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x.view(np.uint16), False, logits, 1)
+    for t in range(T):
+        S = x[t].astype(np.float64)[::128].sum()
+        G = 128 * c * S
+        want = np.zeros(H)
+        want[::128] = c * I * (G / (1 + math.exp(-G))) * G
+        assert np.allclose(y[t], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
