@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profilers)")
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="format v2: the workload's layer with the 128-point Hadamard rotation")
     return ap.parse_args()
 
 
@@ -177,7 +179,7 @@ def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
     sides = [synth.side_vectors(spec, p) for p in range(3)]
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
-                      shared_w=shared_w)
+                      shared_w=shared_w, hadamard=spec.hadamard)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     t0 = time.perf_counter()
     for j in range(n_pairs):
@@ -213,7 +215,7 @@ def run_reference(args):
     sw = synth.shared_weights(spec) if spec.shared else None
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], shared_w=sw,
-                      fp8_round=spec.fp8_round)
+                      fp8_round=spec.fp8_round, hadamard=spec.hadamard)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
     for s in range(args.warmup):
@@ -258,6 +260,9 @@ def pick_workload(args):
     if args.experts:
         spec = dataclasses.replace(spec, num_experts=args.experts)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-E{args.experts}")
+    if args.hadamard:
+        spec = dataclasses.replace(spec, hadamard=True)
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-hadamard")
     return wl, spec
 
 
@@ -267,7 +272,7 @@ def workload_config(wl):
                          f"inter {s.inter}, K={list(s.K)}, T={wl.T} {wl.act}"
                          + (", + fp16 shared expert" if s.shared else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
-            "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round,
+            "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round, "hadamard": s.hadamard,
             "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
 
 
@@ -303,7 +308,8 @@ def run_ours(args):
     d_suh = [t16(s[0]).view(torch.float16) for s in sides]
     d_svh = [t16(s[1]).view(torch.float16) for s in sides]
     d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
-    layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw)
+    layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw,
+                  hadamard=spec.hadamard)
     x = t16(x_np).view(torch.bfloat16)
     lg = torch.from_numpy(lg_np).to(dev)
     T, k = wl.T, wl.top_k

@@ -75,9 +75,17 @@ typedef struct {
     const uint16_t *shared_w[3]; /* device fp16 bits, dense [in][out], or all NULL: one
                                     unquantized shared expert added with weight 1
                                     ([p4] intro: one shared expert per MoE layer) */
+    int hadamard;                /* 0 = format v1; 1 = format v2: the routed projections
+                                    carry the 128-point Hadamard rotation on both sides,
+                                    W_eff = diag(suh) Hb V Hb diag(svh), Hb block diagonal
+                                    with copies of the normalized 128x128 Sylvester matrix,
+                                    entries (-1)^popcount(i & j) / sqrt(128) ([p4]
+                                    Calibration names the 128x128 Hadamard matrix as a
+                                    format primitive).  Other values: EXL3_ERR_ARG */
 } exl3_layer_desc;
 
-/* Validate `desc` and build a handle.  A layer with a shared expert also
+/* Validate `desc` and build a handle.  codes, suh, svh and shared_w must be
+ * 16-byte aligned.  A layer with a shared expert also
  * creates one CUDA stream and two events on the current device (released by
  * exl3_layer_destroy); the shared expert of every forward runs on that stream,
  * forked from the caller's stream after routing and joined before the
@@ -92,8 +100,9 @@ void exl3_layer_destroy(exl3_layer_t *layer);
 /* Decode projection `proj` of `expert` to a dense fp16 matrix out[in][out]
  * (device).  apply_side = 0: the codebook values (after the E4M3 rule when the
  * layer has fp8_round); apply_side = 1: fp16(fp32(fp32(v*suh[i])*svh[o])).
- * Bit-exact check path for the format ([p2] Cold prefill: the dense
- * "LinearEXL3 reference").  Errors: EXL3_ERR_ARG for bad expert/proj/null. */
+ * The Hadamard rotation of format v2 is never applied here: this is the
+ * element-wise, bit-exact check path for the codes ([p2] Cold prefill: the
+ * dense "LinearEXL3 reference").  Errors: EXL3_ERR_ARG for bad expert/proj/null. */
 exl3_status exl3_decode_dense(const exl3_layer_t *layer, int expert, int proj, int apply_side,
                               uint16_t *out, void *stream);
 

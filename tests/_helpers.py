@@ -29,7 +29,7 @@ class HostLayer:
     def oracle(self) -> oracle.Layer:
         s = self.spec
         return oracle.Layer(s.num_experts, s.hidden, s.inter, s.K, self.codes, self.suh, self.svh,
-                            fp8_round=s.fp8_round, shared_w=self.shared)
+                            fp8_round=s.fp8_round, shared_w=self.shared, hadamard=s.hadamard)
 
     def device(self, mult: int = 0):
         import torch
@@ -39,7 +39,8 @@ class HostLayer:
                         svh=[t(a).view(torch.float16) for a in self.svh],
                         shared=[t(a).view(torch.float16) for a in self.shared] if self.shared else None)
         return Layer(self.dev["codes"], self.dev["suh"], self.dev["svh"], self.spec.K,
-                     fp8_round=self.spec.fp8_round, mcg_mult=mult, shared=self.dev["shared"])
+                     fp8_round=self.spec.fp8_round, mcg_mult=mult, shared=self.dev["shared"],
+                     hadamard=self.spec.hadamard)
 
 
 def oracle_forward_parallel(olayer: oracle.Layer, x_bits, is_bf16, logits, top_k, tokens,

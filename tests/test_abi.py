@@ -65,6 +65,13 @@ def test_layer_create_validation(L):
     d = _desc()
     d.shared_w[0] = 8192                                        # all three or none
     assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    for field in ("suh", "svh"):                                 # side vectors aligned too
+        d = _desc()
+        getattr(d, field)[2] += 8
+        assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    d = _desc()
+    d.hadamard = 2                                              # 0 (format v1) or 1 (v2)
+    assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
 
 
 def test_route_validation_and_sizes(L):

@@ -2,6 +2,8 @@
 the same seeded inputs.  Decode and routing must match bit for bit; layer
 outputs must meet max|gpu-oracle|/max|oracle| <= 2e-2 and relative Frobenius
 error <= 5e-3."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -240,12 +242,34 @@ def test_graph_capture_replays_same_output():
     assert torch.equal(out, first)
 
 
+# ------------------------------------------------------------------ format v2 (Hadamard)
+
+
+@pytest.mark.parametrize("H,I,K,fp8,shared,T,k,routing,path", [
+    (512, 256, (2, 2, 3), False, True, 37, 4, "normal", 1),   # GEMV, ragged token groups
+    (384, 384, (4, 4, 4), True, False, 64, 8, "normal", 1),   # GEMV, odd block counts
+    (512, 256, (3, 3, 4), False, False, 40, 4, "normal", 2),  # small-tile kernel, M 64
+    (512, 256, (3, 3, 4), True, False, 120, 4, "normal", 2),  # both small-tile widths
+    (512, 256, (4, 4, 3), False, True, 700, 4, "zipf", 2),    # big + small tiles
+    (384, 384, (2, 2, 2), True, False, 300, 4, "normal", 2),  # big-tile kernel only
+])
+def test_forward_hadamard(H, I, K, fp8, shared, T, k, routing, path):
+    """Format v2: the rotated input passes and the rotated epilogues of the
+    GEMV and of both tensor-core kernels against the oracle, which rotates
+    with the explicit 128x128 matrix."""
+    spec = synth.LayerSpec(seed=90 + sum(K), num_experts=8, hidden=H, inter=I, K=K,
+                           fp8_round=fp8, shared=shared, hadamard=True)
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=path, routing=routing)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
 # ------------------------------------------------------------------ workloads
 
 
-def _workload_parity(name, tokens_fn, path=0):
+def _workload_parity(name, tokens_fn, path=0, hadamard=False):
     wl = synth.WORKLOADS[name]
-    spec = wl.layers[0]
+    spec = dataclasses.replace(wl.layers[0], hadamard=hadamard)
     hl = HostLayer(spec)
     layer = hl.device()
     x, logits = synth.workload_inputs(wl)
@@ -279,6 +303,16 @@ def _prefill_tokens(wl, logits):
 
 def test_prefill_workload_sampled():
     _workload_parity("prefill", _prefill_tokens)
+
+
+def test_decode_workload_hadamard_all_tokens():
+    """The decode workload's layer in format v2 (GEMV path, full size)."""
+    _workload_parity("decode", lambda wl, lg: list(range(wl.T)), hadamard=True)
+
+
+def test_prefill_workload_hadamard_sampled():
+    """The prefill workload's layer in format v2 (tensor-core path, full size)."""
+    _workload_parity("prefill", _prefill_tokens, hadamard=True)
 
 
 def test_long_workload_sampled():

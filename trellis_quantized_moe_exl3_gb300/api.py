@@ -47,10 +47,13 @@ class Layer:
     codes[p]: uint16-bit tensors (torch.int16 or uint16 view) of shape
     [E, in/16, out/16, 16*K[p]]; suh[p]: fp16 [E, in]; svh[p]: fp16 [E, out];
     shared (optional): three fp16 dense [in, out] matrices.  p = 0 gate,
-    1 up, 2 down.  The tensors must stay alive as long as the layer.
+    1 up, 2 down.  hadamard: format v2 (the 128-point Hadamard rotation on
+    both sides of every routed projection).  The tensors must stay alive as
+    long as the layer.
     """
 
-    def __init__(self, codes, suh, svh, K, fp8_round=False, mcg_mult=0, shared=None):
+    def __init__(self, codes, suh, svh, K, fp8_round=False, mcg_mult=0, shared=None,
+                 hadamard=False):
         c0 = codes[0]
         E, nti, nto, w = c0.shape
         H, I = nti * 16, nto * 16
@@ -69,6 +72,7 @@ class Layer:
             d.shared_w[p] = shared[p].data_ptr() if shared is not None else None
         d.fp8_round = int(bool(fp8_round))
         d.mcg_mult = int(mcg_mult)
+        d.hadamard = int(bool(hadamard))
         h = ctypes.c_void_p()
         check(_lib.lib().exl3_layer_create(ctypes.byref(d), ctypes.byref(h)), "exl3_layer_create")
         self._h = h

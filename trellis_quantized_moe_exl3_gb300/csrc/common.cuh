@@ -193,6 +193,37 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 // and must wait here before it touches memory the predecessor reads or writes.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------- Hadamard
+// Format v2 rotation ("GLM-5.3-Flash · exlr8 (K2/K3/K4)", Calibration: a
+// 128x128 Hadamard matrix is a format primitive): v . H over each 128-block,
+// H the Sylvester matrix with entries (-1)^popcount(i & j).  It is applied
+// unnormalized on both sides of a projection, so the product carries a factor
+// 128 that a 2^-7 in the activation scale removes exactly.  The 7 index bits
+// of a block are split between registers and lanes; a stage maps (a, b) to
+// (a + b, a - b) over one index bit, and stages commute.
+constexpr int kHadShift = 7;  // log2 of the block size
+
+template <int N>
+__device__ __forceinline__ void wht_regs(float (&v)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < N; i++)
+      if (!(i & h)) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+}
+
+// One stage over lane bit m (partner lane ^ m, both inside `mask`): the lane
+// with the bit clear keeps v + o, its partner o - v, both as one fma with a
+// sign of +-1 (exact product, one rounding: the same result as the add).
+__device__ __forceinline__ float wht_lane(float v, int m, unsigned mask) {
+  const float o = __shfl_xor_sync(mask, v, m);
+  return fmaf((threadIdx.x & m) ? -1.0f : 1.0f, v, o);
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float load_act(const void* x, int is_bf16, size_t idx) {
   const uint16_t b = reinterpret_cast<const uint16_t*>(x)[idx];

@@ -90,6 +90,7 @@ struct LayerView {
   const uint16_t* svh[3];
   const uint16_t* shared_w[3];
   size_t code_stride[3];  // uint16 words per expert
+  int had;                // format v2: Hadamard rotation on both sides of each projection
 };
 
 cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int apply_side,
@@ -114,7 +115,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
                             cudaStream_t st);
 
 // ---- grouped GEMM path (prefill-sized steps, tcgen05)
-size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I);
+size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had);
 // ev (may be null): events after gather [2], gate/up [3], down input [4], down [5].
 // *r_out receives the pair-row buffer [P][H] the combine reads.
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,

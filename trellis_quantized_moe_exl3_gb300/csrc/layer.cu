@@ -64,7 +64,7 @@ FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
   f.off = o; o += al((size_t)(L.E + 1) * 4);
   f.pairs = o; o += al(P * 4);
   const size_t gv = gemv_scratch_bytes(T, k, L.E, L.H, L.I);
-  const size_t gm = gemm_scratch_bytes(T, k, L.E, L.H, L.I);
+  const size_t gm = gemm_scratch_bytes(T, k, L.E, L.H, L.I, L.had);
   f.gemv = o; o += al(gv > gm ? gv : gm);
   f.shared = o; o += has_shared ? al(shared_scratch_bytes(T, L.H, L.I)) : 0;
   f.total = o;
@@ -99,9 +99,11 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   const uint32_t mult = d->mcg_mult ? d->mcg_mult : kDefaultMcgMult;
   if (!(mult & 1u)) return EXL3_ERR_ARG;
   int nshared = 0;
+  if (d->hadamard != 0 && d->hadamard != 1) return EXL3_ERR_ARG;
   for (int p = 0; p < 3; p++) {
     if (!d->codes[p] || !d->suh[p] || !d->svh[p]) return EXL3_ERR_ARG;
-    if (!aligned16(d->codes[p])) return EXL3_ERR_ARG;
+    if (!aligned16(d->codes[p]) || !aligned16(d->suh[p]) || !aligned16(d->svh[p]))
+      return EXL3_ERR_ARG;
     nshared += d->shared_w[p] != nullptr;
     if (d->shared_w[p] && !aligned16(d->shared_w[p])) return EXL3_ERR_ARG;
   }
@@ -114,6 +116,7 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   v.E = d->num_experts; v.H = d->hidden; v.I = d->inter;
   v.fp8 = d->fp8_round ? 1 : 0;
   v.mult = mult;
+  v.had = d->hadamard;
   for (int p = 0; p < 3; p++) {
     v.K[p] = d->K[p];
     v.codes[p] = d->codes[p];

@@ -24,6 +24,12 @@
 // The epilogue (the decoder warps) reads TMEM: gate/up launch -> svh * acc per
 // position (SwiGLU follows in the down projection's input pass); down launch
 // -> router weight * svh * acc into the pair's own row (no atomics).
+//
+// Format v2 (Hadamard rotation): suh cannot be folded into the weights, since
+// the rotation sits between it and the codes, so the input passes apply it
+// and rotate each 128-input block (gate and up then have separate activation
+// rows, [P + pos] for up); the decoders multiply by 1; the epilogue rotates
+// each 128-output block through shared memory before svh.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -76,7 +82,45 @@ struct GemmParams {
   const float* wts;
   int32_t* status;
   int cluster;              // CTAs per cluster (divides the strip count)
+  int had;                  // format v2: suh on the activation side, outputs rotated
+  int xrow_off;             // activation row (and scale) offset of projection 1
 };
+
+// Format v2 epilogue of the M = outputs kernel: the 4 warps of a column group
+// hold the 128 outputs of a strip (TMEM lanes, thread = output) for the same
+// 16 token columns.  They stage them in shared memory ([output][17] floats,
+// conflict free both ways), then each warp takes 4 of the columns with lane l
+// holding outputs l + 32 j, rotates (j in registers, l by shuffles), scales
+// and stores 128 contiguous outputs of the token's row.
+__device__ __forceinline__ void rotate_store_cols(float* xbuf, const float (&a0)[16], int q4,
+                                                  int lane, int bar_id, int c0, int cnt,
+                                                  const float (&sv)[4], const float* s_scale,
+                                                  const int32_t* s_pid, const GemmParams& p,
+                                                  int pj, int pos0, int o0) {
+#pragma unroll
+  for (int i = 0; i < 16; i++) xbuf[(32 * q4 + lane) * 17 + i] = a0[i];
+  named_bar_sync(bar_id, 128);
+#pragma unroll
+  for (int tt = 0; tt < 4; tt++) {
+    const int cl = 4 * q4 + tt, n = c0 + cl;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) v[j] = xbuf[(lane + 32 * j) * 17 + cl];
+    wht_regs(v);
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+      for (int j = 0; j < 4; j++) v[j] = wht_lane(v[j], m, 0xffffffffu);
+    if (n < cnt) {
+      const float sc = s_scale[n];
+      float* dst = p.gu_out ? p.gu_out + ((size_t)pj * p.n_pos + pos0 + n) * p.out
+                            : p.r_out + (size_t)s_pid[n] * p.out;
+#pragma unroll
+      for (int j = 0; j < 4; j++) dst[o0 + lane + 32 * j] = v[j] * sc * sv[j];
+    }
+  }
+  named_bar_sync(bar_id, 128);  // the buffer is refilled by the next chunk
+}
 
 // {a, b} halves of lane weights u = 16 pp .. 16 pp + 15.  For K = 2 and 4 each
 // 32-bit window is hashed once (a sliding window of 16 + 16/K products whose
@@ -182,9 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per-token epilogue scalars: scale = 1/row-scale (* router weight), pair id
   float* s_scale = reinterpret_cast<float*>(smem + C::kOffScal);
   int32_t* s_pid = reinterpret_cast<int32_t*>(s_scale + kBN);
+  // activation rows (and their scales) of this projection start at xrow0
+  const int xrow0 = pj * p.xrow_off + pos0;
   for (int n = threadIdx.x; n < cnt; n += blockDim.x) {
     const int pos = pos0 + n;
-    float sc = p.xinv[pos];
+    float sc = p.xinv[xrow0 + n];
     int pid = 0;
     if (!p.gu_out) {
       pid = p.seg_pairs[pos];
@@ -217,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&b_full[sb], nbox * kBox);
         uint8_t* dst = b_ring + sb * bstage;
         for (int j = crank; j < nbox; j += p.cluster)
-          tma_load_2d_multicast(dst + j * kBox, &tmap_b, ks * kKS, pos0 + 64 * j, &b_full[sb],
+          tma_load_2d_multicast(dst + j * kBox, &tmap_b, ks * kKS, xrow0 + 64 * j, &b_full[sb],
                                 cmask);
         if (++sb == nbst) {
           sb = 0;
@@ -311,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_suh = [&](int n) {
       const int ks = ks0 + n * kPar;
 #pragma unroll
-      for (int q = 0; q < 4; q++) s2n[q] = __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+      for (int q = 0; q < 4; q++)  // format v2: suh is on the activation side
+        s2n[q] = p.had ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
     };
     LaneWords<K> nxt;
     if (n_my > 0) {
@@ -351,8 +398,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3, cgrp = warp >> 2;
     const int o = 128 * s + 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    const float sv = __half2float(__ushort_as_half((pj ? p.svh[1] : p.svh[0])[(size_t)e * p.out + o]));
-    for (int c0 = 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
+    const uint16_t* svh_e = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out;
+    if (p.had) {
+      // the A ring is idle once the accumulator is complete
+      float* xbuf = reinterpret_cast<float*>(smem) + cgrp * (128 * 17);
+      float svr[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        svr[j] = __half2float(__ushort_as_half(svh_e[128 * s + lane + 32 * j]));
+      for (int c0 = 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
+        float a0[16];
+        tmem_ld16(trow + c0, a0);
+        tmem_ld_wait();
+        rotate_store_cols(xbuf, a0, q4, lane, 1 + cgrp, c0, cnt, svr, s_scale, s_pid, p, pj, pos0,
+                          128 * s);
+      }
+    }
+    const float sv = __half2float(__ushort_as_half(svh_e[o]));
+    for (int c0 = p.had ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait();
@@ -451,9 +514,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == kSDec) tmem_alloc(tmem_slot, kSN);
   float* s_scale = reinterpret_cast<float*>(smem + SCfg::kOffScal);
   int32_t* s_pid = reinterpret_cast<int32_t*>(s_scale + kSM);
+  // activation rows (and their scales) of this projection start at xrow0
+  const int xrow0 = pj * p.xrow_off + pos0;
   for (int n = threadIdx.x; n < cnt; n += blockDim.x) {
     const int pos = pos0 + n;
-    float sc = p.xinv[pos];
+    float sc = p.xinv[xrow0 + n];
     int pid = 0;
     if (!p.gu_out) {
       pid = p.seg_pairs[pos];
@@ -481,7 +546,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         mbar_wait_or_abort(&x_empty[sx], px ^ 1, p.status);
         mbar_arrive_expect_tx(&x_full[sx], nxbox * kBox);
         for (int j = crank; j < nxbox; j += p.cluster)
-          tma_load_2d_multicast(x_ring + sx * kSXStage + j * kBox, &tmap_x, ks * kKS, pos0 + 64 * j,
+          tma_load_2d_multicast(x_ring + sx * kSXStage + j * kBox, &tmap_x, ks * kKS, xrow0 + 64 * j,
                                 &x_full[sx], cmask);
         if (++sx == kSXStages) {
           sx = 0;
@@ -568,7 +633,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     auto load_suh = [&](int n) {
       const int ks = ks0 + n * kSPar;
 #pragma unroll
-      for (int q = 0; q < 4; q++) s2n[q] = __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+      for (int q = 0; q < 4; q++)  // format v2: suh is on the activation side
+        s2n[q] = p.had ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
     };
     LaneWords<K> nxt;
     if (n_my > 0) {
@@ -609,7 +675,50 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int n = (tm == 128 ? 32 : 16) * q4 + lane;  // token of this lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + kSN * s;
-    for (int c0 = 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
+    if (p.had) {
+      // Format v2: warps (q4, 2b) and (q4, 2b + 1) hold the two halves of the
+      // 128-output block b for the same 32 TMEM lanes (tokens).  Both stage
+      // their columns in shared memory (the weight ring is idle once the
+      // accumulator is complete; [row][129] floats, conflict free both ways),
+      // then each takes every other token row with lane l holding outputs
+      // l + 32 j, rotates (j in registers, l by shuffles), scales and stores
+      // 128 contiguous outputs of the row.
+      const int blk = cg >> 1, hlf = cg & 1;
+      float* xbuf = reinterpret_cast<float*>(smem) + (size_t)(2 * q4 + blk) * (32 * 129);
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        float a0[16];
+        tmem_ld16(trow + 64 * cg + 16 * c, a0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; i++) xbuf[lane * 129 + 64 * hlf + 16 * c + i] = a0[i];
+      }
+      named_bar_sync(1 + 2 * q4 + blk, 64);
+      float svr[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        svr[j] = __half2float(__ushort_as_half(svh[128 * blk + lane + 32 * j]));
+      const int rows = tm == 128 ? 32 : 16;
+      for (int r = hlf; r < rows; r += 2) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = xbuf[r * 129 + lane + 32 * j];
+        wht_regs(v);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+          for (int j = 0; j < 4; j++) v[j] = wht_lane(v[j], m, 0xffffffffu);
+        const int nr = rows * q4 + r;
+        if (nr < cnt) {
+          const float sc = s_scale[nr];
+          float* dst = p.gu_out ? p.gu_out + ((size_t)pj * p.n_pos + pos0 + nr) * p.out
+                                : p.r_out + (size_t)s_pid[nr] * p.out;
+#pragma unroll
+          for (int j = 0; j < 4; j++) dst[kSN * s + 128 * blk + lane + 32 * j] = v[j] * sc * svr[j];
+        }
+      }
+    }
+    for (int c0 = p.had ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait();
@@ -724,11 +833,102 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
   if (lane == 0) xinv[pos] = ldexpf(1.0f, -ex);
 }
 
+// Format v2: rows x * suh of gate and up for each position, each 128-input
+// block rotated, fp16 with a power-of-two scale per row that also removes the
+// rotations' factor 128: gate rows at [pos], up rows at [P + pos].  One warp
+// per position; lane l holds inputs 8v .. 8v + 7 of vector v = 32 i + l, so a
+// 128-block is 16 consecutive lanes (3 index bits in registers, 4 by
+// shuffles; H is a multiple of 128, so both half-warps are active or idle
+// together).  The scale comes from a bound instead of the rotated values: an
+// entry of a rotated block is at most the block's L1 norm, so the first pass
+// needs no rotation (the power-of-two scale only has to keep fp16 finite; it
+// does not change the relative rounding of normal fp16 values).
+__global__ void __launch_bounds__(kRowWarps * 32) gather_rows_had_kernel(
+    const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
+    const int32_t* ids, const uint16_t* __restrict__ suh_g, const uint16_t* __restrict__ suh_u,
+    uint16_t* __restrict__ xg, float* __restrict__ xinv) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (pos >= P) return;
+  const int pr = seg_pairs[pos];
+  const int t = pr / k, e = ids[pr];
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
+  const uint4* sg = reinterpret_cast<const uint4*>(suh_g + (size_t)e * H);
+  const uint4* su = reinterpret_cast<const uint4*>(suh_u + (size_t)e * H);
+  const int nv = H / 8;
+  const unsigned hm = 0xFFFFu << (lane & 16);
+  auto prods = [&](int v, float (&fg)[8], float (&fu)[8]) {
+    float fx[8], a[8], b[8];
+    act8(src[v], x_bf16, fx);
+    act8(sg[v], 0, a);
+    act8(su[v], 0, b);
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      fg[q] = fx[q] * a[q];
+      fu[q] = fx[q] * b[q];
+    }
+  };
+  // pass 1: the largest block L1 norm of each row
+  float ag = 0.0f, au = 0.0f;
+  for (int v = lane; v < nv; v += 32) {
+    float fg[8], fu[8];
+    prods(v, fg, fu);
+    float lg = 0.0f, lu = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      lg += fabsf(fg[q]);
+      lu += fabsf(fu[q]);
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+      lg += __shfl_xor_sync(hm, lg, m);
+      lu += __shfl_xor_sync(hm, lu, m);
+    }
+    ag = fmaxf(ag, lg);
+    au = fmaxf(au, lu);
+  }
+  ag = warp_max(ag);
+  au = warp_max(au);
+  auto rows = [&](int v, float (&fg)[8], float (&fu)[8]) {
+    prods(v, fg, fu);
+    wht_regs(fg);
+    wht_regs(fu);
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        fg[q] = wht_lane(fg[q], m, hm);
+        fu[q] = wht_lane(fu[q], m, hm);
+      }
+  };
+  const int eg = fp16_scale_exp(ag), eu = fp16_scale_exp(au);
+  const float scg = ldexpf(1.0f, eg), scu = ldexpf(1.0f, eu);
+  uint4* dg = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
+  uint4* du = reinterpret_cast<uint4*>(xg + ((size_t)P + pos) * H);
+  for (int v = lane; v < nv; v += 32) {
+    float fg[8], fu[8];
+    rows(v, fg, fu);
+    dg[v] = make_uint4(pack_h2(fg[0] * scg, fg[1] * scg), pack_h2(fg[2] * scg, fg[3] * scg),
+                       pack_h2(fg[4] * scg, fg[5] * scg), pack_h2(fg[6] * scg, fg[7] * scg));
+    du[v] = make_uint4(pack_h2(fu[0] * scu, fu[1] * scu), pack_h2(fu[2] * scu, fu[3] * scu),
+                       pack_h2(fu[4] * scu, fu[5] * scu), pack_h2(fu[6] * scu, fu[7] * scu));
+  }
+  if (lane == 0) {
+    xinv[pos] = ldexpf(1.0f, -eg - kHadShift);
+    xinv[(size_t)P + pos] = ldexpf(1.0f, -eu - kHadShift);
+  }
+}
+
 // h = silu(g) * u per position row, as fp16 with a power-of-two row scale
-// (suh of down is applied on the weight side by the decoder).  I is a
-// multiple of 128.
+// (format v1: suh of down is applied on the weight side by the decoder).
+// Format v2 (suh_d non-null): h * suh_d of the position's expert, each
+// 128-block rotated (lane l holds elements 4v .. 4v + 3 of v = 32 i + l: 2
+// index bits in registers, 5 by shuffles), the scale also removing the
+// factor 128.  I is a multiple of 128.
 __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
-    const float* __restrict__ gu, size_t n_pos, int I, uint16_t* __restrict__ hs,
+    const float* __restrict__ gu, size_t n_pos, int I, const int32_t* seg_pairs,
+    const int32_t* ids, const uint16_t* __restrict__ suh_d, uint16_t* __restrict__ hs,
     float* __restrict__ hinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -738,9 +938,28 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
   const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
   uint2* dst = reinterpret_cast<uint2*>(hs + pos * I);
   const int nv = I / 4;
+  const uint2* sd = suh_d ? reinterpret_cast<const uint2*>(suh_d + (size_t)ids[seg_pairs[pos]] * I)
+                          : nullptr;
+  // format v2: times suh_d, then rotated (every lane active: nv % 32 == 0)
+  auto rot = [&](float4& h, int v) {
+    const uint2 sr = __ldg(sd + v);
+    float w[4] = {h.x * __half2float(__ushort_as_half((unsigned short)(sr.x & 0xFFFFu))),
+                  h.y * __half2float(__ushort_as_half((unsigned short)(sr.x >> 16))),
+                  h.z * __half2float(__ushort_as_half((unsigned short)(sr.y & 0xFFFFu))),
+                  h.w * __half2float(__ushort_as_half((unsigned short)(sr.y >> 16)))};
+    wht_regs(w);
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+      for (int q = 0; q < 4; q++) w[q] = wht_lane(w[q], m, 0xffffffffu);
+    h = make_float4(w[0], w[1], w[2], w[3]);
+  };
   auto h4 = [&](int v) {
     const float4 g = __ldcs(gr + v), u = __ldcs(ur + v);
-    return make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+    float4 h = make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z,
+                           silu_f(g.w) * u.w);
+    if (sd) rot(h, v);
+    return h;
   };
   auto amax4 = [](float a, const float4& h) {
     return fmaxf(fmaxf(a, fabsf(h.x)), fmaxf(fmaxf(fabsf(h.y), fabsf(h.z)), fabsf(h.w)));
@@ -762,6 +981,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     if (v < nv) {
       c[i] = make_float4(silu_f(c[i].x) * cu[i].x, silu_f(c[i].y) * cu[i].y,
                          silu_f(c[i].z) * cu[i].z, silu_f(c[i].w) * cu[i].w);
+      if (sd) rot(c[i], v);
       am = amax4(am, c[i]);
     }
   }
@@ -778,7 +998,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     if (v < nv) put(v, c[i]);
   }
   for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, h4(v));
-  if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex);
+  if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex - (sd ? kHadShift : 0));
 }
 
 // Token tiles per expert segment (one CTA, thread per expert): tiles of
@@ -978,12 +1198,14 @@ struct GemmLayout {
   size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, total;
 };
 
-GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
+// Format v2 keeps separate gate and up activation rows (2P rows).
+GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had) {
   GemmLayout g{};
   const size_t P = (size_t)T * top_k;
+  const size_t xr = had ? 2 * P : P;
   size_t o = 0;
-  g.xg = o; o += al(P * H * 2);
-  g.xinv = o; o += al(P * 4);
+  g.xg = o; o += al(xr * H * 2);
+  g.xinv = o; o += al(xr * 4);
   g.gu = o; o += al(2 * P * I * 4);
   g.hs = o; o += al(P * I * 2);
   g.hinv = o; o += al(P * 4);
@@ -997,8 +1219,8 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I) {
 
 }  // namespace
 
-size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I) {
-  return gemm_layout(T, top_k, E, H, I).total;
+size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had) {
+  return gemm_layout(T, top_k, E, H, I, had).total;
 }
 
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
@@ -1007,7 +1229,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   auto rec = [&](int i) {
     if (ev && ev[i]) record_stage_event(ev[i], st);
   };
-  const GemmLayout g = gemm_layout(T, top_k, L.E, L.H, L.I);
+  const GemmLayout g = gemm_layout(T, top_k, L.E, L.H, L.I, L.had);
   char* base = static_cast<char*>(ws);
   uint16_t* xg = reinterpret_cast<uint16_t*>(base + g.xg);
   float* xinv = reinterpret_cast<float*>(base + g.xinv);
@@ -1022,7 +1244,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   const int P = T * top_k;
   const int mt = (int)max_tiles(T, L.E, top_k);
   CUtensorMap tm_x, tm_h;
-  if (!make_tmap(&tm_x, xg, (size_t)P, (size_t)L.H) || !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I))
+  if (!make_tmap(&tm_x, xg, (size_t)P * (L.had ? 2 : 1), (size_t)L.H) ||
+      !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I))
     return cudaErrorInvalidValue;
   cudaError_t err;
   // grids: big tiles on 128-output strips, small tiles on 256-output chunks
@@ -1034,8 +1257,13 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
       cudaSuccess)
     return err;
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
-  err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H,
-                   top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
+  if (L.had)
+    err = launch_pdl(gather_rows_had_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x,
+                     x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
+                     L.suh[0], L.suh[1], xg, xinv);
+  else
+    err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
+                     L.H, top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
   note_launches(2);
   if (err != cudaSuccess) return err;
   rec(2);
@@ -1049,6 +1277,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.gu_out = gu_buf; gu.n_pos = (size_t)P;
   gu.status = rb.status;
   gu.cluster = cluster_for(L.I / 128);
+  gu.had = L.had;
+  gu.xrow_off = L.had ? P : 0;
   // gate and up share one launch, so they share a width (checked at create)
   if ((err = dispatch_gemm(L.K[0], L.fp8, tm_x, gu, mt * 2 * (L.I / 128), st)) != cudaSuccess)
     return err;
@@ -1063,7 +1293,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   rec(3);
 
   err = launch_pdl(swiglu_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
-                   (const float*)gu_buf, (size_t)P, L.I, hs, hinv);
+                   (const float*)gu_buf, (size_t)P, L.I, (const int32_t*)rb.seg_pairs,
+                   (const int32_t*)rb.ids, L.had ? L.suh[2] : (const uint16_t*)nullptr, hs, hinv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(4);
@@ -1075,6 +1306,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   dn.tiles = tiles; dn.n_tiles = ntiles; dn.xinv = hinv; dn.r_out = r;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
   dn.cluster = cluster_for(L.H / 128);
+  dn.had = L.had;
   err = dispatch_gemm(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
   if (err == cudaSuccess && small_ok) {
     GemmParams ds = dn;

@@ -31,6 +31,13 @@
 // Activations enter as fp16 with a power-of-two scale per (pair, projection)
 // chosen from the row's max |x * suh| and undone in the epilogue, so the fp16
 // operand never overflows whatever the input magnitude.
+//
+// Format v2 (Hadamard rotation): the input passes rotate each 128-input block
+// of x * suh (h * suh for down) before the scale is chosen: a thread's 16
+// inputs in registers, the 8 threads of a block by shuffles.  The epilogue
+// rotates each item's partial sums over its 128-output strip (16 outputs of a
+// lane in registers, the 8 lane quads by shuffles) before svh; the rotation
+// is linear, so rotating every K-split partial equals rotating their sum.
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -120,19 +127,32 @@ __device__ __forceinline__ void put16(uint32_t* o, int b, int slot, const float 
   }
 }
 
+// Format v2: rotate the 128-input block of which this thread holds 16
+// consecutive inputs (threads 8j .. 8j+7 hold one block, all active).
+__device__ __forceinline__ void rotate_block16(float (&f)[16]) {
+  wht_regs(f);
+  const unsigned gm = 0xFFu << (threadIdx.x & 24);
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+    for (int q = 0; q < 16; q++) f[q] = wht_lane(f[q], m, gm);
+}
+
 __device__ __forceinline__ float amax16(float a, const float (&f)[16]) {
 #pragma unroll
   for (int q = 0; q < 16; q++) a = fmaxf(a, fabsf(f[q]));
   return a;
 }
 
-// x rows of the pairs, times suh of gate and up, scaled, into the
-// group-interleaved layout [group][proj][in/16][8 tokens][16] (fp16x2).
+// x rows of the pairs, times suh of gate and up (rotated when had), scaled,
+// into the group-interleaved layout [group][proj][in/16][8 tokens][16]
+// (fp16x2).  blockDim is a multiple of 8, so thread b's block shares its
+// 128-input block with threads b ^ 1 .. b ^ 7 in every step.
 __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__ x, int x_bf16,
                                                         int H, int k, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_g,
                                                         const uint16_t* __restrict__ suh_u,
-                                                        uint32_t* __restrict__ xs,
+                                                        int had, uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
@@ -158,6 +178,10 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
     for (int q = 0; q < 16; q++) {
       fg[q] = fx[q] * a[q];
       fu[q] = fx[q] * c[q];
+    }
+    if (had) {
+      rotate_block16(fg);
+      rotate_block16(fu);
     }
   };
   float cg[16], cu[16];
@@ -191,18 +215,19 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
     put16(ou, b, slot, fu, scu);
   }
   if (threadIdx.x == 0) {
-    xs_inv[2 * pos] = ldexpf(1.0f, -eg);
-    xs_inv[2 * pos + 1] = ldexpf(1.0f, -eu);
+    const int hs = had ? kHadShift : 0;  // the unnormalized rotations' 128
+    xs_inv[2 * pos] = ldexpf(1.0f, -eg - hs);
+    xs_inv[2 * pos + 1] = ldexpf(1.0f, -eu - hs);
   }
 }
 
 // h = silu(g) * u for each position's row (g and u summed over the gate/up
-// launch's K splits in split order), times suh of down, scaled,
-// group-interleaved (the down projection's B operand).
+// launch's K splits in split order), times suh of down (rotated when had),
+// scaled, group-interleaved (the down projection's B operand).
 __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, int ns,
                                                         size_t n_pos, int I, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
-                                                        uint32_t* __restrict__ xs,
+                                                        int had, uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
@@ -235,6 +260,7 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
     }
 #pragma unroll
     for (int q = 0; q < 16; q++) h[q] = silu_f(gg[q]) * uu[q] * sv[q];
+    if (had) rotate_block16(h);
   };
   float c[16];
   float am = 0.0f;
@@ -258,7 +284,7 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
     hval(b, h);
     put16(o, b, slot, h, sc);
   }
-  if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex);
+  if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex - (had ? kHadShift : 0));
 }
 
 template <int K, int FP8>
@@ -359,7 +385,7 @@ __device__ __forceinline__ int grab_item(int32_t* work) {
   return __shfl_sync(0xffffffffu, it, 0);
 }
 
-template <int K, int FP8>
+template <int K, int FP8, int HAD>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   using C = Cfg<K>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -500,6 +526,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
       }
       __syncwarp();  // the slot is refilled by a later issue
     }
+    if constexpr (HAD != 0) {
+      // rotate over the strip's 128 outputs: lane (g_l, c_l) holds outputs
+      // 16 g_l + 8 dh + i as acc[i][2 dh + u] for its tokens u = 0, 1
+#pragma unroll
+      for (int u = 0; u < 2; u++) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) v[i] = acc[i & 7][2 * (i >> 3) + u];
+        wht_regs(v);
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1)
+#pragma unroll
+          for (int i = 0; i < 16; i++) v[i] = wht_lane(v[i], m, 0xffffffffu);
+#pragma unroll
+        for (int i = 0; i < 16; i++) acc[i & 7][2 * (i >> 3) + u] = v[i];
+      }
+    }
     // this item's scaled partial sums into its split slab
     float* dst = p.gu_out ? p.gu_out : p.r_out;
     const uint32_t svw[8] = {sv_lo.x, sv_lo.y, sv_lo.z, sv_lo.w, sv_hi.x, sv_hi.y, sv_hi.z, sv_hi.w};
@@ -520,11 +563,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   cp_async_wait<0>();
 }
 
-template <int K, int FP8>
+template <int K, int FP8, int HAD>
 cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
   using C = Cfg<K>;
   static int occ = -1, sms = 0;
-  auto kfn = gemv_kernel<K, FP8>;
+  auto kfn = gemv_kernel<K, FP8, HAD>;
   if (occ < 0) {
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
@@ -547,15 +590,24 @@ cudaError_t launch_gemv(const GemvParams& gp, int items_ub, cudaStream_t st) {
   return err;
 }
 
-cudaError_t dispatch_gemv(int K, int fp8, const GemvParams& gp, int items_ub, cudaStream_t st) {
+// format v2 (had) rotates in the epilogue: its own instantiations, so the
+// format v1 kernels are unchanged by it
+template <int HAD>
+cudaError_t dispatch_gemv_fmt(int K, int fp8, const GemvParams& gp, int items_ub, cudaStream_t st) {
   if (fp8) {
-    if (K == 2) return launch_gemv<2, 1>(gp, items_ub, st);
-    if (K == 3) return launch_gemv<3, 1>(gp, items_ub, st);
-    return launch_gemv<4, 1>(gp, items_ub, st);
+    if (K == 2) return launch_gemv<2, 1, HAD>(gp, items_ub, st);
+    if (K == 3) return launch_gemv<3, 1, HAD>(gp, items_ub, st);
+    return launch_gemv<4, 1, HAD>(gp, items_ub, st);
   }
-  if (K == 2) return launch_gemv<2, 0>(gp, items_ub, st);
-  if (K == 3) return launch_gemv<3, 0>(gp, items_ub, st);
-  return launch_gemv<4, 0>(gp, items_ub, st);
+  if (K == 2) return launch_gemv<2, 0, HAD>(gp, items_ub, st);
+  if (K == 3) return launch_gemv<3, 0, HAD>(gp, items_ub, st);
+  return launch_gemv<4, 0, HAD>(gp, items_ub, st);
+}
+
+cudaError_t dispatch_gemv(int K, int fp8, int had, const GemvParams& gp, int items_ub,
+                          cudaStream_t st) {
+  return had ? dispatch_gemv_fmt<1>(K, fp8, gp, items_ub, st)
+             : dispatch_gemv_fmt<0>(K, fp8, gp, items_ub, st);
 }
 
 // K splits: the smallest power of two that gives ~8 items per resident warp
@@ -625,8 +677,8 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
   if ((err = cudaMemsetAsync(gb.counters, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return err;
-  err = launch_pdl(gather_xs_kernel, dim3(P), dim3(L.H / 16 < 256 ? L.H / 16 : 256), 0, st, x, x_bf16, L.H, top_k, rb, L.suh[0],
-                   L.suh[1], gb.xs_gu, gb.xs_gu_inv);
+  err = launch_pdl(gather_xs_kernel, dim3(P), dim3(L.H / 16 < 256 ? L.H / 16 : 256), 0, st, x,
+                   x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, gb.xs_gu, gb.xs_gu_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(2);
@@ -641,13 +693,13 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
   gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.gu_out = gb.gu; gu.n_pos = (size_t)P;
   gu.work = gb.counters; gu.nsplit = gb.ns_gu;
-  if ((err = dispatch_gemv(L.K[0], L.fp8, gu, (int)(G * 2 * (L.I / 128) * gu.nsplit), st)) !=
+  if ((err = dispatch_gemv(L.K[0], L.fp8, L.had, gu, (int)(G * 2 * (L.I / 128) * gu.nsplit), st)) !=
       cudaSuccess)
     return err;
   rec(3);
 
-  err = launch_pdl(prep_down_kernel, dim3(P), dim3(L.I / 16 < 256 ? L.I / 16 : 256), 0, st, gb.gu, gb.ns_gu, (size_t)P, L.I, rb,
-                   L.suh[2], gb.xs_d, gb.xs_d_inv);
+  err = launch_pdl(prep_down_kernel, dim3(P), dim3(L.I / 16 < 256 ? L.I / 16 : 256), 0, st, gb.gu,
+                   gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(4);
@@ -660,7 +712,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r; dn.n_pos = (size_t)P;
   dn.work = gb.counters + 1; dn.nsplit = gb.ns_d;
-  err = dispatch_gemv(L.K[2], L.fp8, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
+  err = dispatch_gemv(L.K[2], L.fp8, L.had, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
   rec(5);
   return err;
 }

@@ -39,6 +39,7 @@ class LayerSpec:
     K: tuple = (2, 2, 2)
     fp8_round: bool = False
     shared: bool = False
+    hadamard: bool = False  # format v2 (rotation on both sides); no effect on the draws
 
     def dims(self, proj: int):
         """(in_features, out_features) of projection 0=gate, 1=up, 2=down."""
