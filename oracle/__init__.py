@@ -47,7 +47,7 @@ class OracleLayer(ctypes.Structure):
         ("K", ctypes.c_int * 3), ("fp8_round", ctypes.c_int), ("mult", ctypes.c_uint32),
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
-        ("hadamard", ctypes.c_int),
+        ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
     ]
 
 
@@ -220,7 +220,9 @@ class Layer:
     """Holds numpy arrays of one layer (host copies) and its oracle view."""
 
     def __init__(self, num_experts, hidden, inter, K, codes, suh, svh, fp8_round=False,
-                 mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False):
+                 mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False, shared_coded=False):
+        """num_experts routed experts; with shared_coded the code and side
+        arrays hold num_experts + 1 experts, the last one the shared expert."""
         self.arrays = []
         st = OracleLayer()
         st.num_experts, st.hidden, st.inter = num_experts, hidden, inter
@@ -229,6 +231,7 @@ class Layer:
         st.fp8_round = int(bool(fp8_round))
         st.mult = mult
         st.hadamard = int(bool(hadamard))
+        st.shared_coded = int(bool(shared_coded))
         for p in range(3):
             c = np.ascontiguousarray(codes[p], dtype=np.uint16)
             a = np.ascontiguousarray(suh[p], dtype=np.uint16)

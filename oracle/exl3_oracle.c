@@ -356,6 +356,8 @@ typedef struct {
     const uint16_t *svh[3];   /* [E][out] fp16 */
     const uint16_t *shared_w[3]; /* dense fp16 [in][out] or NULL */
     int hadamard;      /* 1: format v2, the 128-point rotation on both sides */
+    int shared_coded;  /* 1: expert num_experts of the code arrays is a trellis-coded shared
+                          expert that every token uses with weight 1 */
 } oracle_layer;
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -499,6 +501,10 @@ static void shared_row(const oracle_layer *L, const double *x, double *y)
 /* MoE layer forward for a subset of tokens (tokens are independent).
  * x: [T][H] bf16 or fp16 bits; logits: [T][E] fp32; tokens: n_sel token
  * indices; y: [n_sel][H] doubles, y_t = sum_{j=0..k-1} r_{t,j} (+ shared).
+ * With shared_coded the shared term is the trellis-coded expert E applied
+ * with weight 1 after the routed pairs (page "GLM-5.3-Flash · exlr8
+ * (K2/K3/K4)", Loading: the shared expert is stored as expert 288, after the
+ * routed ones, at the routed experts' width).
  * Each used expert is decoded once.  Returns 0 on success. */
 int oracle_moe_forward(const oracle_layer *L, const uint16_t *x, int x_is_bf16,
                        const float *logits, int T, int k, const int32_t *tokens, int n_sel,
@@ -539,6 +545,17 @@ int oracle_moe_forward(const oracle_layer *L, const uint16_t *x, int x_is_bf16,
                 expert_row(L, e, Vg, Vu, Vd, xr + (size_t)(p / k) * H, (double)w[p],
                            r + (size_t)p * H);
     }
+    double *rs = NULL;
+    if (L->shared_coded) {
+        rs = (double *)malloc((size_t)n_sel * H * sizeof(double));
+        if (!rs)
+            return 1;
+        decode_proj_double(L, 0, E, Vg);
+        decode_proj_double(L, 1, E, Vu);
+        decode_proj_double(L, 2, E, Vd);
+        for (int s = 0; s < n_sel; s++)
+            expert_row(L, E, Vg, Vu, Vd, xr + (size_t)s * H, 1.0, rs + (size_t)s * H);
+    }
     free(Vg);
     free(Vu);
     free(Vd);
@@ -549,9 +566,13 @@ int oracle_moe_forward(const oracle_layer *L, const uint16_t *x, int x_is_bf16,
         for (int j = 0; j < k; j++)
             for (int o = 0; o < H; o++)
                 ys[o] += r[((size_t)s * k + j) * H + o];
+        if (rs)
+            for (int o = 0; o < H; o++)
+                ys[o] += rs[(size_t)s * H + o];
         if (L->shared_w[0])
             shared_row(L, xr + (size_t)s * H, ys);
     }
+    free(rs);
     free(ids);
     free(w);
     free(xr);

@@ -500,3 +500,59 @@ def test_layer_hadamard_closed_form_zero_codes():
         want = np.zeros(H)
         want[::128] = c * I * (G / (1 + math.exp(-G))) * G
         assert np.allclose(y[t], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+# ------------------------------------------------------------ coded shared expert
+
+
+def test_layer_shared_coded_vs_numpy_dense_reference():
+    """A trellis-coded shared expert stored after the routed experts (index E
+    of the code arrays) adds expert_E(x) with weight 1 to every token: numpy
+    matmul on decode_dense weights (fp64)."""
+    E, H, I, K, T, k = 5, 64, 32, (3, 3, 2), 4, 2
+    _, codes, suh, svh, _ = _small_layer(8, E + 1, H, I, K, False, False)
+    L = oracle.Layer(E, H, I, K, codes, suh, svh, shared_coded=True)
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x, False, logits, k)
+    ids, w, _, _ = oracle.route(logits, k)
+    assert ids.max() < E
+    xf = x.view(np.float16).astype(np.float64)
+    f = lambda a: a.view(np.float16).astype(np.float64)
+
+    def expert(e, xt):
+        W = [f(oracle.decode_dense(codes[p][e], *((I, H) if p == 2 else (H, I)), K[p]))
+             for p in range(3)]
+        g = ((xt * f(suh[0][e])) @ W[0]) * f(svh[0][e])
+        u = ((xt * f(suh[1][e])) @ W[1]) * f(svh[1][e])
+        h = g / (1 + np.exp(-g)) * u
+        return ((h * f(suh[2][e])) @ W[2]) * f(svh[2][e])
+
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            ref[t] += float(w[t, j]) * expert(ids[t, j], xf[t])
+        ref[t] += expert(E, xf[t])
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-9 * np.abs(ref).max())
+
+
+def test_layer_shared_coded_closed_form_zero_codes():
+    """Zero codes for every expert, unit side vectors, top_k = 1: the routed
+    expert (weight 1) and the shared one compute the same closed form
+    (test_layer_closed_form_zero_codes), so y_o = 2 * 1.84375 * I * h."""
+    E, H, I, T = 3, 48, 32, 4
+    codes = [np.zeros((E + 1, (I if p == 2 else H) // 16, (H if p == 2 else I) // 16, 32), np.uint16)
+             for p in range(3)]
+    one = np.uint16(0x3C00)
+    suh = [np.full((E + 1, I if p == 2 else H), one, np.uint16) for p in range(3)]
+    svh = [np.full((E + 1, H if p == 2 else I), one, np.uint16) for p in range(3)]
+    L = oracle.Layer(E, H, I, (2, 2, 2), codes, suh, svh, shared_coded=True)
+    rng = np.random.default_rng(3)
+    x = (0.05 * rng.standard_normal((T, H))).astype(np.float16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x.view(np.uint16), False, logits, 1)
+    for t in range(T):
+        G = 1.84375 * x[t].astype(np.float64).sum()
+        h = G / (1 + math.exp(-G)) * G
+        assert np.allclose(y[t], 2 * 1.84375 * I * h, rtol=1e-13)
