@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
     ap.add_argument("--hadamard", action="store_true",
                     help="format v2: the workload's layer with the 128-point Hadamard rotation")
+    ap.add_argument("--shared-coded", action="store_true",
+                    help="the shared expert trellis-coded as one more expert (weight 1), "
+                         "replacing a dense one")
     return ap.parse_args()
 
 
@@ -86,12 +89,12 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: flo
 # profiles/gemv_kernel_K2_decode.md; reported only while the kernel sources
 # hash to what was captured (otherwise null).
 NCU_TRAFFIC = {
-    ("decode", "gate_up"): 128.093440e6 + 4.645120e6,
-    ("decode", "down"): 63.688192e6 + 0.931328e6,
+    ("decode", "gate_up"): 128.092928e6 + 4.347136e6,
+    ("decode", "down"): 63.688704e6 + 0.863232e6,
 }
 NCU_SOURCES = {
-    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "27ab4b195a7e5aa1616493edd62d84c368acc413",
-    "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "acc08b6543c6c9f48b753a60e3a7426762d31149",
+    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "318b212751492c487eb9778e510184fe1d9beddb",
+    "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
 }
 
 
@@ -179,7 +182,7 @@ def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
     sides = [synth.side_vectors(spec, p) for p in range(3)]
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
-                      shared_w=shared_w, hadamard=spec.hadamard)
+                      shared_w=shared_w, hadamard=spec.hadamard, shared_coded=spec.shared_coded)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     t0 = time.perf_counter()
     for j in range(n_pairs):
@@ -190,10 +193,11 @@ def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
     if shared_w is not None:
         ol.shared_row(x[0], wl.act == "bf16")
     t_shared = time.perf_counter() - t1
-    per_token = wl.top_k * t_pairs + t_shared
+    kp = wl.top_k + int(spec.shared_coded)  # the coded shared expert costs one more pair
+    per_token = kp * t_pairs + t_shared
     sample = (f"{n_pairs} (token, expert) pair(s) of the {wl.T}-token {wl.name} workload"
               + (" + the shared expert of one token" if shared_w is not None else "")
-              + f"; tokens/s = 1 / ({wl.top_k} x pair time"
+              + f"; tokens/s = 1 / ({kp} x pair time"
               + (" + shared time)" if shared_w is not None else ")"))
     return 1.0 / per_token, time.perf_counter() - t0, sample
 
@@ -215,7 +219,8 @@ def run_reference(args):
     sw = synth.shared_weights(spec) if spec.shared else None
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], shared_w=sw,
-                      fp8_round=spec.fp8_round, hadamard=spec.hadamard)
+                      fp8_round=spec.fp8_round, hadamard=spec.hadamard,
+                      shared_coded=spec.shared_coded)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
     for s in range(args.warmup):
@@ -230,10 +235,11 @@ def run_reference(args):
         t, j = pairs[(args.warmup + s) % len(pairs)]
         ol.expert_pair(x[t], wl.act == "bf16", int(ids[t, j]), float(w[t, j]))
     t_pair = (time.perf_counter() - t0) / args.steps
-    per_token = wl.top_k * t_pair + t_shared
+    kp = wl.top_k + int(spec.shared_coded)  # the coded shared expert costs one more pair
+    per_token = kp * t_pair + t_shared
     value = 1.0 / per_token
     sample = (f"one (token, expert) pair of the {wl.T}-token {wl.name} workload per step; tokens/s = "
-              f"1 / ({wl.top_k} x mean pair time"
+              f"1 / ({kp} x mean pair time"
               + (" + shared-expert time of one token)" if sw is not None else ")"))
     line = {
         "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
@@ -263,6 +269,9 @@ def pick_workload(args):
     if args.hadamard:
         spec = dataclasses.replace(spec, hadamard=True)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-hadamard")
+    if args.shared_coded:
+        spec = dataclasses.replace(spec, shared=False, shared_coded=True)
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-sharedcoded")
     return wl, spec
 
 
@@ -270,7 +279,9 @@ def workload_config(wl):
     s = wl.layers[0]
     return {"workload": (f"{wl.name}: {s.num_experts} experts top-{wl.top_k}, hidden {s.hidden}, "
                          f"inter {s.inter}, K={list(s.K)}, T={wl.T} {wl.act}"
-                         + (", + fp16 shared expert" if s.shared else "")),
+                         + (", + fp16 shared expert" if s.shared else "")
+                         + (", + trellis-coded shared expert" if s.shared_coded else "")
+                         + (", Hadamard rotation (format v2)" if s.hadamard else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
             "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round, "hadamard": s.hadamard,
             "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
@@ -309,7 +320,7 @@ def run_ours(args):
     d_svh = [t16(s[1]).view(torch.float16) for s in sides]
     d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
     layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw,
-                  hadamard=spec.hadamard)
+                  hadamard=spec.hadamard, shared_coded=spec.shared_coded)
     x = t16(x_np).view(torch.bfloat16)
     lg = torch.from_numpy(lg_np).to(dev)
     T, k = wl.T, wl.top_k
@@ -334,6 +345,8 @@ def run_ours(args):
     # counts behind the algorithmic work of each kernel
     _, _, r_off, _ = route(lg, k)
     counts = torch.diff(r_off).cpu().numpy()
+    if spec.shared_coded:  # its segment holds every token
+        counts = np.append(counts, T)
     n_active = int((counts > 0).sum())
 
     # headline graph: the forward alone
@@ -456,8 +469,8 @@ def run_ours(args):
     code_b = [H * I * spec.K[p] // 8 for p in range(3)]
     side_b = [(H + I) * 2] * 3
     stage_names = _lib.STAGE_NAMES
-    P = T * k
-    gemm_path = P >= 16 * spec.num_experts
+    P = T * (k + int(spec.shared_coded))          # pairs, the coded shared expert's included
+    gemm_path = P >= 16 * spec.n_coded
     # weight decodes: every expert's weights once per token group (GEMV: <= 8
     # tokens) or token tile (GEMM: <= 512 tokens)
     per = 512 if gemm_path else 8

@@ -82,6 +82,13 @@ typedef struct {
                                     entries (-1)^popcount(i & j) / sqrt(128) ([p4]
                                     Calibration names the 128x128 Hadamard matrix as a
                                     format primitive).  Other values: EXL3_ERR_ARG */
+    int shared_coded;            /* 1: the code, suh and svh arrays hold num_experts + 1
+                                    experts, the last one a trellis-coded shared expert
+                                    that every token uses with weight 1, after its routed
+                                    pairs ([p4] Loading: the shared expert is stored as
+                                    expert 288, after the routed experts, at their width).
+                                    Requires shared_w all NULL and num_experts + 1 <= 1024.
+                                    num_experts stays the router's width (logit columns). */
 } exl3_layer_desc;
 
 /* Validate `desc` and build a handle.  codes, suh, svh and shared_w must be
@@ -97,8 +104,8 @@ typedef struct {
 exl3_status exl3_layer_create(const exl3_layer_desc *desc, exl3_layer_t **out);
 void exl3_layer_destroy(exl3_layer_t *layer);
 
-/* Decode projection `proj` of `expert` to a dense fp16 matrix out[in][out]
- * (device).  apply_side = 0: the codebook values (after the E4M3 rule when the
+/* Decode projection `proj` of `expert` (0 .. num_experts - 1 + shared_coded)
+ * to a dense fp16 matrix out[in][out] (device).  apply_side = 0: the codebook values (after the E4M3 rule when the
  * layer has fp8_round); apply_side = 1: fp16(fp32(fp32(v*suh[i])*svh[o])).
  * The Hadamard rotation of format v2 is never applied here: this is the
  * element-wise, bit-exact check path for the codes ([p2] Cold prefill: the
@@ -159,9 +166,10 @@ size_t exl3_moe_workspace_size(const exl3_layer_t *layer, int T, int top_k);
 /* One MoE layer forward ([p2] Cold prefill (E3): gather, gate/up + SwiGLU,
  * down + scatter; [p1] Running it: decodes the trellis inside the matmul):
  *   x      device [T][H] in dtype dt (fp16 or bf16)
- *   logits device fp32 [T][E]
+ *   logits device fp32 [T][E], E = num_experts (routed experts)
  *   out    device [T][H] in dtype dt; y_t = sum_j w_tj * expert_{id_tj}(x_t)
- *          (+ shared(x_t)), summed over j in order, no atomics
+ *          (+ shared(x_t)), summed over j in order, no atomics; a coded
+ *          shared expert is the last term, a dense one is added after it
  *   ws     device workspace of >= exl3_moe_workspace_size(layer, T, top_k)
  * out may not alias x. */
 exl3_status exl3_moe_forward(const exl3_layer_t *layer, const void *x, exl3_dtype dt,

@@ -72,6 +72,17 @@ def test_layer_create_validation(L):
     d = _desc()
     d.hadamard = 2                                              # 0 (format v1) or 1 (v2)
     assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    d = _desc()
+    d.shared_coded = 2                                          # 0 or 1
+    assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    d = _desc()
+    d.shared_coded = 1                                          # dense or coded, not both
+    for p in range(3):
+        d.shared_w[p] = 8192 * (p + 1)
+    assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    d = _desc(E=1024)
+    d.shared_coded = 1                                          # 1025 experts in the tables
+    assert _create(L, d)[0] == _lib.EXL3_ERR_SHAPE
 
 
 def test_route_validation_and_sizes(L):

@@ -264,12 +264,33 @@ def test_forward_hadamard(H, I, K, fp8, shared, T, k, routing, path):
     assert device_status(layer.workspace(T, k)) == 0
 
 
+# ------------------------------------------------------------------ coded shared expert
+
+
+@pytest.mark.parametrize("E,H,I,K,fp8,had,T,k,routing,path", [
+    (10, 384, 256, (2, 2, 3), False, False, 9, 3, "normal", 1),     # GEMV
+    (8, 512, 256, (3, 3, 4), True, True, 40, 4, "normal", 1),       # GEMV, format v2
+    (20, 256, 128, (2, 2, 2), False, False, 5, 16, "normal", 1),    # 17 pairs per token
+    (8, 512, 256, (4, 4, 4), False, False, 120, 4, "normal", 2),    # shared segment: small tile
+    (8, 512, 256, (3, 3, 2), False, True, 700, 4, "zipf", 2),       # shared segment: 2 big tiles
+    (6, 256, 128, (2, 2, 2), False, False, 1, 1, "normal", 0),      # one token, top-1
+])
+def test_forward_shared_coded(E, H, I, K, fp8, had, T, k, routing, path):
+    """A trellis-coded shared expert (the last expert of the arrays) routed
+    as one more pair per token with weight 1, on both paths."""
+    spec = synth.LayerSpec(seed=110 + sum(K), num_experts=E, hidden=H, inter=I, K=K,
+                           fp8_round=fp8, hadamard=had, shared_coded=True)
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=path, routing=routing)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
 # ------------------------------------------------------------------ workloads
 
 
-def _workload_parity(name, tokens_fn, path=0, hadamard=False):
+def _workload_parity(name, tokens_fn, path=0, **spec_changes):
     wl = synth.WORKLOADS[name]
-    spec = dataclasses.replace(wl.layers[0], hadamard=hadamard)
+    spec = dataclasses.replace(wl.layers[0], **spec_changes)
     hl = HostLayer(spec)
     layer = hl.device()
     x, logits = synth.workload_inputs(wl)
@@ -308,6 +329,11 @@ def test_prefill_workload_sampled():
 def test_decode_workload_hadamard_all_tokens():
     """The decode workload's layer in format v2 (GEMV path, full size)."""
     _workload_parity("decode", lambda wl, lg: list(range(wl.T)), hadamard=True)
+
+
+def test_decode_workload_shared_coded_all_tokens():
+    """The decode workload with its shared expert trellis-coded as expert 288."""
+    _workload_parity("decode", lambda wl, lg: list(range(wl.T)), shared=False, shared_coded=True)
 
 
 def test_prefill_workload_hadamard_sampled():

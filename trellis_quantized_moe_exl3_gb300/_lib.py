@@ -29,7 +29,7 @@ class LayerDesc(ctypes.Structure):
         ("K", ctypes.c_int * 3), ("fp8_round", ctypes.c_int), ("mcg_mult", ctypes.c_uint32),
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
-        ("hadamard", ctypes.c_int),
+        ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
     ]
 
 

@@ -48,14 +48,17 @@ class Layer:
     [E, in/16, out/16, 16*K[p]]; suh[p]: fp16 [E, in]; svh[p]: fp16 [E, out];
     shared (optional): three fp16 dense [in, out] matrices.  p = 0 gate,
     1 up, 2 down.  hadamard: format v2 (the 128-point Hadamard rotation on
-    both sides of every routed projection).  The tensors must stay alive as
-    long as the layer.
+    both sides of every routed projection).  shared_coded: the last expert of
+    the arrays is a trellis-coded shared expert (weight 1 for every token);
+    the router then has E - 1 columns.  The tensors must stay alive as long
+    as the layer.
     """
 
     def __init__(self, codes, suh, svh, K, fp8_round=False, mcg_mult=0, shared=None,
-                 hadamard=False):
+                 hadamard=False, shared_coded=False):
         c0 = codes[0]
         E, nti, nto, w = c0.shape
+        E -= int(bool(shared_coded))  # routed experts
         H, I = nti * 16, nto * 16
         self.E, self.H, self.I = E, H, I
         self.K = tuple(int(k) for k in K)
@@ -73,6 +76,7 @@ class Layer:
         d.fp8_round = int(bool(fp8_round))
         d.mcg_mult = int(mcg_mult)
         d.hadamard = int(bool(hadamard))
+        d.shared_coded = int(bool(shared_coded))
         h = ctypes.c_void_p()
         check(_lib.lib().exl3_layer_create(ctypes.byref(d), ctypes.byref(h)), "exl3_layer_create")
         self._h = h

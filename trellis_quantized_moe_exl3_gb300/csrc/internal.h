@@ -73,12 +73,17 @@ inline size_t max_groups(int T, int E, int top_k) {
   return a < P ? a : P;
 }
 
+// E and top_k here count every table entry: with a coded shared expert,
+// E + 1 experts and top_k + 1 pairs per token.
 size_t route_scratch_bytes(int T, int E, int top_k);
 // Carves RouteBuffers out of `ws` (ids/w/seg may be caller-provided: non-null
 // fields of `given` are kept).
 void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb);
+// E = logits per token, top_k = routed pairs per token; shared = 1 appends
+// pair (expert E, weight 1) to every token (tables of E + 1 experts,
+// top_k + 1 pairs per token).
 cudaError_t launch_route(const float* logits, int T, int E, int top_k, const RouteBuffers& rb,
-                         cudaStream_t st);
+                         cudaStream_t st, int shared = 0);
 
 struct LayerView {
   int E, H, I;
@@ -91,6 +96,8 @@ struct LayerView {
   const uint16_t* shared_w[3];
   size_t code_stride[3];  // uint16 words per expert
   int had;                // format v2: Hadamard rotation on both sides of each projection
+  int sc;                 // 1: expert E - 1 of the arrays is the coded shared expert
+                          // (E counts it; the logits have E - sc columns)
 };
 
 cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int apply_side,

@@ -54,8 +54,11 @@ bool use_gemm(const LayerView& L, int T, int top_k, int path) {
   return (size_t)T * top_k >= (size_t)16 * L.E;
 }
 
-FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k) {
+// k = routed pairs per token; the tables hold k + L.sc (the coded shared
+// expert's pair) per token over L.E experts.
+FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k_routed) {
   FwdLayout f{};
+  const int k = k_routed + L.sc;
   const size_t P = (size_t)T * k;
   size_t o = 0;
   f.route = o; o += al(route_scratch_bytes(T, L.E, k));
@@ -100,6 +103,8 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   if (!(mult & 1u)) return EXL3_ERR_ARG;
   int nshared = 0;
   if (d->hadamard != 0 && d->hadamard != 1) return EXL3_ERR_ARG;
+  if (d->shared_coded != 0 && d->shared_coded != 1) return EXL3_ERR_ARG;
+  if (d->num_experts + d->shared_coded > kMaxExperts) return EXL3_ERR_SHAPE;
   for (int p = 0; p < 3; p++) {
     if (!d->codes[p] || !d->suh[p] || !d->svh[p]) return EXL3_ERR_ARG;
     if (!aligned16(d->codes[p]) || !aligned16(d->suh[p]) || !aligned16(d->svh[p]))
@@ -108,12 +113,14 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
     if (d->shared_w[p] && !aligned16(d->shared_w[p])) return EXL3_ERR_ARG;
   }
   if (nshared != 0 && nshared != 3) return EXL3_ERR_ARG;
+  if (nshared && d->shared_coded) return EXL3_ERR_ARG;  // one shared expert at most
   exl3_status ds = check_device();
   if (ds != EXL3_OK) return ds;
   exl3_layer* L = static_cast<exl3_layer*>(calloc(1, sizeof(exl3_layer)));
   if (!L) return EXL3_ERR_ARG;
   LayerView& v = L->v;
-  v.E = d->num_experts; v.H = d->hidden; v.I = d->inter;
+  v.sc = d->shared_coded;
+  v.E = d->num_experts + v.sc; v.H = d->hidden; v.I = d->inter;
   v.fp8 = d->fp8_round ? 1 : 0;
   v.mult = mult;
   v.had = d->hadamard;
@@ -192,7 +199,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (dt != EXL3_F16 && dt != EXL3_BF16) return EXL3_ERR_ARG;
   if (path < EXL3_PATH_AUTO || path > EXL3_PATH_GEMM) return EXL3_ERR_ARG;
   if (T < 0) return EXL3_ERR_SHAPE;
-  if (top_k < 1 || top_k > kMaxTopK || top_k > L.E) return EXL3_ERR_ARG;
+  if (top_k < 1 || top_k > kMaxTopK || top_k > L.E - L.sc) return EXL3_ERR_ARG;
   if (T == 0) return EXL3_OK;
   if (!x || !logits || !out) return EXL3_ERR_ARG;
   if (!aligned16(x) || !aligned16(out) || (residual && !aligned16(residual))) return EXL3_ERR_ARG;
@@ -202,8 +209,11 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (ws_bytes < f.total) return EXL3_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
+  // with a coded shared expert every token has one more pair (expert E - 1,
+  // weight 1), and from here on the expert kernels see kp pairs per token
+  const int kp = top_k + L.sc;
   RouteBuffers rb{};
-  route_carve(base + f.route, T, L.E, top_k, &rb);
+  route_carve(base + f.route, T, L.E, kp, &rb);
   rb.ids = reinterpret_cast<int32_t*>(base + f.ids);
   rb.w = reinterpret_cast<float*>(base + f.w);
   rb.seg_offsets = reinterpret_cast<int32_t*>(base + f.off);
@@ -216,7 +226,8 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   };
   rec(0);
   if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
-  if (launch_route(logits, T, L.E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (launch_route(logits, T, L.E - L.sc, top_k, rb, st, L.sc) != cudaSuccess)
+    return EXL3_ERR_CUDA;
   // shared expert: forked onto the side stream once routing is done, so it
   // overlaps the expert kernels (which take their work dynamically and do not
   // mind SMs it occupies) instead of delaying the one-CTA routing kernel
@@ -234,14 +245,13 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
 
   float* pair_rows = nullptr;
   int pair_splits = 1;
-  if (use_gemm(L, T, top_k, path)) {
-    if (launch_moe_gemm(L, x, bf16, T, top_k, rb, base + f.gemv, ev, &pair_rows, st) !=
-        cudaSuccess)
+  if (use_gemm(L, T, kp, path)) {
+    if (launch_moe_gemm(L, x, bf16, T, kp, rb, base + f.gemv, ev, &pair_rows, st) != cudaSuccess)
       return EXL3_ERR_CUDA;
   } else {
     GemvBuffers gb{};
-    gemv_carve(base + f.gemv, T, top_k, L.E, L.H, L.I, &gb);
-    if (launch_moe_gemv(L, x, bf16, T, top_k, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
+    gemv_carve(base + f.gemv, T, kp, L.E, L.H, L.I, &gb);
+    if (launch_moe_gemv(L, x, bf16, T, kp, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
     pair_rows = gb.r;
     pair_splits = gb.ns_d;
   }
@@ -249,7 +259,8 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (layer->has_shared && cudaStreamWaitEvent(st, layer->join, 0) != cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(6);
-  if (launch_combine(pair_rows, pair_splits, T, top_k, L.H, sp, ns, residual, out, bf16, st) != cudaSuccess)
+  if (launch_combine(pair_rows, pair_splits, T, kp, L.H, sp, ns, residual, out, bf16, st) !=
+      cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(7);
   return EXL3_OK;

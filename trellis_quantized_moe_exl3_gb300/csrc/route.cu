@@ -11,6 +11,12 @@
 // seg_offsets[e] counts pairs with expert < e; seg_pairs lists pair ids
 // t*k + j expert-major and ascending inside an expert (a stable counting
 // sort: per-chunk counts, a scan over (expert, chunk), a scatter by rank).
+//
+// A layer whose shared expert is trellis-coded (page "GLM-5.3-Flash · exlr8
+// (K2/K3/K4)", Loading: the shared expert is stored as expert 288, after the
+// routed ones) routes it as one more pair per token: pair t*(k+1) + k has
+// expert E (the logits' width) and weight 1, so the tables cover E + 1
+// experts and the expert kernels treat it like any other segment.
 #include "common.cuh"
 #include "internal.h"
 
@@ -121,30 +127,37 @@ __device__ __forceinline__ void write_groups(const RouteBuffers& rb, int e, int 
 
 // Per-chunk stage: top-k of kRouteChunk tokens, local stable ranks and
 // per-expert counts.  With `fused` (single chunk) it also finishes the
-// tables: offsets, active list and scatter.
+// tables: offsets, active list and scatter.  E: logits per token (routed
+// experts); sh = 1 appends the shared pair (expert E, weight 1) to each token,
+// so pairs are t * (k + sh) + j and the tables cover E + sh experts.
 template <int MAXPL>
 __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restrict__ logits, int T,
-                                                           int E, int k, RouteBuffers rb,
+                                                           int E, int k, int sh, RouteBuffers rb,
                                                            int fused) {
   pdl_wait();
-  __shared__ int s_ids[kRouteChunk * kMaxTopK];
+  __shared__ int s_ids[kRouteChunk * (kMaxTopK + 1)];
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_warp[32];
   const int chunk = blockIdx.x;
   const int t0 = chunk * kRouteChunk;
   const int nt = min(kRouteChunk, T - t0);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int kp = k + sh, Et = E + sh;  // pairs per token, experts in the tables
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) s_cnt[e] = 0;
   for (int tl = wid; tl < nt; tl += nw) {
     const int t = t0 + tl;
     int id;
     float wt;
     warp_topk<MAXPL>(logits + (size_t)t * E, E, k, &id, &wt);
     if (lane < k) {
-      rb.ids[(size_t)t * k + lane] = id;
-      rb.w[(size_t)t * k + lane] = wt;
-      s_ids[tl * k + lane] = id;
+      rb.ids[(size_t)t * kp + lane] = id;
+      rb.w[(size_t)t * kp + lane] = wt;
+      s_ids[tl * kp + lane] = id;
+    } else if (lane < kp) {  // the shared expert
+      rb.ids[(size_t)t * kp + lane] = E;
+      rb.w[(size_t)t * kp + lane] = 1.0f;
+      s_ids[tl * kp + lane] = E;
     }
   }
   __syncthreads();
@@ -152,43 +165,43 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
   // token are distinct, so lane j can bump its counter without conflicts
   if (wid == 0) {
     for (int tl = 0; tl < nt; tl++) {
-      if (lane < k) {
-        const int e = s_ids[tl * k + lane];
+      if (lane < kp) {
+        const int e = s_ids[tl * kp + lane];
         const int r = s_cnt[e];
         s_cnt[e] = r + 1;
-        rb.rank[(size_t)(t0 + tl) * k + lane] = r;
+        rb.rank[(size_t)(t0 + tl) * kp + lane] = r;
       }
       __syncwarp();
     }
   }
   __syncthreads();
   if (!fused) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      rb.chunk_counts[(size_t)chunk * E + e] = s_cnt[e];
+    for (int e = threadIdx.x; e < Et; e += blockDim.x)
+      rb.chunk_counts[(size_t)chunk * Et + e] = s_cnt[e];
     return;
   }
   // fused: offsets = exclusive scan of the counts, active list, scatter
   int total = 0, n_act = 0, n_grp = 0;
-  const int cnt = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
+  const int cnt = threadIdx.x < Et ? s_cnt[threadIdx.x] : 0;
   const int off = block_exclusive_scan(cnt, s_warp, &total);
   const int aidx = block_exclusive_scan(cnt > 0 ? 1 : 0, s_warp, &n_act);
   const int ng = (cnt + kGroup - 1) / kGroup;
   const int goff = block_exclusive_scan(ng, s_warp, &n_grp);
-  if (threadIdx.x < E) {
+  if (threadIdx.x < Et) {
     rb.seg_offsets[threadIdx.x] = off;
     if (cnt > 0) rb.active[1 + aidx] = threadIdx.x;
     write_groups(rb, threadIdx.x, off, cnt, goff);
   }
   if (threadIdx.x == 0) {
-    rb.seg_offsets[E] = total;
+    rb.seg_offsets[Et] = total;
     rb.active[0] = n_act;
-    rb.group_off[E] = n_grp;
+    rb.group_off[Et] = n_grp;
   }
   __syncthreads();
-  if (threadIdx.x < E) s_cnt[threadIdx.x] = off;  // segment starts
+  if (threadIdx.x < Et) s_cnt[threadIdx.x] = off;  // segment starts
   __syncthreads();
-  for (int pl = threadIdx.x; pl < nt * k; pl += blockDim.x) {
-    const size_t p = (size_t)t0 * k + pl;
+  for (int pl = threadIdx.x; pl < nt * kp; pl += blockDim.x) {
+    const size_t p = (size_t)t0 * kp + pl;
     const int e = s_ids[pl];
     const int pos = s_cnt[e] + rb.rank[p];
     rb.seg_pairs[pos] = (int)p;
@@ -256,17 +269,17 @@ __global__ void route_empty_kernel(int E, RouteBuffers rb) {
 }
 
 template <int MAXPL>
-cudaError_t launch_chunks(const float* logits, int T, int E, int k, const RouteBuffers& rb,
+cudaError_t launch_chunks(const float* logits, int T, int E, int k, int sh, const RouteBuffers& rb,
                           int nchunks, cudaStream_t st) {
   // one chunk: the scans need a thread per expert, the top-k a warp per token
   // (in turns); fewer warps make the CTA's barriers cheaper
   int threads = 512;
   if (nchunks == 1) {
-    const int need_e = (E + 31) / 32 * 32, need_t = 32 * (T < 16 ? T : 16);
+    const int need_e = (E + sh + 31) / 32 * 32, need_t = 32 * (T < 16 ? T : 16);
     threads = need_e > need_t ? need_e : need_t;
   }
   const cudaError_t err = launch_pdl(route_chunk_kernel<MAXPL>, dim3(nchunks), dim3(threads), 0, st,
-                                     logits, T, E, k, rb, (int)(nchunks == 1));
+                                     logits, T, E, k, sh, rb, (int)(nchunks == 1));
   note_launches(1);
   return err;
 }
@@ -309,26 +322,27 @@ void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb) {
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBuffers& rb,
-                         cudaStream_t st) {
+                         cudaStream_t st, int shared) {
+  const int sh = shared ? 1 : 0;
   if (T == 0) {
-    const cudaError_t e = launch_pdl(route_empty_kernel, dim3(1), dim3(256), 0, st, E, rb);
+    const cudaError_t e = launch_pdl(route_empty_kernel, dim3(1), dim3(256), 0, st, E + sh, rb);
     note_launches(1);
     return e;
   }
   const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
   const int pl = (E + 31) / 32;
   cudaError_t err;
-  if (pl <= 1) err = launch_chunks<1>(logits, T, E, k, rb, nchunks, st);
-  else if (pl <= 2) err = launch_chunks<2>(logits, T, E, k, rb, nchunks, st);
-  else if (pl <= 4) err = launch_chunks<4>(logits, T, E, k, rb, nchunks, st);
-  else if (pl <= 9) err = launch_chunks<9>(logits, T, E, k, rb, nchunks, st);
-  else if (pl <= 16) err = launch_chunks<16>(logits, T, E, k, rb, nchunks, st);
-  else err = launch_chunks<32>(logits, T, E, k, rb, nchunks, st);
+  if (pl <= 1) err = launch_chunks<1>(logits, T, E, k, sh, rb, nchunks, st);
+  else if (pl <= 2) err = launch_chunks<2>(logits, T, E, k, sh, rb, nchunks, st);
+  else if (pl <= 4) err = launch_chunks<4>(logits, T, E, k, sh, rb, nchunks, st);
+  else if (pl <= 9) err = launch_chunks<9>(logits, T, E, k, sh, rb, nchunks, st);
+  else if (pl <= 16) err = launch_chunks<16>(logits, T, E, k, sh, rb, nchunks, st);
+  else err = launch_chunks<32>(logits, T, E, k, sh, rb, nchunks, st);
   if (err != cudaSuccess || nchunks == 1) return err;
-  err = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, rb);
+  err = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, E + sh, nchunks, rb);
   note_launches(1);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, rb);
+  err = launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(256), 0, st, T, E + sh, k + sh, rb);
   note_launches(1);
   return err;
 }

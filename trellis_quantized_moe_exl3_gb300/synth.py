@@ -40,6 +40,12 @@ class LayerSpec:
     fp8_round: bool = False
     shared: bool = False
     hadamard: bool = False  # format v2 (rotation on both sides); no effect on the draws
+    shared_coded: bool = False  # one more coded expert (the shared one) after the routed ones
+
+    @property
+    def n_coded(self) -> int:
+        """Experts in the code and side-vector arrays."""
+        return self.num_experts + int(self.shared_coded)
 
     def dims(self, proj: int):
         """(in_features, out_features) of projection 0=gate, 1=up, 2=down."""
@@ -95,10 +101,10 @@ def expert_codes(spec: LayerSpec, proj: int, expert: int) -> np.ndarray:
 def layer_codes(spec: LayerSpec, proj: int, out: np.ndarray | None = None) -> np.ndarray:
     """Code words of every expert, [E][in/16][out/16][16K]."""
     i, o = spec.dims(proj)
-    shape = (spec.num_experts, i // 16, o // 16, 16 * spec.K[proj])
+    shape = (spec.n_coded, i // 16, o // 16, 16 * spec.K[proj])
     if out is None:
         out = np.empty(shape, dtype=np.uint16)
-    for e in range(spec.num_experts):
+    for e in range(spec.n_coded):
         out[e] = expert_codes(spec, proj, e)
     return out
 
@@ -107,8 +113,8 @@ def side_vectors(spec: LayerSpec, proj: int):
     """suh [E][in], svh [E][out]: fp16 bits of round(1 + 0.1 N(0,1))."""
     i, o = spec.dims(proj)
     g = _rng(spec.seed, TAG_SIDE, proj)
-    suh = (1.0 + 0.1 * g.standard_normal((spec.num_experts, i))).astype(np.float16)
-    svh = (1.0 + 0.1 * g.standard_normal((spec.num_experts, o))).astype(np.float16)
+    suh = (1.0 + 0.1 * g.standard_normal((spec.n_coded, i))).astype(np.float16)
+    svh = (1.0 + 0.1 * g.standard_normal((spec.n_coded, o))).astype(np.float16)
     return suh.view(np.uint16), svh.view(np.uint16)
 
 
