@@ -148,6 +148,16 @@ __device__ __forceinline__ void halves16(const LaneWords<K>& lw, uint32_t mult, 
   }
 }
 
+// Tile (of the 8 in a code row) that lane decodes, quad lane c = lane & 3 of
+// it.  Tiles g and g ^ 2 share a quarter warp (lanes 8q .. 8q + 7), so the 8
+// lanes of every 16-byte store phase of decode_store land in 8 different
+// 16-byte bank groups of the swizzled stage (with g = lane >> 2 the pairs g,
+// g ^ 1 collide two ways).
+__device__ __forceinline__ int dec_tile(int lane) {
+  const int l4 = lane >> 2;
+  return (l4 & 4) | ((l4 & 1) << 1) | ((l4 >> 1) & 1);
+}
+
 // Decode this lane's 64 weights of one tile and store them into the MN-major
 // A stage: lane (g, c) holds outputs 16g..16g+15 (rows of the strip) for
 // inputs c, c+4, c+8, c+12 of the block.  off[4hf + 2jh + jl] is the lane's
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- decode
     const int blk = warp % kJobs;
     const int ks0 = warp / kJobs;
-    const int g = lane >> 2, c = lane & 3;
+    const int g = dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
                                                             (pj ? p.stride[1] : p.stride[0]) * e) +
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto lane_codes = [&](int n) {
       const int ks = ks0 + n * kPar;
       return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
-             lane * 4 * K;
+             (g * 4 + c) * 4 * K;
     };
     // code rows are pulled into L2 kL2Ahead jobs ahead, so the register
     // prefetch one job ahead hits L2
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int blk = warp % 4;
     const int half = (warp / 4) % 2;
     const int ks0 = warp / kSJobs;
-    const int g = lane >> 2, c = lane & 3;
+    const int g = dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
                                                             (pj ? p.stride[1] : p.stride[0]) * e) +
@@ -617,7 +627,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     auto lane_codes = [&](int n) {
       const int ks = ks0 + n * kSPar;
       return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
-             lane * 4 * K;
+             (g * 4 + c) * 4 * K;
     };
     constexpr int kL2Ahead = 8;
     auto prefetch_l2 = [&](int n) {
