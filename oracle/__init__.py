@@ -48,6 +48,7 @@ class OracleLayer(ctypes.Structure):
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
         ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
+        ("expert_K", ctypes.c_void_p),
     ]
 
 
@@ -220,9 +221,13 @@ class Layer:
     """Holds numpy arrays of one layer (host copies) and its oracle view."""
 
     def __init__(self, num_experts, hidden, inter, K, codes, suh, svh, fp8_round=False,
-                 mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False, shared_coded=False):
+                 mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False, shared_coded=False,
+                 expert_K=None):
         """num_experts routed experts; with shared_coded the code and side
-        arrays hold num_experts + 1 experts, the last one the shared expert."""
+        arrays hold num_experts + 1 experts, the last one the shared expert.
+        expert_K ([experts][3] widths) gives every expert and projection its
+        own width; codes[p] is then a flat array of the experts' codes back to
+        back (K is ignored)."""
         self.arrays = []
         st = OracleLayer()
         st.num_experts, st.hidden, st.inter = num_experts, hidden, inter
@@ -232,6 +237,12 @@ class Layer:
         st.mult = mult
         st.hadamard = int(bool(hadamard))
         st.shared_coded = int(bool(shared_coded))
+        if expert_K is not None:
+            ek = np.ascontiguousarray(expert_K, dtype=np.uint8)
+            self.arrays.append(ek)
+            st.expert_K = ek.ctypes.data
+        else:
+            st.expert_K = None
         for p in range(3):
             c = np.ascontiguousarray(codes[p], dtype=np.uint16)
             a = np.ascontiguousarray(suh[p], dtype=np.uint16)

@@ -358,6 +358,9 @@ typedef struct {
     int hadamard;      /* 1: format v2, the 128-point rotation on both sides */
     int shared_coded;  /* 1: expert num_experts of the code arrays is a trellis-coded shared
                           expert that every token uses with weight 1 */
+    const uint8_t *expert_K; /* NULL, or [experts][3] widths per expert and projection: the
+                                codes of projection p are then the experts' arrays back to
+                                back, each at its own width */
 } oracle_layer;
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -408,14 +411,36 @@ void oracle_hadamard_blocks(double *v, int n)
 
 /* Decode projection p of expert e to doubles [in][out] (codebook values,
  * side vectors not applied). */
+/* Width of projection p of expert e, and the word offset of its codes.
+ * reading: pages "GLM-5.3-Flash · exlr8 (K2/K3/K4)", Loading (manifests that
+ * give some experts or projections another width) and
+ * "GLM-5.3-Flash-EXL3-TR3-3.5bpw" (every routed tensor K3 or K4) mix widths
+ * inside a layer without giving a file layout; the plainest one stores each
+ * projection's experts back to back, expert e after experts 0 .. e-1, each
+ * at its own width. */
+static int proj_width(const oracle_layer *L, int p, int e)
+{
+    return L->expert_K ? L->expert_K[(size_t)e * 3 + p] : L->K[p];
+}
+
+static size_t proj_offset(const oracle_layer *L, int p, int e)
+{
+    int in = (p == 2) ? L->inter : L->hidden;
+    int out = (p == 2) ? L->hidden : L->inter;
+    size_t tile_words = (size_t)(in / 16) * (out / 16) * 16;
+    size_t off = 0;
+    for (int f = 0; f < e; f++)
+        off += tile_words * proj_width(L, p, f);
+    return off;
+}
+
 static void decode_proj_double(const oracle_layer *L, int p, int e, double *dst)
 {
     int in = (p == 2) ? L->inter : L->hidden;
     int out = (p == 2) ? L->hidden : L->inter;
-    int K = L->K[p];
-    size_t per_expert = (size_t)(in / 16) * (out / 16) * 16 * K;
+    int K = proj_width(L, p, e);
     uint16_t *tmp = (uint16_t *)malloc((size_t)in * out * sizeof(uint16_t));
-    oracle_decode_dense(L->codes[p] + per_expert * e, in, out, K, L->mult, L->fp8_round,
+    oracle_decode_dense(L->codes[p] + proj_offset(L, p, e), in, out, K, L->mult, L->fp8_round,
                         NULL, NULL, 0, tmp);
     for (size_t i = 0; i < (size_t)in * out; i++)
         dst[i] = oracle_f16_to_double(tmp[i]);

@@ -556,3 +556,70 @@ def test_layer_shared_coded_closed_form_zero_codes():
         G = 1.84375 * x[t].astype(np.float64).sum()
         h = G / (1 + math.exp(-G)) * G
         assert np.allclose(y[t], 2 * 1.84375 * I * h, rtol=1e-13)
+
+
+# ------------------------------------------------------------ per-expert widths
+
+
+def _mixed_layer(seed, E, H, I, shared_coded=False):
+    """Flat per-projection code arrays, each expert at its own width."""
+    rng = np.random.default_rng(seed)
+    n = E + int(shared_coded)
+    ek = rng.integers(2, 5, size=(n, 3)).astype(np.uint8)
+    codes, per = [], []
+    for p in range(3):
+        fi, fo = (I, H) if p == 2 else (H, I)
+        parts = [rng.integers(0, 65536, size=(fi // 16) * (fo // 16) * 16 * int(ek[e, p]),
+                              dtype=np.uint16) for e in range(n)]
+        per.append(parts)
+        codes.append(np.concatenate(parts))
+    suh = [(1 + 0.1 * rng.standard_normal((n, I if p == 2 else H))).astype(np.float16).view(np.uint16)
+           for p in range(3)]
+    svh = [(1 + 0.1 * rng.standard_normal((n, H if p == 2 else I))).astype(np.float16).view(np.uint16)
+           for p in range(3)]
+    return ek, codes, per, suh, svh
+
+
+@pytest.mark.parametrize("shared_coded", [False, True])
+def test_layer_mixed_widths_vs_numpy_dense_reference(shared_coded):
+    """Every expert and projection at its own width (codes back to back):
+    numpy matmul on each expert's decode_dense weights at its width."""
+    E, H, I, T, k = 5, 64, 32, 4, 2
+    ek, codes, per, suh, svh = _mixed_layer(12, E, H, I, shared_coded)
+    L = oracle.Layer(E, H, I, (2, 2, 2), codes, suh, svh, shared_coded=shared_coded, expert_K=ek)
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x, False, logits, k)
+    ids, w, _, _ = oracle.route(logits, k)
+    xf = x.view(np.float16).astype(np.float64)
+    f = lambda a: a.view(np.float16).astype(np.float64)
+
+    def expert(e, xt):
+        W = [f(oracle.decode_dense(per[p][e].reshape(-1), *((I, H) if p == 2 else (H, I)),
+                                   int(ek[e, p]))) for p in range(3)]
+        g = ((xt * f(suh[0][e])) @ W[0]) * f(svh[0][e])
+        u = ((xt * f(suh[1][e])) @ W[1]) * f(svh[1][e])
+        h = g / (1 + np.exp(-g)) * u
+        return ((h * f(suh[2][e])) @ W[2]) * f(svh[2][e])
+
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            ref[t] += float(w[t, j]) * expert(ids[t, j], xf[t])
+        if shared_coded:
+            ref[t] += expert(E, xf[t])
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-9 * np.abs(ref).max())
+
+
+def test_layer_uniform_width_table_equals_plain_layer():
+    """A width table that gives every expert the projection's width is the
+    plain layout ([E][in/16][out/16][16K], expert e at e times the stride)."""
+    E, H, I, K, T, k = 4, 64, 32, (3, 3, 4), 3, 2
+    L0, codes, suh, svh, _ = _small_layer(14, E, H, I, K, False, False)
+    ek = np.tile(np.array(K, np.uint8), (E, 1))
+    L1 = oracle.Layer(E, H, I, (2, 2, 2), [c.reshape(-1) for c in codes], suh, svh, expert_K=ek)
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    assert np.array_equal(L0.forward(x, False, logits, k), L1.forward(x, False, logits, k))
