@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
     ap.add_argument("--hadamard", action="store_true",
                     help="format v2: the workload's layer with the 128-point Hadamard rotation")
+    ap.add_argument("--mixed", action="store_true",
+                    help="every expert tensor K3 or K4 (seeded), the 3.5 bpw mixed recipe")
     ap.add_argument("--shared-coded", action="store_true",
                     help="the shared expert trellis-coded as one more expert (weight 1), "
                          "replacing a dense one")
@@ -182,7 +184,8 @@ def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
     sides = [synth.side_vectors(spec, p) for p in range(3)]
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
-                      shared_w=shared_w, hadamard=spec.hadamard, shared_coded=spec.shared_coded)
+                      shared_w=shared_w, hadamard=spec.hadamard, shared_coded=spec.shared_coded,
+                      expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     t0 = time.perf_counter()
     for j in range(n_pairs):
@@ -220,7 +223,8 @@ def run_reference(args):
     ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                       [s[0] for s in sides], [s[1] for s in sides], shared_w=sw,
                       fp8_round=spec.fp8_round, hadamard=spec.hadamard,
-                      shared_coded=spec.shared_coded)
+                      shared_coded=spec.shared_coded,
+                      expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
     ids, w, _, _ = oracle.route(logits, wl.top_k)
     pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
     for s in range(args.warmup):
@@ -272,6 +276,9 @@ def pick_workload(args):
     if args.shared_coded:
         spec = dataclasses.replace(spec, shared=False, shared_coded=True)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-sharedcoded")
+    if args.mixed:
+        spec = dataclasses.replace(spec, expert_K=synth.mixed_widths(spec.seed, spec.n_coded))
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-mixedK34")
     return wl, spec
 
 
@@ -281,7 +288,8 @@ def workload_config(wl):
                          f"inter {s.inter}, K={list(s.K)}, T={wl.T} {wl.act}"
                          + (", + fp16 shared expert" if s.shared else "")
                          + (", + trellis-coded shared expert" if s.shared_coded else "")
-                         + (", Hadamard rotation (format v2)" if s.hadamard else "")),
+                         + (", Hadamard rotation (format v2)" if s.hadamard else "")
+                         + (", every expert tensor K3 or K4 (seeded)" if s.expert_K else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
             "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round, "hadamard": s.hadamard,
             "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
@@ -320,7 +328,7 @@ def run_ours(args):
     d_svh = [t16(s[1]).view(torch.float16) for s in sides]
     d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
     layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw,
-                  hadamard=spec.hadamard, shared_coded=spec.shared_coded)
+                  hadamard=spec.hadamard, shared_coded=spec.shared_coded, expert_K=spec.expert_K)
     x = t16(x_np).view(torch.bfloat16)
     lg = torch.from_numpy(lg_np).to(dev)
     T, k = wl.T, wl.top_k
@@ -466,29 +474,37 @@ def run_ours(args):
     # roofline of the dominant expert kernel (the larger of gate/up and down)
     hbm, bf16_tf, src = peaks()
     H, I = spec.hidden, spec.inter
-    code_b = [H * I * spec.K[p] // 8 for p in range(3)]
-    side_b = [(H + I) * 2] * 3
+    side_b = (H + I) * 2
     stage_names = _lib.STAGE_NAMES
     P = T * (k + int(spec.shared_coded))          # pairs, the coded shared expert's included
     gemm_path = P >= 16 * spec.n_coded
-    # weight decodes: every expert's weights once per token group (GEMV: <= 8
-    # tokens) or token tile (GEMM: <= 512 tokens)
-    per = 512 if gemm_path else 8
-    units = int(sum((int(c) + per - 1) // per for c in counts))
-    dec_w = {"gate_up": units * 2 * H * I, "down": units * H * I}
-    flops = {"gate_up": 2.0 * P * H * I * 2, "down": 2.0 * P * H * I}
-    code_bytes = {"gate_up": n_active * (code_b[0] + code_b[1] + side_b[0] + side_b[1]),
-                  "down": n_active * (code_b[2] + side_b[2])}
-    dom = max(("gate_up", "down"), key=lambda n: stage_ms[stage_names.index(n)])
-    dom_ms = float(stage_ms[stage_names.index(dom)])
-    kdom = spec.K[0] if dom == "gate_up" else spec.K[2]
     # issue-slot peak of the trellis decode: 128 lane-instructions per SM and
     # clock, 152 SMs, 2070 MHz maximum clock; K = 2 and 4 need 4 integer
     # instructions per weight (window, multiply, correction, mask-xor: two on
     # the ALU pipe, two on the FMA pipe), K = 3 needs 3 on the 64-lane ALU pipe
     # (window, mask, mask-xor) besides the multiply
     sms, clk_hz = 152, 2.070e9
-    peak_wps = sms * clk_hz * (128 / 4 if kdom in (2, 4) else 64 / 3)
+    peak_k = {kk: sms * clk_hz * (128 / 4 if kk in (2, 4) else 64 / 3) for kk in (2, 3, 4)}
+    # weight decodes: every expert's weights once per token group (GEMV: <= 8
+    # tokens) or token tile (GEMM: <= 512 tokens), at the expert's width
+    per = 512 if gemm_path else 8
+    dec_w = {"gate_up": 0, "down": 0}
+    dec_t = {"gate_up": 0.0, "down": 0.0}   # decodes / peak of their width: seconds at peak
+    code_bytes = {"gate_up": 0, "down": 0}
+    for e, c in enumerate(counts):
+        if c <= 0:
+            continue
+        u = (int(c) + per - 1) // per
+        for pr in range(3):
+            st_name = "down" if pr == 2 else "gate_up"
+            kk = spec.width(pr, e)
+            dec_w[st_name] += u * H * I
+            dec_t[st_name] += u * H * I / peak_k[kk]
+            code_bytes[st_name] += H * I * kk // 8 + side_b
+    flops = {"gate_up": 2.0 * P * H * I * 2, "down": 2.0 * P * H * I}
+    dom = max(("gate_up", "down"), key=lambda n: stage_ms[stage_names.index(n)])
+    dom_ms = float(stage_ms[stage_names.index(dom)])
+    peak_wps = dec_w[dom] / dec_t[dom]   # the widths' peaks, weighted by their decodes
     dec_rate = dec_w[dom] / (dom_ms / 1e3)
     hbm_rate = code_bytes[dom] / (dom_ms / 1e3) / 1e9
     if gemm_path:

@@ -89,10 +89,22 @@ typedef struct {
                                     expert 288, after the routed experts, at their width).
                                     Requires shared_w all NULL and num_experts + 1 <= 1024.
                                     num_experts stays the router's width (logit columns). */
+    const uint8_t *expert_K;     /* host, optional: [num_experts + shared_coded][3] code width
+                                    (2..4) of every expert and projection ([p4] Loading: the
+                                    bit201 and bit349 manifests give some experts or
+                                    projections another width; [p5] Rates: every routed
+                                    tensor K3 or K4).  With it K[] is ignored and codes[p]
+                                    holds the experts' codes back to back: expert e at word
+                                    offset sum over f < e of (in/16)(out/16)*16*expert_K[f][p].
+                                    Copied at create (which then allocates two small device
+                                    tables, freed by exl3_layer_destroy).  NULL: K[p] for
+                                    every expert. */
 } exl3_layer_desc;
 
 /* Validate `desc` and build a handle.  codes, suh, svh and shared_w must be
- * 16-byte aligned.  A layer with a shared expert also
+ * 16-byte aligned.  Gate and up may differ in width (K[0] != K[1]): such a
+ * layer, like one with expert_K, runs its expert kernels once per width over
+ * device-built work lists.  A layer with a dense shared expert also
  * creates one CUDA stream and two events on the current device (released by
  * exl3_layer_destroy); the shared expert of every forward runs on that stream,
  * forked from the caller's stream after routing and joined before the

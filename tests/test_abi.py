@@ -52,7 +52,10 @@ def test_layer_create_validation(L):
     assert _create(L, _desc(I=64))[0] == _lib.EXL3_ERR_SHAPE
     assert _create(L, _desc(K=(1, 1, 2)))[0] == _lib.EXL3_ERR_K
     assert _create(L, _desc(K=(2, 2, 5)))[0] == _lib.EXL3_ERR_K
-    assert _create(L, _desc(K=(2, 3, 2)))[0] == _lib.EXL3_ERR_K   # gate/up share a width
+    ek = (ctypes.c_uint8 * 24)(*([3, 4, 2] * 7 + [3, 5, 2]))       # a width table entry of 5
+    d = _desc()
+    d.expert_K = ctypes.cast(ek, ctypes.c_void_p)
+    assert _create(L, d)[0] == _lib.EXL3_ERR_K
     d = _desc()
     d.mcg_mult = 2                                              # multiplier must be odd
     assert _create(L, d)[0] == _lib.EXL3_ERR_ARG

@@ -285,6 +285,44 @@ def test_forward_shared_coded(E, H, I, K, fp8, had, T, k, routing, path):
     assert device_status(layer.workspace(T, k)) == 0
 
 
+# ------------------------------------------------------------------ mixed widths
+
+
+@pytest.mark.parametrize("E,H,I,fp8,had,sc,T,k,routing,path", [
+    (10, 384, 256, False, False, False, 37, 4, "normal", 1),   # GEMV
+    (8, 512, 256, True, True, True, 40, 4, "normal", 1),       # GEMV, format v2, coded shared
+    (8, 512, 256, False, False, False, 120, 4, "normal", 2),   # small tiles
+    (8, 512, 256, True, False, True, 700, 4, "zipf", 2),       # big and small tiles
+    (6, 384, 384, False, True, False, 300, 4, "normal", 2),    # big tiles only
+])
+def test_forward_mixed_widths(E, H, I, fp8, had, sc, T, k, routing, path):
+    """A width per expert and projection (K2, K3 or K4; codes back to back):
+    the expert kernels run once per width over device-built work lists."""
+    seed = 130 + E + T
+    spec = synth.LayerSpec(seed=seed, num_experts=E, hidden=H, inter=I, K=(2, 2, 2),
+                           fp8_round=fp8, hadamard=had, shared_coded=sc,
+                           expert_K=synth.mixed_widths(seed, E + int(sc), (2, 3, 4)))
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=path, routing=routing)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+    hl = HostLayer(spec)
+    for e in range(E + int(sc)):  # decode_dense at each expert's own width
+        for p in range(3):
+            fin, fout = spec.dims(p)
+            o = sum(spec.code_words_per_expert(p, f) for f in range(e))
+            words = hl.codes[p][o:o + spec.code_words_per_expert(p, e)]
+            ref_d = oracle.decode_dense(words, fin, fout, spec.width(p, e), fp8_round=fp8)
+            assert np.array_equal(_u16(layer.decode_dense(e, p)), ref_d)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["gemv", "gemm"])
+def test_forward_gate_up_widths_differ(path):
+    """Gate and up of different widths (K[0] != K[1]) without a table."""
+    spec = synth.LayerSpec(seed=140, num_experts=8, hidden=512, inter=256, K=(3, 4, 2))
+    out, ref, layer = _run_small(spec, 200 if path == 2 else 20, 4, "bf16", path=path)
+    assert_layer_close(out, ref)
+
+
 # ------------------------------------------------------------------ workloads
 
 
@@ -329,6 +367,14 @@ def test_prefill_workload_sampled():
 def test_decode_workload_hadamard_all_tokens():
     """The decode workload's layer in format v2 (GEMV path, full size)."""
     _workload_parity("decode", lambda wl, lg: list(range(wl.T)), hadamard=True)
+
+
+def test_verify_workload_mixed_widths_sampled():
+    """The verify workload with every expert tensor K3 or K4 (the 3.5 bpw
+    mixed recipe), full size, GEMV path."""
+    wl = synth.WORKLOADS["verify3"]
+    ek = synth.mixed_widths(wl.layers[0].seed, wl.layers[0].num_experts)
+    _workload_parity("verify3", lambda wl, lg: [0, 9, 22, 31], expert_K=ek)
 
 
 def test_decode_workload_shared_coded_all_tokens():

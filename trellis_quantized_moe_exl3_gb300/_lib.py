@@ -30,6 +30,7 @@ class LayerDesc(ctypes.Structure):
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
         ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
+        ("expert_K", ctypes.c_void_p),
     ]
 
 

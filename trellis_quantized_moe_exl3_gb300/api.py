@@ -50,18 +50,24 @@ class Layer:
     1 up, 2 down.  hadamard: format v2 (the 128-point Hadamard rotation on
     both sides of every routed projection).  shared_coded: the last expert of
     the arrays is a trellis-coded shared expert (weight 1 for every token);
-    the router then has E - 1 columns.  The tensors must stay alive as long
+    the router then has E - 1 columns.  expert_K ([E][3] ints): a width per
+    expert and projection; codes[p] is then a flat tensor of the experts'
+    codes back to back (K is ignored).  The tensors must stay alive as long
     as the layer.
     """
 
     def __init__(self, codes, suh, svh, K, fp8_round=False, mcg_mult=0, shared=None,
-                 hadamard=False, shared_coded=False):
-        c0 = codes[0]
-        E, nti, nto, w = c0.shape
+                 hadamard=False, shared_coded=False, expert_K=None):
+        E, H = suh[0].shape
+        I = svh[0].shape[1]
         E -= int(bool(shared_coded))  # routed experts
-        H, I = nti * 16, nto * 16
         self.E, self.H, self.I = E, H, I
         self.K = tuple(int(k) for k in K)
+        self._ek = None
+        if expert_K is not None:
+            import numpy as np
+            self._ek = np.ascontiguousarray(np.asarray(expert_K, dtype=np.uint8))
+            assert self._ek.shape == (E + int(bool(shared_coded)), 3)
         self._keep = [*codes, *suh, *svh] + (list(shared) if shared is not None else [])
         for t in self._keep:
             _req(t, "layer tensor")
@@ -77,6 +83,7 @@ class Layer:
         d.mcg_mult = int(mcg_mult)
         d.hadamard = int(bool(hadamard))
         d.shared_coded = int(bool(shared_coded))
+        d.expert_K = self._ek.ctypes.data if self._ek is not None else None
         h = ctypes.c_void_p()
         check(_lib.lib().exl3_layer_create(ctypes.byref(d), ctypes.byref(h)), "exl3_layer_create")
         self._h = h

@@ -62,7 +62,7 @@ cudaError_t launch_k(const LayerView& L, int expert, int proj, int apply_side, u
                      cudaStream_t st) {
   const int in = proj == 2 ? L.I : L.H;
   const int outf = proj == 2 ? L.H : L.I;
-  const uint16_t* codes = L.codes[proj] + L.code_stride[proj] * (size_t)expert;
+  const uint16_t* codes = L.codes[proj] + layer_code_offset(L, expert, proj);
   const uint16_t* suh = L.suh[proj] + (size_t)expert * in;
   const uint16_t* svh = L.svh[proj] + (size_t)expert * outf;
   const int warps = (in / 16) * (outf / 128);
@@ -81,7 +81,7 @@ cudaError_t launch_k(const LayerView& L, int expert, int proj, int apply_side, u
 
 cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int apply_side,
                                 uint16_t* out, cudaStream_t st) {
-  switch (L.K[proj]) {
+  switch (layer_width(L, expert, proj)) {
     case 2: return launch_k<2>(L, expert, proj, apply_side, out, st);
     case 3: return launch_k<3>(L, expert, proj, apply_side, out, st);
     default: return launch_k<4>(L, expert, proj, apply_side, out, st);

@@ -98,7 +98,22 @@ struct LayerView {
   int had;                // format v2: Hadamard rotation on both sides of each projection
   int sc;                 // 1: expert E - 1 of the arrays is the coded shared expert
                           // (E counts it; the logits have E - sc columns)
+  // Mixed widths (a width per expert and projection, or gate and up of
+  // different widths): the expert kernels run once per width over work lists.
+  int mixed;
+  const int32_t* d_kt;             // device [E][3] widths
+  const unsigned long long* d_off; // device [E][3] code word offsets
+  const uint8_t* h_kt;             // host copies of both
+  const size_t* h_off;
 };
+
+// Width of projection p of expert e and the word offset of its codes.
+inline int layer_width(const LayerView& L, int e, int p) {
+  return L.mixed ? L.h_kt[(size_t)e * 3 + p] : L.K[p];
+}
+inline size_t layer_code_offset(const LayerView& L, int e, int p) {
+  return L.mixed ? L.h_off[(size_t)e * 3 + p] : L.code_stride[p] * (size_t)e;
+}
 
 cudaError_t launch_decode_dense(const LayerView& L, int expert, int proj, int apply_side,
                                 uint16_t* out, cudaStream_t st);
@@ -111,7 +126,9 @@ struct GemvBuffers {
   uint32_t* xs_d;    // [group][I/16][8][16] fp16x2 (dup), permuted
   float* xs_d_inv;   // [P]
   float* r;          // [ns_d][P][H] fp32 K-split partial rows by pair id
-  int32_t* counters; // item counters of the two launches
+  int32_t* counters; // item counters: [launch (gate/up, down)][width 2..4]
+  int32_t* n_entries;  // mixed widths: entries per [launch][width]
+  int32_t* entries;    // mixed widths: (group, projection) pairs, [launch][width][cap]
   int ns_gu, ns_d;   // K splits of the two launches
 };
 size_t gemv_scratch_bytes(int T, int top_k, int E, int H, int I);

@@ -19,6 +19,11 @@ struct exl3_layer {
   // caller's stream inside each forward
   cudaStream_t side;
   cudaEvent_t fork, join;
+  // mixed widths: owned width / offset tables (host and device copies)
+  uint8_t* h_kt;
+  size_t* h_off;
+  int32_t* d_kt;
+  unsigned long long* d_off;
 };
 
 namespace {
@@ -96,15 +101,20 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   *out = nullptr;
   if (d->num_experts < 1 || d->num_experts > kMaxExperts) return EXL3_ERR_SHAPE;
   if (d->hidden <= 0 || d->inter <= 0 || d->hidden % 128 || d->inter % 128) return EXL3_ERR_SHAPE;
-  for (int p = 0; p < 3; p++)
-    if (d->K[p] < 2 || d->K[p] > 4) return EXL3_ERR_K;
-  if (d->K[0] != d->K[1]) return EXL3_ERR_K;
+  if (d->shared_coded != 0 && d->shared_coded != 1) return EXL3_ERR_ARG;
+  const int n_coded = d->num_experts + d->shared_coded;  // experts in the arrays
+  if (d->expert_K) {
+    for (int i = 0; i < 3 * n_coded; i++)
+      if (d->expert_K[i] < 2 || d->expert_K[i] > 4) return EXL3_ERR_K;
+  } else {
+    for (int p = 0; p < 3; p++)
+      if (d->K[p] < 2 || d->K[p] > 4) return EXL3_ERR_K;
+  }
   const uint32_t mult = d->mcg_mult ? d->mcg_mult : kDefaultMcgMult;
   if (!(mult & 1u)) return EXL3_ERR_ARG;
   int nshared = 0;
   if (d->hadamard != 0 && d->hadamard != 1) return EXL3_ERR_ARG;
-  if (d->shared_coded != 0 && d->shared_coded != 1) return EXL3_ERR_ARG;
-  if (d->num_experts + d->shared_coded > kMaxExperts) return EXL3_ERR_SHAPE;
+  if (n_coded > kMaxExperts) return EXL3_ERR_SHAPE;
   for (int p = 0; p < 3; p++) {
     if (!d->codes[p] || !d->suh[p] || !d->svh[p]) return EXL3_ERR_ARG;
     if (!aligned16(d->codes[p]) || !aligned16(d->suh[p]) || !aligned16(d->svh[p]))
@@ -125,13 +135,53 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   v.mult = mult;
   v.had = d->hadamard;
   for (int p = 0; p < 3; p++) {
-    v.K[p] = d->K[p];
+    v.K[p] = d->expert_K ? d->expert_K[p] : d->K[p];
     v.codes[p] = d->codes[p];
     v.suh[p] = d->suh[p];
     v.svh[p] = d->svh[p];
     v.shared_w[p] = d->shared_w[p];
     const size_t in = p == 2 ? v.I : v.H, outf = p == 2 ? v.H : v.I;
-    v.code_stride[p] = (in / 16) * (outf / 16) * 16 * (size_t)d->K[p];
+    v.code_stride[p] = (in / 16) * (outf / 16) * 16 * (size_t)v.K[p];
+  }
+  // Mixed widths: a width per expert and projection (expert_K), or gate and
+  // up of different widths.  Codes of a projection lie expert after expert,
+  // each at its own width, so the offsets are running sums.
+  v.mixed = d->expert_K != nullptr || d->K[0] != d->K[1];
+  if (v.mixed) {
+    const size_t n = (size_t)3 * n_coded;
+    L->h_kt = static_cast<uint8_t*>(malloc(n));
+    L->h_off = static_cast<size_t*>(malloc(n * sizeof(size_t)));
+    int32_t* kt32 = static_cast<int32_t*>(malloc(n * sizeof(int32_t)));
+    unsigned long long* off64 = static_cast<unsigned long long*>(malloc(n * sizeof(unsigned long long)));
+    bool ok = L->h_kt && L->h_off && kt32 && off64;
+    if (ok) {
+      size_t run[3] = {0, 0, 0};
+      for (int e = 0; e < n_coded; e++)
+        for (int p = 0; p < 3; p++) {
+          const int k = d->expert_K ? d->expert_K[(size_t)e * 3 + p] : d->K[p];
+          const size_t in = p == 2 ? v.I : v.H, outf = p == 2 ? v.H : v.I;
+          L->h_kt[(size_t)e * 3 + p] = (uint8_t)k;
+          kt32[(size_t)e * 3 + p] = k;
+          L->h_off[(size_t)e * 3 + p] = run[p];
+          off64[(size_t)e * 3 + p] = run[p];
+          run[p] += (in / 16) * (outf / 16) * 16 * (size_t)k;
+        }
+      ok = cudaMalloc(&L->d_kt, n * sizeof(int32_t)) == cudaSuccess &&
+           cudaMalloc(&L->d_off, n * sizeof(unsigned long long)) == cudaSuccess &&
+           cudaMemcpy(L->d_kt, kt32, n * sizeof(int32_t), cudaMemcpyHostToDevice) == cudaSuccess &&
+           cudaMemcpy(L->d_off, off64, n * sizeof(unsigned long long), cudaMemcpyHostToDevice) ==
+               cudaSuccess;
+    }
+    free(kt32);
+    free(off64);
+    v.h_kt = L->h_kt;
+    v.h_off = L->h_off;
+    v.d_kt = L->d_kt;
+    v.d_off = L->d_off;
+    if (!ok) {
+      exl3_layer_destroy(L);
+      return EXL3_ERR_CUDA;
+    }
   }
   L->has_shared = nshared == 3;
   if (L->has_shared) {
@@ -151,6 +201,10 @@ void exl3_layer_destroy(exl3_layer_t* layer) {
   if (layer->side) cudaStreamDestroy(layer->side);
   if (layer->fork) cudaEventDestroy(layer->fork);
   if (layer->join) cudaEventDestroy(layer->join);
+  if (layer->d_kt) cudaFree(layer->d_kt);
+  if (layer->d_off) cudaFree(layer->d_off);
+  free(layer->h_kt);
+  free(layer->h_off);
   free(layer);
 }
 

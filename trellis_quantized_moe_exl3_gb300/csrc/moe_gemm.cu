@@ -84,7 +84,35 @@ struct GemmParams {
   int cluster;              // CTAs per cluster (divides the strip count)
   int had;                  // format v2: suh on the activation side, outputs rotated
   int xrow_off;             // activation row (and scale) offset of projection 1
+  // mixed widths: this launch's list of (tile, projection) pairs whose width
+  // is this instantiation's K, and the experts' code offsets
+  const int32_t* entries;   // [n][2], or null: every tile, every projection
+  const int32_t* n_entries;
+  const unsigned long long* off;  // [E][3] code word offsets, or null: stride * e
+  int proj0;                // global index of this launch's projection 0 (0 or 2)
 };
+
+// (tile, projection) of the CTA's work unit u (its index over strips): from
+// the width's list in mixed mode, else u = tile * nproj + projection.  False
+// past the end of the work (the whole cluster shares u).
+__device__ __forceinline__ bool tile_of(const GemmParams& p, int u, int* tile, int* pj) {
+  if (p.entries) {
+    if (u >= p.n_entries[0]) return false;
+    *tile = p.entries[2 * u];
+    *pj = p.entries[2 * u + 1];
+    return true;
+  }
+  *pj = u % p.nproj;
+  *tile = u / p.nproj;
+  return *tile < p.n_tiles[0];
+}
+
+// First code word of projection pj of expert e.
+__device__ __forceinline__ const uint16_t* gemm_expert_codes(const GemmParams& p, int e, int pj) {
+  return (pj ? p.codes[1] : p.codes[0]) +
+         (p.off ? (size_t)p.off[(size_t)e * 3 + p.proj0 + pj]
+                : (pj ? p.stride[1] : p.stride[0]) * (size_t)e);
+}
 
 // Format v2 epilogue of the M = outputs kernel: the 4 warps of a column group
 // hold the 128 outputs of a strip (TMEM lanes, thread = output) for the same
@@ -198,10 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~(uintptr_t)1023);
   const int strips = p.out / 128;
   const int s = blockIdx.x % strips;
-  const int pj = (blockIdx.x / strips) % p.nproj;
-  const int tile = blockIdx.x / (strips * p.nproj);
   pdl_wait();
-  if (tile >= p.n_tiles[0]) return;  // the whole cluster shares the tile
+  int tile, pj;
+  if (!tile_of(p, blockIdx.x / strips, &tile, &pj)) return;  // the whole cluster shares the tile
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int n0 = cnt < kHalfN ? ((cnt + 15) / 16) * 16 : kHalfN;
   const int n1 = cnt > kHalfN ? ((cnt - kHalfN + 15) / 16) * 16 : 0;
@@ -331,8 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ks0 = warp / kJobs;
     const int g = dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
-    const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
-                                                            (pj ? p.stride[1] : p.stride[0]) * e) +
+    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
                            (size_t)8 * s * 32 * K;
     const int n_my = (nks - ks0 + kPar - 1) / kPar;
     // lane-constant swizzled offsets of this lane's 8 output chunks in a block
@@ -490,10 +516,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                              ~(uintptr_t)1023);
   const int chunks = p.out / kSN;
   const int s = blockIdx.x % chunks;
-  const int pj = (blockIdx.x / chunks) % p.nproj;
-  const int tile = blockIdx.x / (chunks * p.nproj);
   pdl_wait();
-  if (tile >= p.n_tiles[0]) return;  // the whole cluster shares the tile
+  int tile, pj;
+  if (!tile_of(p, blockIdx.x / chunks, &tile, &pj)) return;  // the whole cluster shares the tile
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int nks = p.in / kKS;
   const int tm = cnt <= 64 ? 64 : 128;  // MMA M
@@ -611,8 +636,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int ks0 = warp / kSJobs;
     const int g = dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
-    const uint8_t* cbase = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
-                                                            (pj ? p.stride[1] : p.stride[0]) * e) +
+    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
                            (size_t)8 * (2 * s + half) * 32 * K;
     const int n_my = (nks - ks0 + kSPar - 1) / kSPar;
     int off[8];
@@ -1077,6 +1101,34 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t*
   }
 }
 
+// Mixed widths: split the (tile, projection) work of the four launches (big
+// and small tiles; gate/up and down) into one list per width.  Thread per
+// (tile, projection p of 3).  Segments (in pairs): big gate/up 3 x 2mt, big
+// down 3 x mt, small gate/up 3 x 2E, small down 3 x E; counts[kind * 6 +
+// launch * 3 + width].  The order inside a list does not matter.
+__global__ void __launch_bounds__(256) gemm_width_lists_kernel(
+    const int32_t* __restrict__ n_tiles, const int32_t* __restrict__ tiles,
+    const int32_t* __restrict__ tiles_s, const int32_t* __restrict__ kt, int mt, int E,
+    int32_t* __restrict__ counts, int32_t* __restrict__ entries) {
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int small = i >= 3 * mt;
+  const int j = small ? i - 3 * mt : i;
+  const int t = j / 3, pg = j % 3;
+  if (t >= (small ? n_tiles[1] : n_tiles[0]) || (small && t >= E)) return;
+  const int e = (small ? tiles_s : tiles)[4 * t];
+  const int w = kt[(size_t)e * 3 + pg] - 2;
+  const int launch = pg == 2 ? 1 : 0;
+  const int n = small ? E : mt;  // tiles of this kind at most
+  const size_t seg = small ? (size_t)9 * mt + (launch ? (size_t)6 * E : 0)
+                           : (launch ? (size_t)6 * mt : 0);
+  const size_t cap = launch ? (size_t)n : (size_t)2 * n;
+  const int slot = atomicAdd(&counts[small * 6 + launch * 3 + w], 1);
+  int32_t* en = entries + (seg + (size_t)w * cap + slot) * 2;
+  en[0] = t;
+  en[1] = launch ? 0 : pg;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1205,7 +1257,7 @@ size_t max_tiles(int T, int E, int top_k) {
 }
 
 struct GemmLayout {
-  size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, total;
+  size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, counts, lists, total;
 };
 
 // Format v2 keeps separate gate and up activation rows (2P rows).
@@ -1223,6 +1275,8 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had) {
   g.tiles = o; o += al(max_tiles(T, E, top_k) * 16);
   g.tiles_s = o; o += al((size_t)E * 16);
   g.ntiles = o; o += al(16);
+  g.counts = o; o += al(12 * 4);  // mixed widths: list lengths
+  g.lists = o; o += al((size_t)18 * (max_tiles(T, E, top_k) + E) * 4);
   g.total = o;
   return g;
 }
@@ -1250,6 +1304,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   int32_t* tiles = reinterpret_cast<int32_t*>(base + g.tiles);
   int32_t* tiles_s = reinterpret_cast<int32_t*>(base + g.tiles_s);
   int32_t* ntiles = reinterpret_cast<int32_t*>(base + g.ntiles);
+  int32_t* lcounts = reinterpret_cast<int32_t*>(base + g.counts);
+  int32_t* lists = reinterpret_cast<int32_t*>(base + g.lists);
   *r_out = r;
   const int P = T * top_k;
   const int mt = (int)max_tiles(T, L.E, top_k);
@@ -1266,6 +1322,37 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
                         (const int32_t*)rb.seg_offsets, (int)small_ok, tiles, tiles_s, ntiles)) !=
       cudaSuccess)
     return err;
+  if (L.mixed) {
+    if ((err = cudaMemsetAsync(lcounts, 0, 12 * sizeof(int32_t), st)) != cudaSuccess) return err;
+    const int threads = 3 * (mt + L.E);
+    err = launch_pdl(gemm_width_lists_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0,
+                     st, (const int32_t*)ntiles, (const int32_t*)tiles, (const int32_t*)tiles_s,
+                     L.d_kt, mt, L.E, lcounts, lists);
+    note_launches(1);
+    if (err != cudaSuccess) return err;
+  }
+  // one launch of a kernel, or (mixed widths) one per width over its list;
+  // kind 0 = big tiles, 1 = small tiles; launch 0 = gate/up, 1 = down
+  auto run = [&](int kind, int launch, const CUtensorMap& tm, const GemmParams& gp, int grid,
+                 int K) -> cudaError_t {
+    auto one = [&](int k, const GemmParams& q) {
+      return kind ? dispatch_gemm64(k, L.fp8, tm, q, grid, st) : dispatch_gemm(k, L.fp8, tm, q, grid, st);
+    };
+    if (!L.mixed) return one(K, gp);
+    const size_t n = kind ? (size_t)L.E : (size_t)mt;
+    const size_t seg = kind ? (size_t)9 * mt + (launch ? (size_t)6 * L.E : 0)
+                            : (launch ? (size_t)6 * mt : 0);
+    const size_t cap = launch ? n : 2 * n;
+    for (int w = 0; w < 3; w++) {
+      GemmParams q = gp;
+      q.entries = lists + (seg + (size_t)w * cap) * 2;
+      q.n_entries = lcounts + kind * 6 + launch * 3 + w;
+      q.off = L.d_off;
+      const cudaError_t e2 = one(w + 2, q);
+      if (e2 != cudaSuccess) return e2;
+    }
+    return cudaSuccess;
+  };
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
   if (L.had)
     err = launch_pdl(gather_rows_had_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x,
@@ -1289,16 +1376,15 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.cluster = cluster_for(L.I / 128);
   gu.had = L.had;
   gu.xrow_off = L.had ? P : 0;
-  // gate and up share one launch, so they share a width (checked at create)
-  if ((err = dispatch_gemm(L.K[0], L.fp8, tm_x, gu, mt * 2 * (L.I / 128), st)) != cudaSuccess)
-    return err;
+  gu.proj0 = 0;
+  // without mixed widths gate and up share a width (one launch)
+  if ((err = run(0, 0, tm_x, gu, mt * 2 * (L.I / 128), L.K[0])) != cudaSuccess) return err;
   if (small_ok) {
     GemmParams gs = gu;
     gs.tiles = tiles_s;
     gs.n_tiles = ntiles + 1;
     gs.cluster = cluster_for(L.I / kSN);
-    if ((err = dispatch_gemm64(L.K[0], L.fp8, tm_x, gs, L.E * 2 * (L.I / kSN), st)) != cudaSuccess)
-      return err;
+    if ((err = run(1, 0, tm_x, gs, L.E * 2 * (L.I / kSN), L.K[0])) != cudaSuccess) return err;
   }
   rec(3);
 
@@ -1317,13 +1403,14 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
   dn.cluster = cluster_for(L.H / 128);
   dn.had = L.had;
-  err = dispatch_gemm(L.K[2], L.fp8, tm_h, dn, mt * (L.H / 128), st);
+  dn.proj0 = 2;
+  err = run(0, 1, tm_h, dn, mt * (L.H / 128), L.K[2]);
   if (err == cudaSuccess && small_ok) {
     GemmParams ds = dn;
     ds.tiles = tiles_s;
     ds.n_tiles = ntiles + 1;
     ds.cluster = cluster_for(L.H / kSN);
-    err = dispatch_gemm64(L.K[2], L.fp8, tm_h, ds, L.E * (L.H / kSN), st);
+    err = run(1, 1, tm_h, ds, L.E * (L.H / kSN), L.K[2]);
   }
   rec(5);
   return err;

@@ -366,7 +366,36 @@ struct GemvParams {
   size_t n_pos;            // positions = pairs
   int32_t* work;           // item counter, zero on entry
   int nsplit;
+  // mixed widths: this launch's work list of (group, projection) pairs whose
+  // width is this instantiation's K, and the experts' code offsets
+  const int32_t* entries;  // [n][2], or null: every group, every projection
+  const int32_t* n_entries;
+  const unsigned long long* off;  // [E][3] code word offsets, or null: stride * e
+  int proj0;               // global index of this launch's projection 0 (0 or 2)
 };
+
+// Mixed widths: split the token groups' (group, projection) work into one
+// list per width.  Thread per (group, projection p of 3): gate and up go to
+// the gate/up launch's lists, down to the down launch's.  The order inside a
+// list does not matter (every item writes its own rows).
+__global__ void __launch_bounds__(256) width_lists_kernel(const int32_t* __restrict__ n_groups,
+                                                          const int32_t* __restrict__ groups,
+                                                          const int32_t* __restrict__ kt,
+                                                          int cap_gu, int cap_d,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ entries) {
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 3 * n_groups[0]) return;
+  const int g = i / 3, pg = i % 3;
+  const int w = kt[(size_t)groups[4 * g] * 3 + pg] - 2;
+  const int launch = pg == 2 ? 1 : 0;
+  const int cap = launch ? cap_d : cap_gu;
+  const int slot = atomicAdd(&counts[launch * 3 + w], 1);
+  int32_t* e = entries + ((size_t)launch * 3 * cap_gu + (size_t)w * cap + slot) * 2;
+  e[0] = g;
+  e[1] = launch ? 0 : pg;
+}
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
@@ -395,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   const int strips = p.out / 128;
   const int nblk = p.in / 16;
   const int bps = nblk / p.nsplit;   // blocks (jobs) per item, >= kStages - 1
-  const int n_items = p.n_groups[0] * p.nproj * p.nsplit * strips;
+  const int n_items = (p.entries ? p.n_entries[0] : p.n_groups[0] * p.nproj) * p.nsplit * strips;
   const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
 
   // item id -> (group, projection, split, strip); consecutive ids are
@@ -405,8 +434,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
     int r = it / strips;
     q = r % p.nsplit;
     r /= p.nsplit;
-    pj = r % p.nproj;
-    g = r / p.nproj;
+    if (p.entries) {
+      g = p.entries[2 * r];
+      pj = p.entries[2 * r + 1];
+    } else {
+      pj = r % p.nproj;
+      g = r / p.nproj;
+    }
+  };
+  // first code word of projection pj of expert e
+  auto expert_codes = [&](int e, int pj) {
+    return (pj ? p.codes[1] : p.codes[0]) +
+           (p.off ? (size_t)p.off[(size_t)e * 3 + p.proj0 + pj]
+                  : (pj ? p.stride[1] : p.stride[0]) * (size_t)e);
   };
   // Producer cursor: the source addresses of the next block to copy.
   struct Cursor {
@@ -420,9 +460,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
     const int e = p.groups[4 * g];
     const int blk = q * bps;
     cur.b = 0;
-    cur.cs = reinterpret_cast<const uint8_t*>((pj ? p.codes[1] : p.codes[0]) +
-                                              (pj ? p.stride[1] : p.stride[0]) * e) +
-             (size_t)blk * row_bytes + (size_t)8 * s * 32 * K;
+    cur.cs = reinterpret_cast<const uint8_t*>(expert_codes(e, pj)) + (size_t)blk * row_bytes +
+             (size_t)8 * s * 32 * K;
     // lane l copies 16 bytes of token slot l / 4; slots the group does not
     // fill are left alone (their MMA columns are discarded)
     cur.xsrc = (lane >> 2) < p.groups[4 * g + 2]
@@ -625,7 +664,7 @@ int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct GemvLayout {
-  size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, counters, total;
+  size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, counters, entries, total;
   int ns_gu, ns_d;
 };
 
@@ -642,7 +681,8 @@ GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
   g.xs_d = o; o += al(G * (I / 16) * kXsChunk);
   g.xs_d_inv = o; o += al(P * 4);
   g.r = o; o += al((size_t)g.ns_d * P * H * 4);
-  g.counters = o; o += al(2 * 4);
+  g.counters = o; o += al(12 * 4);  // 6 item counters, 6 list lengths
+  g.entries = o; o += al(3 * G * 3 * 2 * 4);  // lists of (group, projection) for mixed widths
   g.total = o;
   return g;
 }
@@ -663,6 +703,8 @@ void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb
   gb->xs_d_inv = reinterpret_cast<float*>(q + g.xs_d_inv);
   gb->r = reinterpret_cast<float*>(q + g.r);
   gb->counters = reinterpret_cast<int32_t*>(q + g.counters);
+  gb->n_entries = gb->counters + 6;
+  gb->entries = reinterpret_cast<int32_t*>(q + g.entries);
   gb->ns_gu = g.ns_gu;
   gb->ns_d = g.ns_d;
 }
@@ -676,7 +718,15 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   const int P = T * top_k;
   const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
-  if ((err = cudaMemsetAsync(gb.counters, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(gb.counters, 0, 12 * sizeof(int32_t), st)) != cudaSuccess) return err;
+  if (L.mixed) {
+    const int threads = (int)(3 * G);
+    err = launch_pdl(width_lists_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st,
+                     (const int32_t*)(rb.group_off + L.E), (const int32_t*)rb.groups, L.d_kt,
+                     (int)(2 * G), (int)G, gb.n_entries, gb.entries);
+    note_launches(1);
+    if (err != cudaSuccess) return err;
+  }
   err = launch_pdl(gather_xs_kernel, dim3(P), dim3(L.H / 16 < 256 ? L.H / 16 : 256), 0, st, x,
                    x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, gb.xs_gu, gb.xs_gu_inv);
   note_launches(1);
@@ -692,10 +742,21 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   gu.xs = gb.xs_gu; gu.xs_inv = gb.xs_gu_inv;
   gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
   gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.gu_out = gb.gu; gu.n_pos = (size_t)P;
-  gu.work = gb.counters; gu.nsplit = gb.ns_gu;
-  if ((err = dispatch_gemv(L.K[0], L.fp8, L.had, gu, (int)(G * 2 * (L.I / 128) * gu.nsplit), st)) !=
-      cudaSuccess)
-    return err;
+  gu.work = gb.counters; gu.nsplit = gb.ns_gu; gu.proj0 = 0;
+  const int ub_gu = (int)(G * 2 * (L.I / 128) * gu.nsplit);
+  if (!L.mixed) {
+    if ((err = dispatch_gemv(L.K[0], L.fp8, L.had, gu, ub_gu, st)) != cudaSuccess) return err;
+  } else {
+    // one launch per width over its list (an empty list ends at once)
+    gu.off = L.d_off;
+    for (int w = 0; w < 3; w++) {
+      GemvParams gw = gu;
+      gw.entries = gb.entries + (size_t)w * 2 * G * 2;
+      gw.n_entries = gb.n_entries + w;
+      gw.work = gb.counters + w;
+      if ((err = dispatch_gemv(w + 2, L.fp8, L.had, gw, ub_gu, st)) != cudaSuccess) return err;
+    }
+  }
   rec(3);
 
   err = launch_pdl(prep_down_kernel, dim3(P), dim3(L.I / 16 < 256 ? L.I / 16 : 256), 0, st, gb.gu,
@@ -711,8 +772,20 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   dn.xs = gb.xs_d; dn.xs_inv = gb.xs_d_inv;
   dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r; dn.n_pos = (size_t)P;
-  dn.work = gb.counters + 1; dn.nsplit = gb.ns_d;
-  err = dispatch_gemv(L.K[2], L.fp8, L.had, dn, (int)(G * (L.H / 128) * dn.nsplit), st);
+  dn.work = gb.counters + 3; dn.nsplit = gb.ns_d; dn.proj0 = 2;
+  const int ub_d = (int)(G * (L.H / 128) * dn.nsplit);
+  if (!L.mixed) {
+    err = dispatch_gemv(L.K[2], L.fp8, L.had, dn, ub_d, st);
+  } else {
+    dn.off = L.d_off;
+    for (int w = 0; w < 3 && err == cudaSuccess; w++) {
+      GemvParams gw = dn;
+      gw.entries = gb.entries + ((size_t)3 * 2 * G + (size_t)w * G) * 2;
+      gw.n_entries = gb.n_entries + 3 + w;
+      gw.work = gb.counters + 3 + w;
+      err = dispatch_gemv(w + 2, L.fp8, L.had, gw, ub_d, st);
+    }
+  }
   rec(5);
   return err;
 }

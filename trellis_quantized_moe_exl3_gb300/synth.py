@@ -24,6 +24,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 TAG_CODES, TAG_SIDE, TAG_ACT, TAG_LOGITS, TAG_BIAS, TAG_PERM, TAG_GUMBEL, TAG_SHARED = range(1, 9)
+TAG_WIDTHS = 9
 
 
 def _rng(*key) -> np.random.Generator:
@@ -41,6 +42,7 @@ class LayerSpec:
     shared: bool = False
     hadamard: bool = False  # format v2 (rotation on both sides); no effect on the draws
     shared_coded: bool = False  # one more coded expert (the shared one) after the routed ones
+    expert_K: tuple | None = None  # per expert (gate, up, down) widths; codes then flat
 
     @property
     def n_coded(self) -> int:
@@ -51,9 +53,12 @@ class LayerSpec:
         """(in_features, out_features) of projection 0=gate, 1=up, 2=down."""
         return (self.inter, self.hidden) if proj == 2 else (self.hidden, self.inter)
 
-    def code_words_per_expert(self, proj: int) -> int:
+    def width(self, proj: int, expert: int) -> int:
+        return self.expert_K[expert][proj] if self.expert_K else self.K[proj]
+
+    def code_words_per_expert(self, proj: int, expert: int = 0) -> int:
         i, o = self.dims(proj)
-        return (i // 16) * (o // 16) * 16 * self.K[proj]
+        return (i // 16) * (o // 16) * 16 * self.width(proj, expert)
 
 
 @dataclass(frozen=True)
@@ -93,13 +98,23 @@ WORKLOADS = {
 def expert_codes(spec: LayerSpec, proj: int, expert: int) -> np.ndarray:
     """Uniform-random uint16 code words [in/16][out/16][16K] of one expert."""
     i, o = spec.dims(proj)
-    n = spec.code_words_per_expert(proj)
+    n = spec.code_words_per_expert(proj, expert)
     a = _rng(spec.seed, TAG_CODES, proj, expert).integers(0, 65536, size=n, dtype=np.uint16)
-    return a.reshape(i // 16, o // 16, 16 * spec.K[proj])
+    return a.reshape(i // 16, o // 16, 16 * spec.width(proj, expert))
+
+
+def mixed_widths(seed: int, n: int, choices=(3, 4)) -> tuple:
+    """A width per expert and projection, drawn uniformly from `choices`
+    (the 3.5 bpw mixed recipe: every routed tensor K3 or K4)."""
+    w = _rng(seed, TAG_WIDTHS).choice(np.asarray(choices), size=(n, 3))
+    return tuple(tuple(int(v) for v in row) for row in w)
 
 
 def layer_codes(spec: LayerSpec, proj: int, out: np.ndarray | None = None) -> np.ndarray:
-    """Code words of every expert, [E][in/16][out/16][16K]."""
+    """Code words of every expert, [E][in/16][out/16][16K]; with per-expert
+    widths a flat array of the experts' codes back to back."""
+    if spec.expert_K:
+        return np.concatenate([expert_codes(spec, proj, e).reshape(-1) for e in range(spec.n_coded)])
     i, o = spec.dims(proj)
     shape = (spec.n_coded, i // 16, o // 16, 16 * spec.K[proj])
     if out is None:
