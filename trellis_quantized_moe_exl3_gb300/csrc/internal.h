@@ -105,6 +105,7 @@ struct LayerView {
   const unsigned long long* d_off; // device [E][3] code word offsets
   const uint8_t* h_kt;             // host copies of both
   const size_t* h_off;
+  int wmask[2];                    // widths present (bit K - 2): [0] gate/up, [1] down
 };
 
 // Width of projection p of expert e and the word offset of its codes.

@@ -161,6 +161,7 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
           const int k = d->expert_K ? d->expert_K[(size_t)e * 3 + p] : d->K[p];
           const size_t in = p == 2 ? v.I : v.H, outf = p == 2 ? v.H : v.I;
           L->h_kt[(size_t)e * 3 + p] = (uint8_t)k;
+          v.wmask[p == 2 ? 1 : 0] |= 1 << (k - 2);
           kt32[(size_t)e * 3 + p] = k;
           L->h_off[(size_t)e * 3 + p] = run[p];
           off64[(size_t)e * 3 + p] = run[p];

@@ -1344,6 +1344,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
                             : (launch ? (size_t)6 * mt : 0);
     const size_t cap = launch ? n : 2 * n;
     for (int w = 0; w < 3; w++) {
+      if (!((L.wmask[launch] >> w) & 1)) continue;  // no expert has this width
       GemmParams q = gp;
       q.entries = lists + (seg + (size_t)w * cap) * 2;
       q.n_entries = lcounts + kind * 6 + launch * 3 + w;

@@ -750,6 +750,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     // one launch per width over its list (an empty list ends at once)
     gu.off = L.d_off;
     for (int w = 0; w < 3; w++) {
+      if (!((L.wmask[0] >> w) & 1)) continue;  // no expert has this width
       GemvParams gw = gu;
       gw.entries = gb.entries + (size_t)w * 2 * G * 2;
       gw.n_entries = gb.n_entries + w;
@@ -779,6 +780,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   } else {
     dn.off = L.d_off;
     for (int w = 0; w < 3 && err == cudaSuccess; w++) {
+      if (!((L.wmask[1] >> w) & 1)) continue;
       GemvParams gw = dn;
       gw.entries = gb.entries + ((size_t)3 * 2 * G + (size_t)w * G) * 2;
       gw.n_entries = gb.n_entries + 3 + w;
