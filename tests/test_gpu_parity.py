@@ -285,6 +285,22 @@ def test_forward_shared_coded(E, H, I, K, fp8, had, T, k, routing, path):
     assert device_status(layer.workspace(T, k)) == 0
 
 
+# ------------------------------------------------------------------ edge shapes
+
+
+@pytest.mark.parametrize("E,H,I,K,had,T,k", [
+    (1, 128, 128, (2, 2, 2), False, 5, 1),     # one expert, the smallest dimensions
+    (6, 256, 128, (3, 3, 4), False, 10, 6),    # top_k = E: every expert for every token
+    (4, 128, 128, (4, 4, 3), True, 7, 2),      # format v2 on single 128-blocks
+])
+@pytest.mark.parametrize("path", [1, 2], ids=["gemv", "gemm"])
+def test_forward_edge_shapes(E, H, I, K, had, T, k, path):
+    spec = synth.LayerSpec(seed=150 + E + k, num_experts=E, hidden=H, inter=I, K=K, hadamard=had)
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=path)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
 # ------------------------------------------------------------------ mixed widths
 
 

@@ -91,7 +91,8 @@ __device__ __forceinline__ void group_of(const int32_t* seg_offsets, const int32
   *slot = l % kGroup;
 }
 
-// Both input passes below give each thread one 16-input block per step
+// Both input passes below (launched with input_pass_threads: whole warps,
+// blockDim a multiple of 8) give each thread one 16-input block per step
 // (16-byte loads of x / suh, float4 loads of fp32 rows), keep its first block
 // in registers between the max pass and the write pass (re-reading any
 // further ones), and write the block's 16 token-slot values as four 16-byte
@@ -663,6 +664,15 @@ int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
 
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// Threads of an input pass over n inputs: one per 16-input block, at most
+// 256, and at least one full warp (block_max reduces whole warps; blocks
+// beyond n/16 idle).  n/16 is a multiple of 8, so every 8-thread rotation
+// group is entirely inside or outside the blocks.
+int input_pass_threads(int n) {
+  const int b = n / 16;
+  return b < 32 ? 32 : (b > 256 ? 256 : b);
+}
+
 struct GemvLayout {
   size_t xs_gu, xs_gu_inv, gu, xs_d, xs_d_inv, r, counters, entries, total;
   int ns_gu, ns_d;
@@ -727,7 +737,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     note_launches(1);
     if (err != cudaSuccess) return err;
   }
-  err = launch_pdl(gather_xs_kernel, dim3(P), dim3(L.H / 16 < 256 ? L.H / 16 : 256), 0, st, x,
+  err = launch_pdl(gather_xs_kernel, dim3(P), dim3(input_pass_threads(L.H)), 0, st, x,
                    x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, gb.xs_gu, gb.xs_gu_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
@@ -760,7 +770,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   }
   rec(3);
 
-  err = launch_pdl(prep_down_kernel, dim3(P), dim3(L.I / 16 < 256 ? L.I / 16 : 256), 0, st, gb.gu,
+  err = launch_pdl(prep_down_kernel, dim3(P), dim3(input_pass_threads(L.I)), 0, st, gb.gu,
                    gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
