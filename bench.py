@@ -86,30 +86,37 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: flo
     return world * tokens_per_step * steps / (total_ms / 1e3)
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
-# the decode step's expert kernels, from one ncu capture summarised in
-# profiles/gemv_kernel_K2_decode.md; reported only while the kernel sources
-# hash to what was captured (otherwise null).
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant stage's launches in one step, from ncu captures summarised under
+# profiles/ (decode: gemv_kernel_K2_decode.md; prefill: the big- and
+# small-tile kernels of the gate/up stage, prefill_gemm_dram.md); reported
+# only while the kernel sources hash to what was captured (otherwise null).
 NCU_TRAFFIC = {
     ("decode", "gate_up"): 128.092928e6 + 4.347136e6,
     ("decode", "down"): 63.688704e6 + 0.863232e6,
 }
 NCU_SOURCES = {
-    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "318b212751492c487eb9778e510184fe1d9beddb",
-    "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
+    "decode": {
+        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "318b212751492c487eb9778e510184fe1d9beddb",
+        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
+    },
+    "prefill": {},
 }
 
 
 def ncu_traffic(workload, kernel):
     import hashlib
-    for rel, digest in NCU_SOURCES.items():
+    srcs = NCU_SOURCES.get(workload)
+    if not srcs or (workload, kernel) not in NCU_TRAFFIC:
+        return None
+    for rel, digest in srcs.items():
         try:
             with open(os.path.join(ROOT, rel), "rb") as f:
                 if hashlib.sha1(f.read()).hexdigest() != digest:
                     return None
         except OSError:
             return None
-    return NCU_TRAFFIC.get((workload, kernel))
+    return NCU_TRAFFIC[(workload, kernel)]
 
 
 def peaks():
@@ -510,7 +517,8 @@ def run_ours(args):
     if gemm_path:
         tf = flops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_tf,
-                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": None,
+                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": ncu_traffic(wl.name, dom),
+                "traffic_unit": "bytes per step of the stage's launches (ncu)",
                 "algorithmic_flops": flops[dom], "ms": dom_ms,
                 "peak_source": f"{src} (bf16_tflops burst; the fp16 dense rate equals bf16)",
                 "alu_view": {"achieved": dec_rate / 1e9, "peak": peak_wps / 1e9,
