@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
         float a0[16];
         tmem_ld16(trow + c0, a0);
-        tmem_ld_wait();
+        tmem_ld_wait(a0);
         rotate_store_cols(xbuf, a0, q4, lane, 1 + cgrp, c0, cnt, svr, s_scale, s_pid, p, pj, pos0,
                           128 * s);
       }
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c0 = p.had ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
-      tmem_ld_wait();
+      tmem_ld_wait(a0);
 #pragma unroll
       for (int i = 0; i < 16; i++) {
         const int n = c0 + i;
@@ -723,7 +723,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int c = 0; c < 4; c++) {
         float a0[16];
         tmem_ld16(trow + 64 * cg + 16 * c, a0);
-        tmem_ld_wait();
+        tmem_ld_wait(a0);
 #pragma unroll
         for (int i = 0; i < 16; i++) xbuf[lane * 129 + 64 * hlf + 16 * c + i] = a0[i];
       }
@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int c0 = p.had ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
-      tmem_ld_wait();
+      tmem_ld_wait(a0);
       if (lane_live && n < cnt) {
         const uint4 sva = __ldg(reinterpret_cast<const uint4*>(svh + c0));
         const uint4 svb = __ldg(reinterpret_cast<const uint4*>(svh + c0 + 8));
