@@ -88,7 +88,7 @@ const char* exl3_status_string(exl3_status s) {
     case EXL3_OK: return "ok";
     case EXL3_ERR_ARG: return "invalid argument";
     case EXL3_ERR_SHAPE: return "invalid shape";
-    case EXL3_ERR_K: return "code width must be 2, 3 or 4 (gate and up equal)";
+    case EXL3_ERR_K: return "code width must be 2, 3 or 4";
     case EXL3_ERR_WORKSPACE: return "workspace missing or too small";
     case EXL3_ERR_CUDA: return "CUDA error";
     case EXL3_ERR_DEVICE: return "unsupported device or device status set";

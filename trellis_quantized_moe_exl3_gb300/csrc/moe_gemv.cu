@@ -743,7 +743,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   if (err != cudaSuccess) return err;
   rec(2);
 
-  // gate and up share one launch, so they share a width (checked at create)
+  // gate and up share one launch (one per width when the layer mixes widths)
   GemvParams gu{};
   gu.codes[0] = L.codes[0]; gu.codes[1] = L.codes[1];
   gu.stride[0] = L.code_stride[0]; gu.stride[1] = L.code_stride[1];
