@@ -92,20 +92,20 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: flo
 # small-tile kernels of the gate/up stage, prefill_gemm_dram.md); reported
 # only while the kernel sources hash to what was captured (otherwise null).
 NCU_TRAFFIC = {
-    ("decode", "gate_up"): 128.105472e6 + 4.872192e6,
-    ("prefill", "gate_up"): 4070311936,  # big-tile + small-tile launches
-    ("prefill", "down"): 2428143616,
-    ("decode", "down"): 63.691520e6 + 0.919808e6,
+    ("decode", "gate_up"): 128.116736e6 + 4.404480e6,
+    ("prefill", "gate_up"): 4072320512,  # big-tile + small-tile launches
+    ("prefill", "down"): 2429370624,
+    ("decode", "down"): 63.692288e6 + 0.870144e6,
 }
 NCU_SOURCES = {
     "decode": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "3c4d2aad7ee0890a402f53425b8f502f08717b97",
+        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "d195d448e473addceaac4a0d4c850cd1e9550ed8",
         "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
     },
     "prefill": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemm.cu": "729fd43af4607d11880a25834aaf91e8d697b05d",
+        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemm.cu": "6b460aa5a90cb5bd2a19b8ac321fa9d9eacfb102",
         "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
-        "trellis_quantized_moe_exl3_gb300/csrc/umma.cuh": "700a0580e2723b9d92b1231ff8c270db6f0e329f",
+        "trellis_quantized_moe_exl3_gb300/csrc/umma.cuh": "b447c8cca474276a478c6b77fc3e35111d3004a0",
         "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "90e55f7d8ddca6b4f57fedbba41ac44ecb974179",
     },
 }
