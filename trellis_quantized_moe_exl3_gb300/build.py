@@ -50,7 +50,9 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
         obj = os.path.join(OUT_DIR, os.path.basename(src).replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, src, headers):
-            jobs.append([nvcc, *ARCH, *flags, "-c", src, "-o", obj])
+            # compiled to a private name and renamed, so processes building at
+            # the same time (ranks of one job) never see a half-written object
+            jobs.append(([nvcc, *ARCH, *flags, "-c", src, "-o", obj + f".tmp{os.getpid()}"], obj))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,8 +60,14 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
         return r.stdout + r.stderr
 
+    def compile_one(job):
+        cmd, obj = job
+        out = run(cmd)
+        os.replace(cmd[-1], obj)
+        return out
+
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
-        for out in ex.map(run, jobs):
+        for out in ex.map(compile_one, jobs):
             if verbose and out.strip():
                 print(out)
     if force or jobs or not os.path.exists(LIB_PATH):
