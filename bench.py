@@ -546,7 +546,9 @@ def run_ours(args):
         "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 (MMA operands; fp32 accumulate; bf16 activations in/out)",
+        "dtype": "f16",
+        "arithmetic": "integer trellis decode; fp16 MMA operands, fp32 accumulate; "
+                      "bf16 activations in and out",
         "data": "synthetic (seeded PCG64): uniform uint16 codes, side vectors 1+0.1N(0,1), "
                 "N(0,1) activations and router logits",
         "config": {**workload_config(wl), "cuda_graph": use_graph, "n_active_experts": n_active,
