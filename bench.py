@@ -567,7 +567,9 @@ def run_ours(args):
         "clocks": clk,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
-        rate, secs, sample = oracle_pair_rate(wl, spec, x_np, lg_np, 3, shared_w=sw, codes=codes)
+        # one whole token: its top_k (token, expert) pairs (+ its shared expert)
+        rate, secs, sample = oracle_pair_rate(wl, spec, x_np, lg_np, wl.top_k, shared_w=sw,
+                                              codes=codes)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": sample, "seconds": secs}
     if rank == 0:
