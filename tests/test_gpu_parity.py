@@ -301,6 +301,16 @@ def test_forward_edge_shapes(E, H, I, K, had, T, k, path):
     assert device_status(layer.workspace(T, k)) == 0
 
 
+@pytest.mark.parametrize("path", [1, 2], ids=["gemv", "gemm"])
+def test_forward_max_experts_and_top_k(path):
+    """The largest expert count (1024: 32 logits per lane in the top-k, a
+    thread per expert in the table scans) with the largest top_k (16)."""
+    spec = synth.LayerSpec(seed=160, num_experts=1024, hidden=128, inter=128, K=(2, 2, 3))
+    out, ref, layer = _run_small(spec, 40, 16, "bf16", path=path)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(40, 16)) == 0
+
+
 # ------------------------------------------------------------------ mixed widths
 
 
