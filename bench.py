@@ -86,6 +86,38 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: flo
     return world * tokens_per_step * steps / (total_ms / 1e3)
 
 
+# Issue-slot peak of the trellis decode (weights/s): 128 lane-instructions per
+# SM and clock, 152 SMs, 2070 MHz maximum clock; K = 2 and 4 need 4 integer
+# instructions per weight (window, multiply, correction, mask-xor: two on the
+# ALU pipe, two on the FMA pipe), K = 3 needs 3 on the 64-lane ALU pipe
+# (window, mask, mask-xor) besides the multiply.
+DECODE_PEAK = {kk: 152 * 2.070e9 * (128 / 4 if kk in (2, 4) else 64 / 3) for kk in (2, 3, 4)}
+
+
+def expert_work(spec, counts, per: int):
+    """Algorithmic work of the two expert stages ("gate_up", "down") of one
+    step: weight decodes (every active expert's weights once per unit of
+    `per` tokens: a GEMV token group or a tensor-core tile), the same divided
+    by the decode peak of each expert's width (seconds at peak), and code +
+    side-vector bytes of the active experts.  counts: tokens per expert."""
+    H, I = spec.hidden, spec.inter
+    side_b = (H + I) * 2
+    dec_w = {"gate_up": 0, "down": 0}
+    dec_t = {"gate_up": 0.0, "down": 0.0}
+    code_bytes = {"gate_up": 0, "down": 0}
+    for e, c in enumerate(counts):
+        if c <= 0:
+            continue
+        u = (int(c) + per - 1) // per
+        for pr in range(3):
+            st = "down" if pr == 2 else "gate_up"
+            kk = spec.width(pr, e)
+            dec_w[st] += u * H * I
+            dec_t[st] += u * H * I / DECODE_PEAK[kk]
+            code_bytes[st] += H * I * kk // 8 + side_b
+    return dec_w, dec_t, code_bytes
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # dominant stage's launches in one step, from ncu captures summarised under
 # profiles/ (decode: gemv_kernel_K2_decode.md; prefill: the big- and
@@ -488,33 +520,10 @@ def run_ours(args):
     # roofline of the dominant expert kernel (the larger of gate/up and down)
     hbm, bf16_tf, src = peaks()
     H, I = spec.hidden, spec.inter
-    side_b = (H + I) * 2
     stage_names = _lib.STAGE_NAMES
     P = T * (k + int(spec.shared_coded))          # pairs, the coded shared expert's included
     gemm_path = P >= 16 * spec.n_coded
-    # issue-slot peak of the trellis decode: 128 lane-instructions per SM and
-    # clock, 152 SMs, 2070 MHz maximum clock; K = 2 and 4 need 4 integer
-    # instructions per weight (window, multiply, correction, mask-xor: two on
-    # the ALU pipe, two on the FMA pipe), K = 3 needs 3 on the 64-lane ALU pipe
-    # (window, mask, mask-xor) besides the multiply
-    sms, clk_hz = 152, 2.070e9
-    peak_k = {kk: sms * clk_hz * (128 / 4 if kk in (2, 4) else 64 / 3) for kk in (2, 3, 4)}
-    # weight decodes: every expert's weights once per token group (GEMV: <= 8
-    # tokens) or token tile (GEMM: <= 512 tokens), at the expert's width
-    per = 512 if gemm_path else 8
-    dec_w = {"gate_up": 0, "down": 0}
-    dec_t = {"gate_up": 0.0, "down": 0.0}   # decodes / peak of their width: seconds at peak
-    code_bytes = {"gate_up": 0, "down": 0}
-    for e, c in enumerate(counts):
-        if c <= 0:
-            continue
-        u = (int(c) + per - 1) // per
-        for pr in range(3):
-            st_name = "down" if pr == 2 else "gate_up"
-            kk = spec.width(pr, e)
-            dec_w[st_name] += u * H * I
-            dec_t[st_name] += u * H * I / peak_k[kk]
-            code_bytes[st_name] += H * I * kk // 8 + side_b
+    dec_w, dec_t, code_bytes = expert_work(spec, counts, 512 if gemm_path else 8)
     flops = {"gate_up": 2.0 * P * H * I * 2, "down": 2.0 * P * H * I}
     dom = max(("gate_up", "down"), key=lambda n: stage_ms[stage_names.index(n)])
     dom_ms = float(stage_ms[stage_names.index(dom)])

@@ -49,3 +49,27 @@ def test_job_throughput_counts_every_rank():
     # 2 ranks x 4 tokens x 10 steps in 5 ms = 16,000 tokens/s
     assert bench.job_tokens_per_s(2, 4, 10, 5.0) == pytest.approx(16000.0)
     assert bench.max_over_ranks(3.0, torch.device("cpu"), 1) == 3.0
+
+
+def test_expert_work_accounting():
+    """The bench's algorithmic work of the expert stages: decodes once per
+    unit of tokens, code bytes at each expert's width, and the decode peak of
+    a mixed-width stage weighted by its decodes."""
+    import dataclasses
+
+    import bench
+    from trellis_quantized_moe_exl3_gb300 import synth
+    spec = synth.LayerSpec(seed=0, num_experts=3, hidden=256, inter=128, K=(2, 2, 4))
+    counts = [0, 9, 8]  # expert 1: two groups of <= 8 tokens; expert 2: one
+    dec_w, dec_t, code_b = bench.expert_work(spec, counts, 8)
+    H, I = 256, 128
+    assert dec_w == {"gate_up": 3 * 2 * H * I, "down": 3 * H * I}
+    assert code_b == {"gate_up": 2 * (2 * H * I * 2 // 8 + 2 * (H + I) * 2),
+                      "down": 2 * (H * I * 4 // 8 + (H + I) * 2)}
+    assert abs(dec_w["gate_up"] / dec_t["gate_up"] - bench.DECODE_PEAK[2]) < 1e-3
+    mixed = dataclasses.replace(spec, expert_K=((3, 3, 3), (3, 4, 2), (4, 4, 4)))
+    dec_w, dec_t, code_b = bench.expert_work(mixed, counts, 8)
+    # expert 1 (2 units) gate K3 + up K4, expert 2 (1 unit) gate and up K4
+    want_t = H * I * (2 / bench.DECODE_PEAK[3] + 2 / bench.DECODE_PEAK[4] + 2 / bench.DECODE_PEAK[4])
+    assert abs(dec_t["gate_up"] - want_t) < 1e-15
+    assert code_b["down"] == H * I * 2 // 8 + H * I * 4 // 8 + 2 * (H + I) * 2
