@@ -67,7 +67,9 @@ class Layer:
         if expert_K is not None:
             import numpy as np
             self._ek = np.ascontiguousarray(np.asarray(expert_K, dtype=np.uint8))
-            assert self._ek.shape == (E + int(bool(shared_coded)), 3)
+            if self._ek.shape != (E + int(bool(shared_coded)), 3):
+                raise ValueError(f"expert_K must be [{E + int(bool(shared_coded))}][3], "
+                                 f"not {list(self._ek.shape)}")
         self._keep = [*codes, *suh, *svh] + (list(shared) if shared is not None else [])
         for t in self._keep:
             _req(t, "layer tensor")
