@@ -390,6 +390,24 @@ def test_prefill_workload_sampled():
     _workload_parity("prefill", _prefill_tokens)
 
 
+def test_large_T_sampled():
+    """131,072 tokens (1,048,576 pairs; the pages report their fused MoE
+    failing at 98,304): workspace sizing and 64-bit indexing on the
+    tensor-core path, sampled parity at both ends and the middle."""
+    T, k = 131072, 8
+    spec = synth.LayerSpec(seed=170, K=(2, 2, 2))
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x = synth.activations(171, T, spec.hidden, "bf16")
+    logits = synth.router_logits(171, T, spec.num_experts, "zipf")
+    out = layer.forward(_act(x, "bf16"), torch.from_numpy(logits).cuda(), k)
+    torch.cuda.synchronize()
+    assert device_status(layer.workspace(T, k)) == 0
+    toks = [0, T // 2, T - 1]
+    ref = oracle_forward_parallel(hl.oracle(), x, True, logits, k, toks)
+    assert_layer_close(act_to_f64(out)[toks], ref)
+
+
 def test_decode_workload_hadamard_all_tokens():
     """The decode workload's layer in format v2 (GEMV path, full size)."""
     _workload_parity("decode", lambda wl, lg: list(range(wl.T)), hadamard=True)
