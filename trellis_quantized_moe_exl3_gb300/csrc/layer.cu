@@ -259,6 +259,8 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (!x || !logits || !out) return EXL3_ERR_ARG;
   if (!aligned16(x) || !aligned16(out) || (residual && !aligned16(residual))) return EXL3_ERR_ARG;
   if (x == out) return EXL3_ERR_ARG;
+  // the dense shared expert's gate/up launch has a grid z of 2 * ceil(T / 8)
+  if (layer->has_shared && (size_t)T > (size_t)8 * (65535 / 2)) return EXL3_ERR_SHAPE;
   const FwdLayout f = fwd_layout(L, layer->has_shared, T, top_k);
   if (!ws) return EXL3_ERR_WORKSPACE;
   if (ws_bytes < f.total) return EXL3_ERR_WORKSPACE;
