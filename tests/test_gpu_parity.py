@@ -470,3 +470,45 @@ def test_long_workload_sampled():
         torch.cuda.empty_cache()
     assert_layer_close(act_to_f64(xt)[toks], oracle.bf16_bits_to_f64(x_chain), max_rel=4 * 2e-2,
                        fro_rel=4 * 5e-3)
+
+
+def test_forward_argument_errors_leave_output():
+    """Argument errors of exl3_moe_forward_ex return their status before any
+    launch and leave the output untouched."""
+    import ctypes
+
+    from trellis_quantized_moe_exl3_gb300 import _lib
+    spec = synth.LayerSpec(seed=180, num_experts=6, hidden=256, inter=128, K=(2, 2, 2))
+    hl = HostLayer(spec)
+    layer = hl.device()
+    T, k = 8, 2
+    x = _act(synth.activations(181, T, spec.hidden, "bf16"), "bf16")
+    lg = torch.from_numpy(synth.router_logits(181, T, spec.num_experts, "normal")).cuda()
+    out = torch.full_like(x, 7.0)
+    n = layer.workspace_size(T, k)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    L = _lib.lib()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    bf = _lib.EXL3_BF16
+
+    def call(x_=None, dt=bf, T_=T, k_=k, out_=None, path=0, ws_=ws, nbytes=n):
+        xp = x_ if x_ is not None else p(x)
+        op = out_ if out_ is not None else p(out)
+        wp = p(ws_) if ws_ is not None else None
+        return L.exl3_moe_forward_ex(layer.handle, xp, dt, p(lg), T_, k_, None, op, path, wp,
+                                     nbytes, None)
+
+    assert call(dt=7) == _lib.EXL3_ERR_ARG
+    assert call(path=3) == _lib.EXL3_ERR_ARG
+    assert call(T_=-1) == _lib.EXL3_ERR_SHAPE
+    assert call(k_=0) == _lib.EXL3_ERR_ARG
+    assert call(k_=spec.num_experts + 1) == _lib.EXL3_ERR_ARG
+    assert call(out_=p(x)) == _lib.EXL3_ERR_ARG                       # out aliases x
+    assert call(x_=ctypes.c_void_p(x.data_ptr() + 2)) == _lib.EXL3_ERR_ARG  # misaligned
+    assert call(ws_=None) == _lib.EXL3_ERR_WORKSPACE
+    assert call(nbytes=n - 1) == _lib.EXL3_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    assert call() == 0
+    torch.cuda.synchronize()
+    assert not bool((out == 7.0).all())
