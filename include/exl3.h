@@ -191,7 +191,9 @@ exl3_status exl3_moe_forward(const exl3_layer_t *layer, const void *x, exl3_dtyp
 /* As exl3_moe_forward, plus an optional residual (device [T][H] in dt, may
  * be NULL; out = round(residual + y)) and an explicit kernel path.
  * Both return EXL3_ERR_SHAPE for T > 262,136 on a layer with a dense shared
- * expert (its launches cover 8 tokens per grid slice). */
+ * expert (its launches cover 8 tokens per grid slice), and for more than 2^29
+ * (token, expert) pairs (2^26 on the decode-sized GEMV path; exl3_moe_route
+ * takes 2^29 too). */
 exl3_status exl3_moe_forward_ex(const exl3_layer_t *layer, const void *x, exl3_dtype dt,
                                 const float *logits, int T, int top_k, const void *residual,
                                 void *out, int path, void *ws, size_t ws_bytes, void *stream);

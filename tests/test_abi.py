@@ -107,6 +107,8 @@ def test_route_validation_and_sizes(L):
                             None) == _lib.EXL3_ERR_SHAPE
     assert L.exl3_moe_route(dummy, 4, 2000, 8, dummy, dummy, dummy, dummy, dummy, 1 << 20,
                             None) == _lib.EXL3_ERR_SHAPE
+    assert L.exl3_moe_route(dummy, 1 << 27, 288, 8, dummy, dummy, dummy, dummy, dummy, 1 << 20,
+                            None) == _lib.EXL3_ERR_SHAPE              # 2^30 pairs > 2^29
     assert L.exl3_moe_route(dummy, 4, 288, 8, dummy, dummy, dummy, dummy, None, 1 << 20,
                             None) == _lib.EXL3_ERR_WORKSPACE
     assert L.exl3_moe_route(dummy, 4, 288, 8, dummy, dummy, dummy, dummy, dummy, 16,

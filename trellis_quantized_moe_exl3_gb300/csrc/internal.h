@@ -44,6 +44,11 @@ constexpr int kRouteChunk = 128;   // tokens per routing CTA
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kGroup = 8;          // tokens per GEMV token group (MMA N)
+// Pairs (tokens x top_k) a call may hold: positions and TMA row coordinates
+// are 32-bit (the GEMM path addresses 2 x pairs rows); the GEMV path forms
+// split x projection x pairs row indices, so it takes 32 times fewer.
+constexpr size_t kMaxPairs = (size_t)1 << 29;
+constexpr size_t kMaxGemvPairs = (size_t)1 << 26;
 
 // Device status bits (workspace status word).
 enum : int32_t {

@@ -229,6 +229,7 @@ exl3_status exl3_moe_route(const float* logits, int T, int E, int top_k, int32_t
                            void* stream) {
   if (T < 0 || E < 1 || E > kMaxExperts) return EXL3_ERR_SHAPE;
   if (top_k < 1 || top_k > kMaxTopK || top_k > E) return EXL3_ERR_ARG;
+  if ((size_t)T * (size_t)top_k > kMaxPairs) return EXL3_ERR_SHAPE;
   if (!seg_offsets || !ws) return ws ? EXL3_ERR_ARG : EXL3_ERR_WORKSPACE;
   if (T > 0 && (!logits || !ids || !w || !seg_pairs)) return EXL3_ERR_ARG;
   if (ws_bytes < route_scratch_bytes(T, E, top_k)) return EXL3_ERR_WORKSPACE;
@@ -255,6 +256,9 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (path < EXL3_PATH_AUTO || path > EXL3_PATH_GEMM) return EXL3_ERR_ARG;
   if (T < 0) return EXL3_ERR_SHAPE;
   if (top_k < 1 || top_k > kMaxTopK || top_k > L.E - L.sc) return EXL3_ERR_ARG;
+  const size_t pairs = (size_t)T * (size_t)(top_k + L.sc);
+  if (pairs > kMaxPairs || (!use_gemm(L, T, top_k + L.sc, path) && pairs > kMaxGemvPairs))
+    return EXL3_ERR_SHAPE;
   if (T == 0) return EXL3_OK;
   if (!x || !logits || !out) return EXL3_ERR_ARG;
   if (!aligned16(x) || !aligned16(out) || (residual && !aligned16(residual))) return EXL3_ERR_ARG;
