@@ -48,7 +48,7 @@ class OracleLayer(ctypes.Structure):
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
         ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
-        ("expert_K", ctypes.c_void_p),
+        ("expert_K", ctypes.c_void_p), ("act_fp8", ctypes.c_int),
     ]
 
 
@@ -106,6 +106,8 @@ def lib():
             L.oracle_hadamard128_entry.restype = ctypes.c_double
             L.oracle_hadamard_blocks.argtypes = [u16p, ctypes.c_int]
             L.oracle_hadamard_blocks.restype = None
+            L.oracle_quantize_row_e4m3.argtypes = [u16p, ctypes.c_int, u16p]
+            L.oracle_quantize_row_e4m3.restype = None
             _lib = L
     return _lib
 
@@ -203,6 +205,14 @@ def hadamard_blocks(v: np.ndarray) -> np.ndarray:
     return v
 
 
+def quantize_row_e4m3(a: np.ndarray) -> np.ndarray:
+    """The row as the FP8 x FP8 product's activation operand: q_i * s."""
+    a = np.array(a, dtype=np.float64, copy=True)
+    out = np.zeros_like(a)
+    lib().oracle_quantize_row_e4m3(_ptr(a), a.size, _ptr(out))
+    return out
+
+
 # ---------------------------------------------------------------- routing
 def route(logits: np.ndarray, top_k: int):
     """ids [T,k] int32, w [T,k] f32, seg_offsets [E+1] int32, seg_pairs [T*k] int32."""
@@ -222,7 +232,7 @@ class Layer:
 
     def __init__(self, num_experts, hidden, inter, K, codes, suh, svh, fp8_round=False,
                  mult=DEFAULT_MCG_MULT, shared_w=None, hadamard=False, shared_coded=False,
-                 expert_K=None):
+                 expert_K=None, act_fp8=False):
         """num_experts routed experts; with shared_coded the code and side
         arrays hold num_experts + 1 experts, the last one the shared expert.
         expert_K ([experts][3] widths) gives every expert and projection its
@@ -237,6 +247,7 @@ class Layer:
         st.mult = mult
         st.hadamard = int(bool(hadamard))
         st.shared_coded = int(bool(shared_coded))
+        st.act_fp8 = int(bool(act_fp8))
         if expert_K is not None:
             ek = np.ascontiguousarray(expert_K, dtype=np.uint8)
             self.arrays.append(ek)

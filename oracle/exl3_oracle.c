@@ -29,7 +29,8 @@
  * Parity status: every function here is pinned by tests/test_oracle_pins.py
  * (closed forms, exhaustive states, library converters, brute force, dense
  * reference; the Hadamard matrix against scipy's Sylvester construction and a
- * closed-form rotated layer).  Compatibility with real EXL3/exlr8 checkpoints is unpinned: no
+ * closed-form rotated layer; the E4M3 activation operand against torch's
+ * float8_e4m3fn conversion).  Compatibility with real EXL3/exlr8 checkpoints is unpinned: no
  * checkpoint or test vector exists for this build.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (contraction off so
@@ -361,6 +362,8 @@ typedef struct {
     const uint8_t *expert_K; /* NULL, or [experts][3] widths per expert and projection: the
                                 codes of projection p are then the experts' arrays back to
                                 back, each at its own width */
+    int act_fp8;       /* 1: every projection's input row is quantised to E4M3 with a
+                          per-row scale (the FP8 x FP8 product's activation operand) */
 } oracle_layer;
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -384,6 +387,33 @@ double oracle_hadamard128_entry(int i, int j)
         bits >>= 1;
     }
     return (par ? -1.0 : 1.0) / sqrt(128.0);
+}
+
+/* Per-row E4M3 quantisation of an activation row for an FP8 x FP8 product.
+ * Page "GLM-5.3-Flash · exlr8 (K2/K3/K4)", Widths: with the E4M3 codebook the
+ * prefill runs on FP8 tensor cores; the pages give no activation recipe.
+ * reading: the row is taken in fp32 (the precision in which a kernel makes
+ * these integer decisions), s = fp32(amax / 448) with amax the row's largest
+ * magnitude, q_i = E4M3_RNE_sat(fp32(a_i / s)), and the row becomes q_i * s
+ * (exact in double).  An all-zero row stays zero.  out may alias a. */
+void oracle_quantize_row_e4m3(const double *a, int n, double *out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; i++) {
+        float ai = (float)a[i];
+        if (fabsf(ai) > amax)
+            amax = fabsf(ai);
+    }
+    if (amax == 0.0f) {
+        for (int i = 0; i < n; i++)
+            out[i] = 0.0;
+        return;
+    }
+    float s = amax / 448.0f;
+    for (int i = 0; i < n; i++) {
+        float q = (float)a[i] / s;
+        out[i] = oracle_e4m3_rne_sat((double)q) * (double)s;
+    }
 }
 
 /* v <- v . Hb for a row vector of n values (n a multiple of 128), where Hb is
@@ -465,6 +495,8 @@ static void project(const oracle_layer *L, const double *in, int n_in, const uin
         a[i] = in[i] * oracle_f16_to_double(suh[i]);
     if (L->hadamard)
         oracle_hadamard_blocks(a, n_in);
+    if (L->act_fp8)   /* the operand the tensor core multiplies: the rotated row */
+        oracle_quantize_row_e4m3(a, n_in, a);
     for (int o = 0; o < n_out; o++)
         out[o] = 0.0;
     for (int i = 0; i < n_in; i++) {

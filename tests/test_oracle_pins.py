@@ -623,3 +623,67 @@ def test_layer_uniform_width_table_equals_plain_layer():
     x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
     logits = rng.standard_normal((T, E)).astype(np.float32)
     assert np.array_equal(L0.forward(x, False, logits, k), L1.forward(x, False, logits, k))
+
+
+# ------------------------------------------------------------ FP8 activations (NEXT row 2)
+
+
+def _torch_quantize_row(a):
+    """Independent restatement through torch's float8_e4m3fn conversion."""
+    a32 = torch.tensor(np.asarray(a, np.float64), dtype=torch.float32)
+    amax = a32.abs().max()
+    if float(amax) == 0.0:
+        return np.zeros(a32.numel())
+    s = amax / torch.tensor(448.0, dtype=torch.float32)
+    q = (a32 / s).to(torch.float8_e4m3fn).to(torch.float64)
+    return (q * s.to(torch.float64)).numpy()
+
+
+@pytest.mark.parametrize("scale", [1.0, 1e-3, 37.5])
+def test_quantize_row_e4m3_vs_torch(scale):
+    """Per-row E4M3 quantisation equals torch's float8_e4m3fn conversion of
+    the fp32 quotient a / s, s = fp32(amax / 448), on rows with values down
+    in the E4M3 subnormal range."""
+    rng = np.random.default_rng(21)
+    a = scale * rng.standard_normal(4096) * np.exp(rng.uniform(-8, 0, 4096))
+    assert np.array_equal(oracle.quantize_row_e4m3(a), _torch_quantize_row(a))
+
+
+def test_quantize_row_e4m3_closed_forms():
+    """Powers of two below the row maximum quantise without error relative to
+    the scale (a_i / s = 448 * 2^-k, exact in E4M3); a zero row stays zero."""
+    a = np.array([1.0, -0.5, 0.25, -0.125, 2.0 ** -6, -1.0])
+    s = np.float32(1.0) / np.float32(448.0)
+    want = np.array([448.0, -224.0, 112.0, -56.0, 7.0, -448.0]) * np.float64(s)
+    assert np.array_equal(oracle.quantize_row_e4m3(a), want)
+    assert np.array_equal(oracle.quantize_row_e4m3(np.zeros(8)), np.zeros(8))
+
+
+def test_layer_fp8_activations_vs_numpy_dense_reference():
+    """With FP8 activations every projection multiplies the quantised input
+    row (after suh): numpy matmul with rows quantised through torch."""
+    E, H, I, K, T, k = 5, 64, 32, (4, 4, 4), 3, 2
+    L0, codes, suh, svh, _ = _small_layer(22, E, H, I, K, True, False)
+    L = oracle.Layer(E, H, I, K, codes, suh, svh, fp8_round=True, act_fp8=True)
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((T, H)).astype(np.float16).view(np.uint16)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    y = L.forward(x, False, logits, k)
+    ids, w, _, _ = oracle.route(logits, k)
+    xf = x.view(np.float16).astype(np.float64)
+    f = lambda a: a.view(np.float16).astype(np.float64)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            W = [f(oracle.decode_dense(codes[p][e], *((I, H) if p == 2 else (H, I)), K[p],
+                                       fp8_round=True)) for p in range(3)]
+            g = (_torch_quantize_row(xf[t] * f(suh[0][e])) @ W[0]) * f(svh[0][e])
+            u = (_torch_quantize_row(xf[t] * f(suh[1][e])) @ W[1]) * f(svh[1][e])
+            h = g / (1 + np.exp(-g)) * u
+            ref[t] += float(w[t, j]) * ((_torch_quantize_row(h * f(suh[2][e])) @ W[2]) * f(svh[2][e]))
+    assert np.allclose(y, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
+    # and it differs from the unquantised layer by the E4M3 rounding (~1-4 %)
+    y0 = L0.forward(x, False, logits, k)
+    rel = np.linalg.norm(y - y0) / np.linalg.norm(y0)
+    assert 1e-3 < rel < 0.1
