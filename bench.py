@@ -2,10 +2,15 @@
 """Benchmark of one EXL3 trellis MoE layer forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode,verify3,verify4,prefill]
 
-Workload: the GLM-5.3-Flash-shaped decode step (288 routed experts, top-8,
-hidden 4096, intermediate 2048, K=2 codes, 4 bf16 tokens, plus an fp16 shared
-expert), synthetic seeded data.  One JSON line on rank 0.
+Workloads (synthetic seeded data, the GLM-5.3-Flash MoE layer shape: 288
+routed experts, top-8, hidden 4096, intermediate 2048): the decode step (K2,
+4 bf16 tokens, plus an fp16 shared expert), the speculative-verify batch (32
+tokens, K3 and K4) and the prefill layer (K4 with the E4M3 rule, 7168
+tokens).  By default all four run, one after the other, and rank 0 prints ONE
+JSON line: its top-level numbers are the decode step's, and "configs" holds
+one block per workload with the same fields.
 
 ours:      the CUDA library through its C ABI; the step is captured once in a
            CUDA graph and replayed; L2 is flushed (512 MiB written, then 512
@@ -15,8 +20,9 @@ ours:      the CUDA library through its C ABI; the step is captured once in a
            roofline.  e2e: the same forward through the public API with
            pinned-host inputs copied in and the output copied out inside the
            timed region.
-reference: the CPU oracle as it stands, on this host, on a bounded sample
-           (one (token, expert) pair per step).
+reference: the CPU oracle as it stands, on this host's cores: a step is one
+           token of the workload (its top_k (token, expert) pairs, plus the
+           shared expert, each on its own thread).
 Under torchrun (N > 1) every rank runs its own token batch (weak scaling).
 """
 from __future__ import annotations
@@ -33,7 +39,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "decode"
+WORKLOADS = ("decode", "verify3", "verify4", "prefill")
 
 
 def parse():
@@ -43,8 +49,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default=WORKLOAD,
-                    help="decode (default), verify3, verify4, prefill: parity/profiling cases")
+    ap.add_argument("--workload", default=",".join(WORKLOADS),
+                    help="comma-separated workloads (decode, verify3, verify4, prefill, long); "
+                         "the first gives the line's top-level numbers")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profilers)")
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
@@ -119,10 +126,11 @@ def expert_work(spec, counts, per: int):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant stage's launches in one step, from ncu captures summarised under
-# profiles/ (decode: gemv_kernel_K2_decode.md; prefill: the big- and
-# small-tile kernels of the gate/up stage, prefill_gemm_dram.md); reported
-# only while the kernel sources hash to what was captured (otherwise null).
+# dominant stage's launches in one step, from ncu captures of this bench
+# (decode: the GEMV gate/up and down launches; prefill: the big- and
+# small-tile tensor-core launches of each stage, captured on the 64-expert
+# case and scaled); reported only while the kernel sources hash to what was
+# captured (otherwise null).
 NCU_TRAFFIC = {
     ("decode", "gate_up"): 128.116736e6 + 4.404480e6,
     ("prefill", "gate_up"): 4072320512,  # big-tile + small-tile launches
@@ -219,99 +227,84 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_pair_rate(wl, spec, x, logits, n_pairs, shared_w=None, codes=None):
-    """Time the CPU oracle on n_pairs (token, expert) pairs of token 0 and the
-    shared expert of token 0; returns (tokens/s, seconds used, sample text)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_layer(spec, codes=None):
     import numpy as np
 
     import oracle
     from trellis_quantized_moe_exl3_gb300 import synth
     codes = codes if codes is not None else [synth.layer_codes(spec, p) for p in range(3)]
     sides = [synth.side_vectors(spec, p) for p in range(3)]
-    ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
-                      [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
-                      shared_w=shared_w, hadamard=spec.hadamard, shared_coded=spec.shared_coded,
-                      expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
-    ids, w, _, _ = oracle.route(logits, wl.top_k)
-    t0 = time.perf_counter()
-    for j in range(n_pairs):
-        t, jj = divmod(j, wl.top_k)
-        ol.expert_pair(x[t % wl.T], wl.act == "bf16", int(ids[t % wl.T, jj]), float(w[t % wl.T, jj]))
-    t_pairs = (time.perf_counter() - t0) / n_pairs
-    t1 = time.perf_counter()
-    if shared_w is not None:
-        ol.shared_row(x[0], wl.act == "bf16")
-    t_shared = time.perf_counter() - t1
-    kp = wl.top_k + int(spec.shared_coded)  # the coded shared expert costs one more pair
-    per_token = kp * t_pairs + t_shared
-    sample = (f"{n_pairs} (token, expert) pair(s) of the {wl.T}-token {wl.name} workload"
-              + (" + the shared expert of one token" if shared_w is not None else "")
-              + f"; tokens/s = 1 / ({kp} x pair time"
-              + (" + shared time)" if shared_w is not None else ")"))
-    return 1.0 / per_token, time.perf_counter() - t0, sample
-
-
-# ----------------------------------------------------------------------------- reference arm
-def run_reference(args):
-    world, rank, _ = dist_env()
-    if rank != 0:
-        return
-    import numpy as np
-
-    import oracle
-    from trellis_quantized_moe_exl3_gb300 import synth
-    wl, spec = pick_workload(args)
-    x = synth.activations(wl.seed, wl.T, spec.hidden, wl.act)
-    logits = synth.router_logits(spec.seed, wl.T, spec.num_experts, wl.routing)
-    codes = [synth.layer_codes(spec, p) for p in range(3)]
-    sides = [synth.side_vectors(spec, p) for p in range(3)]
     sw = synth.shared_weights(spec) if spec.shared else None
-    ol = oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
-                      [s[0] for s in sides], [s[1] for s in sides], shared_w=sw,
-                      fp8_round=spec.fp8_round, hadamard=spec.hadamard,
-                      shared_coded=spec.shared_coded,
-                      expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
-    ids, w, _, _ = oracle.route(logits, wl.top_k)
-    pairs = [(t, j) for t in range(wl.T) for j in range(wl.top_k)]
-    for s in range(args.warmup):
-        t, j = pairs[s % len(pairs)]
-        ol.expert_pair(x[t], wl.act == "bf16", int(ids[t, j]), float(w[t, j]))
-    ts = time.perf_counter()
-    if sw is not None:
-        ol.shared_row(x[0], wl.act == "bf16")
-    t_shared = time.perf_counter() - ts
-    t0 = time.perf_counter()
-    for s in range(args.steps):
-        t, j = pairs[(args.warmup + s) % len(pairs)]
-        ol.expert_pair(x[t], wl.act == "bf16", int(ids[t, j]), float(w[t, j]))
-    t_pair = (time.perf_counter() - t0) / args.steps
-    kp = wl.top_k + int(spec.shared_coded)  # the coded shared expert costs one more pair
-    per_token = kp * t_pair + t_shared
-    value = 1.0 / per_token
-    sample = (f"one (token, expert) pair of the {wl.T}-token {wl.name} workload per step; tokens/s = "
-              f"1 / ({kp} x mean pair time"
-              + (" + shared-expert time of one token)" if sw is not None else ")"))
-    line = {
-        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_token * 1e3 * wl.T, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": workload_config(wl),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+    return oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
+                        [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
+                        shared_w=sw, hadamard=spec.hadamard, shared_coded=spec.shared_coded,
+                        expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
 
 
-def pick_workload(args):
+class OracleTokens:
+    """One token of a workload through the CPU oracle as it stands: the
+    token's top_k (token, expert) pairs (the coded shared expert's pair
+    included) and the dense shared expert, each a task on its own thread (the
+    C oracle releases the GIL), so a step uses min(tasks, host cores) cores."""
+
+    def __init__(self, wl, spec, x, logits, codes=None):
+        import oracle
+        self.wl, self.spec, self.x = wl, spec, x
+        self.ol = oracle_layer(spec, codes)
+        self.ids, self.w, _, _ = oracle.route(logits, wl.top_k)
+        self.n_tasks = wl.top_k + int(spec.shared_coded) + int(spec.shared)
+        self.cores = max(1, min(self.n_tasks, host_cores()))
+
+    def _tasks(self, t):
+        wl, spec, bf = self.wl, self.spec, self.wl.act == "bf16"
+        jobs = [(lambda j=j: self.ol.expert_pair(self.x[t], bf, int(self.ids[t, j]),
+                                                 float(self.w[t, j])))
+                for j in range(wl.top_k)]
+        if spec.shared_coded:
+            jobs.append(lambda: self.ol.expert_pair(self.x[t], bf, spec.num_experts, 1.0))
+        if spec.shared:
+            jobs.append(lambda: self.ol.shared_row(self.x[t], bf))
+        return jobs
+
+    def step(self, t) -> float:
+        """Seconds of wall time for token t."""
+        import concurrent.futures as cf
+        jobs = self._tasks(t % self.wl.T)
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=self.cores) as ex:
+            list(ex.map(lambda f: f(), jobs))
+        return time.perf_counter() - t0
+
+    def sample_text(self, n):
+        return (f"{n} token(s) of the {self.wl.T}-token {self.wl.name} workload, each step one "
+                f"token: its {self.n_tasks} expert evaluations (top-{self.wl.top_k} pairs"
+                + (" + the coded shared expert" if self.spec.shared_coded else "")
+                + (" + the dense shared expert" if self.spec.shared else "")
+                + f") on {self.cores} threads; tokens/s = tokens / wall time")
+
+
+def oracle_baseline(wl, spec, x, logits, n_tokens=2, codes=None):
+    ot = OracleTokens(wl, spec, x, logits, codes)
+    secs = [ot.step(t) for t in range(n_tokens)]
+    tot = sum(secs)
+    return {"value": n_tokens / tot, "unit": "tokens/s", "cores": ot.cores, "kind": "oracle",
+            "sample": ot.sample_text(n_tokens), "seconds": tot, "host_cores": host_cores()}
+
+
+def pick_workload(args, name):
     import dataclasses
 
     from trellis_quantized_moe_exl3_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
-    spec = wl.layers[args.layer]
-    if args.layer:
+    wl = synth.WORKLOADS[name]
+    spec = wl.layers[args.layer if name == "long" else 0]
+    if name == "long" and args.layer:
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-layer{args.layer}")
     if args.experts:
         spec = dataclasses.replace(spec, num_experts=args.experts)
@@ -328,39 +321,83 @@ def pick_workload(args):
     return wl, spec
 
 
-def workload_config(wl):
-    s = wl.layers[0]
+def workload_config(wl, spec):
+    """The workload's identity: the same keys on both arms."""
+    s = spec
     return {"workload": (f"{wl.name}: {s.num_experts} experts top-{wl.top_k}, hidden {s.hidden}, "
                          f"inter {s.inter}, K={list(s.K)}, T={wl.T} {wl.act}"
+                         + (", E4M3-rounded codebook" if s.fp8_round else "")
                          + (", + fp16 shared expert" if s.shared else "")
                          + (", + trellis-coded shared expert" if s.shared_coded else "")
                          + (", Hadamard rotation (format v2)" if s.hadamard else "")
                          + (", every expert tensor K3 or K4 (seeded)" if s.expert_K else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
             "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round, "hadamard": s.hadamard,
+            "routing": wl.routing,
             "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
 
 
+def line_config(blocks):
+    first = blocks[0]
+    cfg = dict(first["config"])
+    cfg["workloads"] = [b["name"] for b in blocks]
+    return cfg
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from trellis_quantized_moe_exl3_gb300 import synth
+    names = [n for n in args.workload.split(",") if n]
+    blocks = []
+    for i, name in enumerate(names):
+        wl, spec = pick_workload(args, name)
+        x = synth.activations(wl.seed, wl.T, spec.hidden, wl.act)
+        logits = synth.router_logits(spec.seed, wl.T, spec.num_experts, wl.routing)
+        ot = OracleTokens(wl, spec, x, logits)
+        # the first workload takes the full --steps/--warmup; the others a
+        # bounded sample of two tokens each, so the run stays within minutes
+        warm, steps = (args.warmup, args.steps) if i == 0 else (0, 2)
+        for t in range(warm):
+            ot.step(t)
+        secs = [ot.step(warm + t) for t in range(steps)]
+        ms = 1e3 * sum(secs) / steps
+        value = 1e3 / ms
+        blocks.append({"name": name, "config": workload_config(wl, spec), "value": value,
+                       "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "warmup": warm,
+                       "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ot.cores,
+                                        "kind": "oracle", "sample": ot.sample_text(steps),
+                                        "host_cores": host_cores()}})
+        del ot
+    top = blocks[0]
+    line = {
+        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": top["value"],
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": top["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": line_config(blocks),
+        "cpu_baseline": top["cpu_baseline"],
+        "e2e": {"value": top["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "configs": {b["name"]: {k: v for k, v in b.items() if k != "name"} for b in blocks},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- ours
-def run_ours(args):
+def measure_workload(args, name, dev, world, rank, local):
+    """Time one workload on this rank's GPU; returns its block of the line."""
     import ctypes
 
     import numpy as np
     import torch
 
     from trellis_quantized_moe_exl3_gb300 import _lib, synth
-    from trellis_quantized_moe_exl3_gb300 import build as lib_build
     from trellis_quantized_moe_exl3_gb300.api import Layer, route
 
-    world, rank, local = dist_env()
-    lib_build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    wl, spec = pick_workload(args)
+    wl, spec = pick_workload(args, name)
     codes = [synth.layer_codes(spec, p) for p in range(3)]
     sides = [synth.side_vectors(spec, p) for p in range(3)]
     sw = synth.shared_weights(spec) if spec.shared else None
@@ -375,7 +412,8 @@ def run_ours(args):
     d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
     layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw,
                   hadamard=spec.hadamard, shared_coded=spec.shared_coded, expert_K=spec.expert_K)
-    x = t16(x_np).view(torch.bfloat16)
+    act_t = torch.bfloat16 if wl.act == "bf16" else torch.float16
+    x = t16(x_np).view(act_t)
     lg = torch.from_numpy(lg_np).to(dev)
     T, k = wl.T, wl.top_k
     ws = layer.workspace(T, k, dev)
@@ -494,9 +532,9 @@ def run_ours(args):
     stage_ms /= args.steps
 
     # e2e: public API with host buffers, copies inside the timed region
-    x_host = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_host = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).view(act_t).pin_memory()
     lg_host = torch.from_numpy(lg_np).pin_memory()
-    out_host = torch.empty((T, spec.hidden), dtype=torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, spec.hidden), dtype=act_t).pin_memory()
     x_d = torch.empty_like(x)
     lg_d = torch.empty_like(lg)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -517,7 +555,37 @@ def run_ours(args):
     e2e_tot = max_over_ranks(float(np.sum(e2e_ms)), dev, world)
     e2e_value = job_tokens_per_s(world, T, args.steps, e2e_tot)
 
-    # roofline of the dominant expert kernel (the larger of gate/up and down)
+    roof = roofline(wl, spec, counts, T, k, stage_ms, sw is not None)
+    block = {
+        "name": name, "config": workload_config(wl, spec), "value": value, "unit": "tokens/s",
+        "ms_per_step": ms_per_step, "steps": args.steps, "warmup": args.warmup,
+        "roofline": roof["roofline"], "step_roofline": roof["step"],
+        "stage_ms": {n: float(v) for n, v in zip(_lib.STAGE_NAMES, stage_ms)},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2 + lg_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2),
+                "ms_per_step": e2e_tot / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "run": {"cuda_graph": use_graph, "n_active_experts": n_active,
+                "path": roof["path"], "launches_per_step": launches_per_step,
+                "stage_times": "separate graph with stage events" if stage_live else "eager re-run"},
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
+        block["cpu_baseline"] = oracle_baseline(wl, spec, x_np, lg_np, 2, codes=codes)
+    del layer, d_codes, d_suh, d_svh, d_sw, ws, flush, g, g_stage
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return block
+
+
+def roofline(wl, spec, counts, T, k, stage_ms, has_shared):
+    """Roofline of the dominant expert stage (the larger of gate/up and down):
+    decode-sized steps against HBM on the active experts' code and
+    side-vector bytes (with the decode issue-slot view beside it),
+    prefill-sized steps against the dense tensor peak on 2 P H I flops per
+    projection (with the decode view beside it)."""
+    from trellis_quantized_moe_exl3_gb300 import _lib
     hbm, bf16_tf, src = peaks()
     H, I = spec.hidden, spec.inter
     stage_names = _lib.STAGE_NAMES
@@ -530,57 +598,83 @@ def run_ours(args):
     peak_wps = dec_w[dom] / dec_t[dom]   # the widths' peaks, weighted by their decodes
     dec_rate = dec_w[dom] / (dom_ms / 1e3)
     hbm_rate = code_bytes[dom] / (dom_ms / 1e3) / 1e9
+    alu_view = {"achieved": dec_rate / 1e9, "peak": peak_wps / 1e9, "unit": "Gweight/s",
+                "frac": dec_rate / peak_wps, "weight_decodes": dec_w[dom],
+                "peak_source": "derived: 152 SMs x 2070 MHz x 128 issue slots / "
+                               "instructions per weight"}
+    traffic = ncu_traffic(wl.name, dom)
     if gemm_path:
         tf = flops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_tf,
-                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": ncu_traffic(wl.name, dom),
+                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": traffic,
                 "traffic_unit": "bytes per step of the stage's launches (ncu)",
                 "algorithmic_flops": flops[dom], "ms": dom_ms,
                 "peak_source": f"{src} (bf16_tflops burst; the fp16 dense rate equals bf16)",
-                "alu_view": {"achieved": dec_rate / 1e9, "peak": peak_wps / 1e9,
-                             "unit": "Gweight/s", "frac": dec_rate / peak_wps,
-                             "weight_decodes": dec_w[dom]}}
+                "alu_view": alu_view}
     else:
-        traffic = ncu_traffic(wl.name, dom)
-        roof = {"bound": "alu", "kernel": dom, "achieved": dec_rate / 1e9,
-                "peak": peak_wps / 1e9, "unit": "Gweight/s", "frac": dec_rate / peak_wps,
-                "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
-                "weight_decodes": dec_w[dom], "ms": dom_ms,
-                "peak_source": "derived: 152 SMs x 2070 MHz x 128 issue slots / instructions per weight",
-                "hbm_view": {"achieved": hbm_rate, "peak": hbm, "unit": "GB/s",
-                             "frac": hbm_rate / hbm, "algorithmic_bytes": code_bytes[dom],
-                             "peak_source": f"{src} (hbm_gbs, burst)"}}
-    step_bytes = code_bytes["gate_up"] + code_bytes["down"] + (3 * H * I * 2 if sw else 0)
+        roof = {"bound": "hbm", "kernel": dom, "achieved": hbm_rate, "peak": hbm,
+                "unit": "GB/s", "frac": hbm_rate / hbm, "traffic": traffic,
+                "traffic_unit": "bytes per launch (ncu)",
+                "algorithmic_bytes": code_bytes[dom], "ms": dom_ms,
+                "peak_source": f"{src} (hbm_gbs, burst)",
+                "alu_view": alu_view}
+    step_bytes = code_bytes["gate_up"] + code_bytes["down"] + (3 * H * I * 2 if has_shared else 0)
+    ms_step = float(sum(stage_ms))
+    step = {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+            "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm,
+            "what": "code + side-vector + shared-expert bytes of one step / step time"}
+    return {"roofline": roof, "step": step,
+            "path": "gemm (tcgen05)" if gemm_path else "gemv (mma.sync)"}
+
+
+def merge_clocks(blocks):
+    sms, mx, reasons, n = [], None, set(), 0
+    for b in blocks:
+        c = b["clocks"]
+        if c.get("sm_mhz") is not None:
+            sms.append(c["sm_mhz"])
+        mx = c.get("sm_max_mhz") or mx
+        reasons |= set(c.get("reasons", []))
+        n += c.get("samples", 0)
+    return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+            "reasons": sorted(reasons), "samples": n,
+            "per_workload": {b["name"]: b["clocks"].get("sm_mhz") for b in blocks}}
+
+
+def run_ours(args):
+    import torch
+
+    from trellis_quantized_moe_exl3_gb300 import build as lib_build
+
+    world, rank, local = dist_env()
+    lib_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    names = [n for n in args.workload.split(",") if n]
+    blocks = [measure_workload(args, n, dev, world, rank, local) for n in names]
+    top = blocks[0]
     line = {
-        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16",
+        "metric": "moe_layer_tokens_per_s", "value": top["value"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": top["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16",
         "arithmetic": "integer trellis decode; fp16 MMA operands, fp32 accumulate; "
                       "bf16 activations in and out",
         "data": "synthetic (seeded PCG64): uniform uint16 codes, side vectors 1+0.1N(0,1), "
                 "N(0,1) activations and router logits",
-        "config": {**workload_config(wl), "cuda_graph": use_graph, "n_active_experts": n_active,
-                   "path": "gemm (tcgen05)" if gemm_path else "gemv (mma.sync)",
-                   "stage_times": "separate graph with stage events" if stage_live else "eager re-run"},
-        "roofline": roof,
-        "step_roofline": {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
-                          "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm,
-                          "what": "code + side-vector + shared-expert bytes of one step / step time"},
-        "stage_ms": {n: float(v) for n, v in zip(stage_names, stage_ms)},
-        "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": int(x_host.numel() * 2 + lg_host.numel() * 4),
-                "d2h_bytes_per_step": int(out_host.numel() * 2),
-                "ms_per_step": e2e_tot / args.steps},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "config": line_config(blocks),
+        "roofline": top["roofline"],
+        "e2e": top["e2e"],
+        "gpu_launches": top["gpu_launches"],
+        "clocks": merge_clocks(blocks),
+        "configs": {b["name"]: {kk: v for kk, v in b.items() if kk != "name"} for b in blocks},
     }
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
-        # one whole token: its top_k (token, expert) pairs (+ its shared expert)
-        rate, secs, sample = oracle_pair_rate(wl, spec, x_np, lg_np, wl.top_k, shared_w=sw,
-                                              codes=codes)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": sample, "seconds": secs}
+    if "cpu_baseline" in top:
+        line["cpu_baseline"] = top["cpu_baseline"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -160,7 +160,10 @@ exl3_status exl3_moe_route(const float *logits, int T, int E, int top_k, int32_t
  *     any T <= 4096 with E <= 1024 and top_k <= 16 fits.
  *   - The first call on a device looks up the array's device address
  *     (once per device, with that device current); make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept for the life
+ *     of the process, so every call must run in the device's primary
+ *     context (the CUDA runtime's default): not after cudaDeviceReset, and
+ *     not under a context the caller created and made current.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents.  Each call clears what has to start at zero, but calls
  *     whose work overlaps on the GPU (different streams without ordering,
@@ -223,6 +226,24 @@ exl3_status exl3_layer_set_stage_events(exl3_layer_t *layer, void *const *events
  * host-side counter; launches captured into a CUDA graph count once, at
  * capture). */
 uint64_t exl3_launch_count(void);
+
+/* Test hook for the bounded waits of the tensor-core kernels (the pages have
+ * no counterpart).  Every wait inside those kernels has a clock budget; when
+ * one runs out, the kernel sets bit 4 (value 4) of the device status word,
+ * every CTA of the grid stops issuing work, drains the copies and tensor-core
+ * operations it already issued, frees its TMEM and returns, and
+ * exl3_get_device_status then reports EXL3_ERR_DEVICE with that bit.  This
+ * hook makes such a wait run out on purpose, without any fault: in the
+ * gate/up launch of the chosen kernel (1 = big tiles of more than 128
+ * tokens, 2 = small tiles of at most 128 tokens) the thread that loads the
+ * activation operands skips K step `ks` (64 inputs per step; a step past the
+ * end has no effect), so the MMA issuer waits on a barrier that nothing
+ * completes, and every wait of that launch gets `budget_cycles` SM clock
+ * cycles (100,000 .. 1,000,000,000) instead of the default 1,000,000,000.
+ * kernel = 0 clears the hook.  It stays set for every later forward of the
+ * process; a forward run with it gives an unspecified output.  Not thread
+ * safe.  Errors: EXL3_ERR_ARG for values outside these ranges. */
+exl3_status exl3_test_set_wait_fault(int kernel, int ks, long long budget_cycles);
 
 const char *exl3_status_string(exl3_status s);
 

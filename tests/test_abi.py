@@ -124,3 +124,14 @@ def test_forward_validation_without_layer(L):
     assert L.exl3_rmsnorm(vp(4096), 1, 4, 250, 1e-6, vp(4096), None) == _lib.EXL3_ERR_SHAPE
     s = ctypes.c_int32()
     assert L.exl3_get_device_status(None, None, ctypes.byref(s)) == _lib.EXL3_ERR_ARG
+
+
+def test_wait_fault_hook_validation(L):
+    """The bounded-wait test hook checks its arguments on the host (and
+    kernel 0 always clears it)."""
+    assert L.exl3_test_set_wait_fault(3, 1, 1000000) == _lib.EXL3_ERR_ARG
+    assert L.exl3_test_set_wait_fault(1, -1, 1000000) == _lib.EXL3_ERR_ARG
+    assert L.exl3_test_set_wait_fault(1, 1, 10) == _lib.EXL3_ERR_ARG
+    assert L.exl3_test_set_wait_fault(2, 1, 1 << 40) == _lib.EXL3_ERR_ARG
+    assert L.exl3_test_set_wait_fault(1, 2, 2000000) == _lib.EXL3_OK
+    assert L.exl3_test_set_wait_fault(0, 0, 0) == _lib.EXL3_OK

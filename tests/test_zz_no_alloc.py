@@ -5,8 +5,9 @@ owns every device allocation and passes in only the call's tensors, or a
 loop that must not call cudaMalloc because it can synchronise the device.
 exl3_moe_route_static serves them by keeping its routing scratch in a
 library-owned device array.  This test calls it through the C ABI twice in a
-row, with different sizes so that the second call starts from the first
-call's leftovers, and requires each result to equal, bit for bit, what
+row, in both orders of a large (multi-chunk) and a small case, so that each
+second call starts from the first call's leftovers, and requires every
+result to equal, bit for bit, both the CPU oracle's routing and what
 exl3_moe_route computes from the same logits with its own workspace (routing
 is integer and index work plus an fp32 softmax in a fixed order, so the
 tolerance of the routing tests is exact equality).
@@ -19,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from trellis_quantized_moe_exl3_gb300 import _lib, synth
 
 pytestmark = pytest.mark.gpu
@@ -50,19 +52,26 @@ def _route_with_workspace(logits, k):
     return ids, w, off, pairs
 
 
-def test_route_static_matches_workspace_route_twice():
+@pytest.mark.parametrize("order", [(0, 1), (1, 0)], ids=["large_then_small", "small_then_large"])
+def test_route_static_matches_oracle_and_workspace_route_twice(order):
     L = _lib.lib()
-    inputs = [torch.from_numpy(synth.router_logits(90 + i, T, E, dist)).cuda()
-              for i, (T, E, _, dist) in enumerate(CASES)]
+    cases = [CASES[i] for i in order]
+    inputs = [synth.router_logits(90 + i, CASES[i][0], CASES[i][1], CASES[i][3]) for i in order]
+    d_inputs = [torch.from_numpy(lg).cuda() for lg in inputs]
     results = []
-    for (T, E, k, _), logits in zip(CASES, inputs):  # back to back on one stream
+    for (T, E, k, _), lg in zip(cases, d_inputs):  # back to back on one stream
         outs = _outputs(T, E, k)
-        st = L.exl3_moe_route_static(_ptr(logits), T, E, k, *map(_ptr, outs), None)
+        st = L.exl3_moe_route_static(_ptr(lg), T, E, k, *map(_ptr, outs), None)
         assert st == 0, _lib.status_string(st)
         results.append(outs)
     torch.cuda.synchronize()
-    for (T, E, k, _), logits, got in zip(CASES, inputs, results):
-        want = _route_with_workspace(logits, k)
+    for (T, E, k, _), lg, d_lg, got in zip(cases, inputs, d_inputs, results):
+        ref = oracle.route(lg, k)
+        got_np = [t.cpu().numpy() for t in got]
+        got_np[3] = got_np[3][:T * k]
+        for g, r in zip(got_np, ref):
+            assert np.array_equal(g.view(np.int32).ravel(), np.asarray(r).view(np.int32).ravel())
+        want = _route_with_workspace(d_lg, k)
         torch.cuda.synchronize()
         for g, r in zip(got, want):
             assert torch.equal(g.view(torch.int32), r.view(torch.int32))

@@ -85,6 +85,8 @@ def lib():
     L.exl3_layer_set_stage_events.restype = i
     L.exl3_launch_count.argtypes = []
     L.exl3_launch_count.restype = ctypes.c_uint64
+    L.exl3_test_set_wait_fault.argtypes = [i, i, ctypes.c_longlong]
+    L.exl3_test_set_wait_fault.restype = i
     L.exl3_status_string.argtypes = [i]
     L.exl3_status_string.restype = ctypes.c_char_p
     _lib = L

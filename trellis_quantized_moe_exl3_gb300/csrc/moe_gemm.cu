@@ -53,7 +53,6 @@ constexpr int kAStage = 128 * kKS * 2;        // 16 KB
 constexpr int kBox = 64 * kKS * 2;            // one TMA box: 64 tokens x 64 inputs, 8 KB
 constexpr int kBStages = 2;
 constexpr int kBStage = kBN * kKS * 2;        // 64 KB
-constexpr int kMaxCluster = 2;        // strips of one tile sharing activation loads
 
 template <int K>
 struct GCfg {
@@ -81,7 +80,9 @@ struct GemmParams {
   const int32_t* seg_pairs;
   const float* wts;
   int32_t* status;
-  int cluster;              // CTAs per cluster (divides the strip count)
+  long long budget;         // clock budget of every pipeline wait
+  int fault_ks;             // test hook: the K step whose operand loads the TMA
+                            // thread skips (a wait that nothing completes); -1 = none
   int had;                  // format v2: suh on the activation side, outputs rotated
   int xrow_off;             // activation row (and scale) offset of projection 1
   // mixed widths: this launch's list of (tile, projection) pairs whose width
@@ -94,7 +95,7 @@ struct GemmParams {
 
 // (tile, projection) of the CTA's work unit u (its index over strips): from
 // the width's list in mixed mode, else u = tile * nproj + projection.  False
-// past the end of the work (the whole cluster shares u).
+// past the end of the work.
 __device__ __forceinline__ bool tile_of(const GemmParams& p, int u, int* tile, int* pj) {
   if (p.entries) {
     if (u >= p.n_entries[0]) return false;
@@ -112,6 +113,36 @@ __device__ __forceinline__ const uint16_t* gemm_expert_codes(const GemmParams& p
   return (pj ? p.codes[1] : p.codes[0]) +
          (p.off ? (size_t)p.off[(size_t)e * 3 + p.proj0 + pj]
                 : (pj ? p.stride[1] : p.stride[0]) * (size_t)e);
+}
+
+// Pipeline wait of one CTA role.  A false return means: stop issuing work
+// and unwind.  It happens when this wait ran out of budget, when any CTA of
+// the grid recorded a timeout (status bit 4), or when another role of this
+// CTA already gave up (abort flag in shared memory); in every case bit 4 of
+// the status word is set by the time any role sees the false return.
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
+                                          volatile uint32_t* abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait_or_abort(bar, parity, p.status, p.budget)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+// Epilogue entry of the decoder warps (threads 0 .. nthreads - 1): wait for
+// the accumulator, then take one CTA-wide decision whether to read TMEM and
+// store (thread 0 decides between two named barriers), so that warps which
+// exchange data through named barriers in the epilogue all take the same
+// branch.  False once any role of the grid gave up.
+constexpr int kEpiBar = 15;  // named barrier id (the epilogues use 1 .. 8)
+__device__ __forceinline__ bool epilogue_live(uint64_t* acc_full, const GemmParams& p,
+                                              volatile uint32_t* abort_flag,
+                                              volatile uint32_t* live_slot, int nthreads) {
+  pipe_wait(acc_full, 0, p, abort_flag);
+  named_bar_sync(kEpiBar, nthreads);
+  if (threadIdx.x == 0)
+    *live_slot = !*abort_flag && !(*reinterpret_cast<volatile int32_t*>(p.status) & 4);
+  named_bar_sync(kEpiBar, nthreads);
+  return *live_slot != 0;
 }
 
 // Format v2 epilogue of the M = outputs kernel: the 4 warps of a column group
@@ -228,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int s = blockIdx.x % strips;
   pdl_wait();
   int tile, pj;
-  if (!tile_of(p, blockIdx.x / strips, &tile, &pj)) return;  // the whole cluster shares the tile
+  if (!tile_of(p, blockIdx.x / strips, &tile, &pj)) return;
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int n0 = cnt < kHalfN ? ((cnt + 15) / 16) * 16 : kHalfN;
   const int n1 = cnt > kHalfN ? ((cnt - kHalfN + 15) / 16) * 16 : 0;
@@ -245,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_empty = b_full + kBStages;
   uint64_t* acc_full = b_empty + kBStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -254,9 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < nbst; i++) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], p.cluster);  // released by the MMA of every CTA of the cluster
+      mbar_init(&b_empty[i], 1);
     }
     mbar_init(acc_full, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kDec) tmem_alloc(tmem_slot, 2 * kHalfN);
@@ -278,41 +311,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peers may multicast into this CTA only after its barriers exist
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1);
-  const int crank = (int)cluster_ctarank();
 
   if (warp == kDec) {
     // ---------------------------------------------------------------- TMA
-    // Every CTA of the cluster computes another strip of the same tile, so the
-    // activation boxes are shared: CTA r loads boxes j = r (mod cluster) and
-    // multicasts them; a stage is refilled once all CTAs released it.
-    // (single-thread loops: stage index and phase advance incrementally and
-    // the descriptors are precomputed, so nothing on this critical path
-    // divides)
+    // The strips of a tile are neighbouring CTAs, so the activation boxes one
+    // CTA loads are mostly L2 hits for the others.  (single-thread loops:
+    // stage index and phase advance incrementally and the descriptors are
+    // precomputed, so nothing on this critical path divides)
     if (lane == 0) {
-      int sb = 0;
+      int sb = 0, issued = 0;
       uint32_t pb = 0;
       for (int ks = 0; ks < nks; ks++) {
-        mbar_wait_or_abort(&b_empty[sb], pb ^ 1, p.status);
-        mbar_arrive_expect_tx(&b_full[sb], nbox * kBox);
-        uint8_t* dst = b_ring + sb * bstage;
-        for (int j = crank; j < nbox; j += p.cluster)
-          tma_load_2d_multicast(dst + j * kBox, &tmap_b, ks * kKS, xrow0 + 64 * j, &b_full[sb],
-                                cmask);
+        if (!pipe_wait(&b_empty[sb], pb ^ 1, p, abort_flag)) break;
+        if (ks != p.fault_ks) {
+          mbar_arrive_expect_tx(&b_full[sb], nbox * kBox);
+          uint8_t* dst = b_ring + sb * bstage;
+          for (int j = 0; j < nbox; j++)
+            tma_load_2d(dst + j * kBox, &tmap_b, ks * kKS, xrow0 + 64 * j, &b_full[sb]);
+        }
+        issued = ks + 1;
         if (++sb == nbst) {
           sb = 0;
           pb ^= 1;
         }
       }
-      // before leaving: all boxes for this CTA have landed, and every CTA of
-      // the cluster has released the last stages (their release arrives here)
-      for (int ks = nks - nbst < 0 ? 0 : nks - nbst; ks < nks; ks++) {
-        mbar_wait_or_abort(&b_full[ks % nbst], (ks / nbst) & 1, p.status);
-        mbar_wait_or_abort(&b_empty[ks % nbst], (ks / nbst) & 1, p.status);
-      }
+      // before the CTA may exit, every box this thread requested has landed:
+      // loads can be outstanding only in the last nbst stages issued (a stage
+      // is refilled only after the MMA consumed it)
+      for (int ks = issued - nbst < 0 ? 0 : issued - nbst; ks < issued; ks++)
+        if (ks != p.fault_ks) mbar_drain(&b_full[ks % nbst], (ks / nbst) & 1, p.budget);
     }
   } else if (warp == kDec + 1) {
     // ---------------------------------------------------------------- MMA
@@ -326,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       for (int ks = 0; ks < nks; ks++) {
-        mbar_wait_or_abort(&a_full[sa], pa, p.status);
-        mbar_wait_or_abort(&b_full[sb], pb, p.status);
+        if (!pipe_wait(&a_full[sa], pa, p, abort_flag) || !pipe_wait(&b_full[sb], pb, p, abort_flag))
+          break;
         tc_fence_after();
         const uint64_t ad = a_desc0 + (uint64_t)(sa * (kAStage >> 4));
         const uint64_t bd = b_desc0 + (uint64_t)(sb * (bstage >> 4));
@@ -340,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      bd + ((kHalfN * 128) >> 4) + kk * (32 >> 4), id1, acc);
         }
         umma_commit(&a_empty[sa]);
-        umma_commit_multicast(&b_empty[sb], cmask);
+        umma_commit(&b_empty[sb]);
         if (++sa == nast) {
           sa = 0;
           pa ^= 1;
@@ -350,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb ^= 1;
         }
       }
+      // always committed, after an abort too: it completes once every MMA
+      // issued above is done, which TMEM deallocation waits for
       umma_commit(acc_full);
     }
   } else {
@@ -413,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 4; q++) s2[q] = s2n[q] | (s2n[q] << 16);
       if (n + 1 < n_my) load_suh(n + 1);
       fetch_neighbour<K>(lw);
-      mbar_wait_or_abort(&a_empty[sa], pa ^ 1, p.status);
+      if (!__all_sync(0xffffffffu, pipe_wait(&a_empty[sa], pa ^ 1, p, abort_flag))) break;
       decode_store<K, FP8>(lw, p.mult, neg16, smem + sa * kAStage + blk * 4096, off, s2);
       fence_async_smem();
       __syncwarp();
@@ -426,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------- epilogue
-    mbar_wait_or_abort(acc_full, 0, p.status);
+    // (skipped, stores and all, once any role of the grid gave up)
+    const bool live = epilogue_live(acc_full, p, abort_flag, abort_flag + 1, kDec * 32);
     tc_fence_after();
     // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its access quarter) and
     // every (kDec/4)-th chunk of 16 token columns (column n = token n: the
@@ -435,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int o = 128 * s + 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh_e = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out;
-    if (p.had) {
+    if (live && p.had) {
       // the A ring is idle once the accumulator is complete
       float* xbuf = reinterpret_cast<float*>(smem) + cgrp * (128 * 17);
       float svr[4];
@@ -451,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const float sv = __half2float(__ushort_as_half(svh_e[o]));
-    for (int c0 = p.had ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
+    for (int c0 = p.had || !live ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait(a0);
@@ -471,10 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == kDec) {
+    // every MMA issued has completed (immediate unless a role gave up early)
+    mbar_drain(acc_full, 0, p.budget);
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kHalfN);
   }
-  cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
 // ---------------------------------------------------------------------------
@@ -518,7 +551,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int s = blockIdx.x % chunks;
   pdl_wait();
   int tile, pj;
-  if (!tile_of(p, blockIdx.x / chunks, &tile, &pj)) return;  // the whole cluster shares the tile
+  if (!tile_of(p, blockIdx.x / chunks, &tile, &pj)) return;
   const int e = p.tiles[4 * tile], pos0 = p.tiles[4 * tile + 1], cnt = p.tiles[4 * tile + 2];
   const int nks = p.in / kKS;
   const int tm = cnt <= 64 ? 64 : 128;  // MMA M
@@ -531,6 +564,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   uint64_t* x_empty = x_full + kSXStages;
   uint64_t* acc_full = x_empty + kSXStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
   uint8_t* const x_ring = smem + SCfg::kOffX;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -541,9 +575,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     for (int i = 0; i < kSXStages; i++) {
       mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], p.cluster);  // released by the MMA of every CTA of the cluster
+      mbar_init(&x_empty[i], 1);
     }
     mbar_init(acc_full, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kSDec) tmem_alloc(tmem_slot, kSN);
@@ -564,34 +599,34 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peers may multicast into this CTA only after its barriers exist
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1);
-  const int crank = (int)cluster_ctarank();
 
   if (warp == kSDec) {
     // ---------------------------------------------------------------- TMA
-    // one or two 64-token boxes per K step; CTA r of the cluster loads boxes
-    // j = r (mod cluster) and multicasts them (every CTA computes other outputs)
+    // one or two 64-token boxes per K step (the output chunks of a tile are
+    // neighbouring CTAs, so most of these loads hit L2)
     if (lane == 0) {
-      int sx = 0;
+      int sx = 0, issued = 0;
       uint32_t px = 0;
       for (int ks = 0; ks < nks; ks++) {
-        mbar_wait_or_abort(&x_empty[sx], px ^ 1, p.status);
-        mbar_arrive_expect_tx(&x_full[sx], nxbox * kBox);
-        for (int j = crank; j < nxbox; j += p.cluster)
-          tma_load_2d_multicast(x_ring + sx * kSXStage + j * kBox, &tmap_x, ks * kKS, xrow0 + 64 * j,
-                                &x_full[sx], cmask);
+        if (!pipe_wait(&x_empty[sx], px ^ 1, p, abort_flag)) break;
+        if (ks != p.fault_ks) {
+          mbar_arrive_expect_tx(&x_full[sx], nxbox * kBox);
+          for (int j = 0; j < nxbox; j++)
+            tma_load_2d(x_ring + sx * kSXStage + j * kBox, &tmap_x, ks * kKS, xrow0 + 64 * j,
+                        &x_full[sx]);
+        }
+        issued = ks + 1;
         if (++sx == kSXStages) {
           sx = 0;
           px ^= 1;
         }
       }
-      for (int ks = nks - kSXStages < 0 ? 0 : nks - kSXStages; ks < nks; ks++) {
-        mbar_wait_or_abort(&x_full[ks % kSXStages], (ks / kSXStages) & 1, p.status);
-        mbar_wait_or_abort(&x_empty[ks % kSXStages], (ks / kSXStages) & 1, p.status);
-      }
+      // drain: loads can be outstanding only in the last kSXStages issued
+      for (int ks = issued - kSXStages < 0 ? 0 : issued - kSXStages; ks < issued; ks++)
+        if (ks != p.fault_ks)
+          mbar_drain(&x_full[ks % kSXStages], (ks / kSXStages) & 1, p.budget);
     }
   } else if (warp == kSDec + 1) {
     // ---------------------------------------------------------------- MMA
@@ -605,8 +640,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       int sw = 0, sx = 0;
       uint32_t pw = 0, px = 0;
       for (int ks = 0; ks < nks; ks++) {
-        mbar_wait_or_abort(&w_full[sw], pw, p.status);
-        mbar_wait_or_abort(&x_full[sx], px, p.status);
+        if (!pipe_wait(&w_full[sw], pw, p, abort_flag) || !pipe_wait(&x_full[sx], px, p, abort_flag))
+          break;
         tc_fence_after();
         const uint64_t xd = x_desc0 + (uint64_t)(sx * (kSXStage >> 4));
         const uint64_t wd = w_desc0 + (uint64_t)(sw * (kSWStage >> 4));
@@ -615,7 +650,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           umma_f16(tmem, xd + kk * (32 >> 4), wd + kk * (8192 >> 4), idesc,
                    (ks > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&w_empty[sw]);
-        umma_commit_multicast(&x_empty[sx], cmask);
+        umma_commit(&x_empty[sx]);
         if (++sw == kSWStages) {
           sw = 0;
           pw ^= 1;
@@ -625,7 +660,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           px ^= 1;
         }
       }
-      umma_commit(acc_full);
+      umma_commit(acc_full);  // always (see the big-tile kernel)
     }
   } else {
     // ---------------------------------------------------------------- decode
@@ -686,7 +721,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int q = 0; q < 4; q++) s2[q] = s2n[q] | (s2n[q] << 16);
       if (n + 1 < n_my) load_suh(n + 1);
       fetch_neighbour<K>(lw);
-      mbar_wait_or_abort(&w_empty[sw], pw ^ 1, p.status);
+      if (!__all_sync(0xffffffffu, pipe_wait(&w_empty[sw], pw ^ 1, p, abort_flag))) break;
       decode_store<K, FP8>(lw, p.mult, neg16, smem + sw * kSWStage + job_off, off, s2);
       fence_async_smem();
       __syncwarp();
@@ -702,14 +737,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // warp w reads TMEM lanes 32 (w % 4) .. + 31, which hold tokens
     // 16 (w % 4) + lane, lane < 16 (M 64) or 32 (w % 4) + lane (M 128); it
     // takes output columns 64 (w / 4) .. + 63
-    mbar_wait_or_abort(acc_full, 0, p.status);
+    const bool live = epilogue_live(acc_full, p, abort_flag, abort_flag + 1, kSDec * 32);
     tc_fence_after();
     const int q4 = warp & 3, cg = warp >> 2;
     const bool lane_live = tm == 128 || lane < 16;
     const int n = (tm == 128 ? 32 : 16) * q4 + lane;  // token of this lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + kSN * s;
-    if (p.had) {
+    if (live && p.had) {
       // Format v2: warps (q4, 2b) and (q4, 2b + 1) hold the two halves of the
       // 128-output block b for the same 32 TMEM lanes (tokens).  Both stage
       // their columns in shared memory (the weight ring is idle once the
@@ -752,7 +787,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
       }
     }
-    for (int c0 = p.had ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
+    for (int c0 = p.had || !live ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait(a0);
@@ -779,10 +814,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == kSDec) {
+    mbar_drain(acc_full, 0, p.budget);  // every MMA issued has completed
     tc_fence_after();
     tmem_dealloc(tmem, kSN);
   }
-  cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
 // Row kernels: one warp per position row, 16-byte vector accesses; the first
@@ -1175,15 +1210,11 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = gp.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   cudaError_t err = cudaLaunchKernelEx(&cfg, kfn, tm, gp);
   note_launches(1);
   return err;
@@ -1203,15 +1234,11 @@ cudaError_t launch_gemm64(const CUtensorMap& tm, const GemmParams& gp, int grid,
   cfg.blockDim = dim3(kSThreads, 1, 1);
   cfg.dynamicSmemBytes = SCfg::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = gp.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   cudaError_t err = cudaLaunchKernelEx(&cfg, kfn, tm, gp);
   note_launches(1);
   return err;
@@ -1243,13 +1270,15 @@ cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParam
 
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Largest cluster size (<= kMaxCluster) that divides the number of strips, so
-// a cluster always holds strips of one tile.
-int cluster_for(int strips) {
-  int c = kMaxCluster;
-  while (c > 1 && strips % c) c >>= 1;
-  return c;
-}
+// Test hook of the bounded waits (exl3_test_set_wait_fault): which gate/up
+// tensor-core launch skips one K step's activation loads, and the clock
+// budget of that launch's waits.
+struct WaitFault {
+  int kernel = 0;  // 0 none, 1 big-tile kernel, 2 small-tile kernel (gate/up launch)
+  int ks = -1;
+  long long budget = kWaitBudgetCycles;
+};
+WaitFault g_fault;
 
 size_t max_tiles(int T, int E, int top_k) {
   const size_t P = (size_t)T * top_k;
@@ -1374,17 +1403,26 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
   gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.gu_out = gu_buf; gu.n_pos = (size_t)P;
   gu.status = rb.status;
-  gu.cluster = cluster_for(L.I / 128);
+  gu.budget = kWaitBudgetCycles;
+  gu.fault_ks = -1;
   gu.had = L.had;
   gu.xrow_off = L.had ? P : 0;
   gu.proj0 = 0;
+  const WaitFault wf = g_fault;
+  auto with_fault = [&](GemmParams q, int kernel) {
+    if (wf.kernel == kernel) {
+      q.fault_ks = wf.ks;
+      q.budget = wf.budget;
+    }
+    return q;
+  };
   // without mixed widths gate and up share a width (one launch)
-  if ((err = run(0, 0, tm_x, gu, mt * 2 * (L.I / 128), L.K[0])) != cudaSuccess) return err;
+  if ((err = run(0, 0, tm_x, with_fault(gu, 1), mt * 2 * (L.I / 128), L.K[0])) != cudaSuccess)
+    return err;
   if (small_ok) {
-    GemmParams gs = gu;
+    GemmParams gs = with_fault(gu, 2);
     gs.tiles = tiles_s;
     gs.n_tiles = ntiles + 1;
-    gs.cluster = cluster_for(L.I / kSN);
     if ((err = run(1, 0, tm_x, gs, L.E * 2 * (L.I / kSN), L.K[0])) != cudaSuccess) return err;
   }
   rec(3);
@@ -1402,7 +1440,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   dn.in = L.I; dn.out = L.H; dn.nproj = 1; dn.mult = L.mult;
   dn.tiles = tiles; dn.n_tiles = ntiles; dn.xinv = hinv; dn.r_out = r;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.status = rb.status;
-  dn.cluster = cluster_for(L.H / 128);
+  dn.budget = kWaitBudgetCycles;
+  dn.fault_ks = -1;
   dn.had = L.had;
   dn.proj0 = 2;
   err = run(0, 1, tm_h, dn, mt * (L.H / 128), L.K[2]);
@@ -1410,7 +1449,6 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     GemmParams ds = dn;
     ds.tiles = tiles_s;
     ds.n_tiles = ntiles + 1;
-    ds.cluster = cluster_for(L.H / kSN);
     err = run(1, 1, tm_h, ds, L.E * (L.H / kSN), L.K[2]);
   }
   rec(5);
@@ -1418,3 +1456,17 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
 }
 
 }  // namespace exl3
+
+extern "C" exl3_status exl3_test_set_wait_fault(int kernel, int ks, long long budget_cycles) {
+  if (kernel == 0) {
+    exl3::g_fault = exl3::WaitFault{};
+    return EXL3_OK;
+  }
+  if (kernel < 1 || kernel > 2 || ks < 0 || budget_cycles < 100000 ||
+      budget_cycles > exl3::kWaitBudgetCycles)
+    return EXL3_ERR_ARG;
+  exl3::g_fault.kernel = kernel;
+  exl3::g_fault.ks = ks;
+  exl3::g_fault.budget = budget_cycles;
+  return EXL3_OK;
+}

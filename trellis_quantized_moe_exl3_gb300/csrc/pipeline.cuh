@@ -46,24 +46,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity; false when the budget ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitBudgetCycles) return false;
-  }
-  return true;
-}
-
 // Bounded wait that also gives up as soon as any CTA has recorded a timeout
 // in the device status word (bit 4), so a stuck pipeline ends the whole grid
 // quickly instead of every CTA spending its own budget.  The status word (a
 // global load) is read only every kStatusPollCycles, so a wait that needs
-// a few retries is not slowed by memory round trips.
+// a few retries is not slowed by memory round trips.  A wait that runs out
+// of budget sets bit 4 itself; either way a false return means "stop issuing
+// work and unwind".
 constexpr long long kStatusPollCycles = 20000;  // ~10 us
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   int32_t* status) {
+                                                   int32_t* status,
+                                                   long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   long long next_poll = t0 + kStatusPollCycles;
@@ -71,13 +64,24 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
     const long long now = clock64();
     if (now >= next_poll) {
       if (*reinterpret_cast<volatile int32_t*>(status) & 4) return false;
-      if (now - t0 > kWaitBudgetCycles) {
+      if (now - t0 > budget) {
         atomicOr(status, 4);
         return false;
       }
       next_poll = now + kStatusPollCycles;
     }
   }
+  return true;
+}
+
+// Teardown wait: bounded by the clock budget only (it ignores the status
+// word), for draining copies and tensor-core work this CTA issued before it
+// releases shared memory or TMEM.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, long long budget) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > budget) return false;
   return true;
 }
 

@@ -20,7 +20,11 @@ void* g_addr[kMaxDevices] = {};
 
 // Device address of g_route_scratch on the current device.  In host code the
 // array's name is only a host-side shadow, so the address has to come from
-// the runtime, once per device, with that device current.
+// the runtime, once per device, with that device current.  The address is
+// cached by device index, which assumes every call runs in the device's
+// primary context (the runtime's default) for the life of the process: after
+// cudaDeviceReset, or under a context the caller made current itself, the
+// cached address would belong to a module that is gone.
 cudaError_t static_scratch(void** out) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);

@@ -113,39 +113,6 @@ __device__ __forceinline__ void tmem_ld_wait(float (&v)[16]) {
                : "memory");
 }
 
-// Arrive on the mbarrier at the same shared-memory offset in every CTA of
-// `cta_mask` (within the cluster) once this thread's tcgen05 ops complete.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// 2-D TMA tile load delivered to the same shared-memory offset in every CTA of
-// `cta_mask`, signalling the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst_smem, const void* tmap, int c0,
-                                                      int c1, uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Whole-cluster barrier (every thread of every CTA of the cluster).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
 // 2-D TMA tile load (coordinates: c0 innermost, in elements) completing on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, int c0, int c1,
                                             uint64_t* bar) {
