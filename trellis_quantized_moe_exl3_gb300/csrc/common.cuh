@@ -77,6 +77,24 @@ __device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
   return r;
 }
 
+// The codebook's mask-xor, (x & 0x8FFF8FFF) ^ 0x3B603B60, as ONE three-input
+// logic operation.  A LOP3 takes a single immediate, so with both constants
+// as immediates the compiler splits it into two logic operations: one more
+// ALU-pipe instruction per decoded weight, on the pipe that bounds the decode.
+// The constants therefore come in registers (mcg_consts(), taken once per
+// decode routine).
+struct McgConsts {
+  uint32_t mask, xr;
+};
+__device__ __forceinline__ McgConsts mcg_consts() {
+  return McgConsts{opaque_u32(kMcgMask), opaque_u32(kMcgXor)};
+}
+__device__ __forceinline__ uint32_t mcg_maskxor(uint32_t x, const McgConsts& c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(x), "r"(c.mask), "r"(c.xr));
+  return r;
+}
+
 // State of lane-local weight u (0..63): bits [uK, uK+16) of the lane stream.
 // u is a compile-time constant after unrolling, so this is one funnel shift
 // (or plain shift) and one mask.
@@ -96,8 +114,8 @@ __device__ __forceinline__ uint32_t lane_state(const LaneWords<K>& lw, int u) {
 }
 
 // mcg codebook before the final add: the two fp16 halves {a (low), b (high)}.
-__device__ __forceinline__ uint32_t mcg_halves(uint32_t s, uint32_t mult) {
-  return ((s * mult) & kMcgMask) ^ kMcgXor;
+__device__ __forceinline__ uint32_t mcg_halves(uint32_t s, uint32_t mult, const McgConsts& c) {
+  return mcg_maskxor(s * mult, c);
 }
 
 // {a, b} halves of lane-local weight u.  For K = 2 and 4 the 16 bits above a
@@ -109,15 +127,15 @@ __device__ __forceinline__ uint32_t mcg_halves(uint32_t s, uint32_t mult) {
 // K = 3 the window is masked.
 template <int K>
 __device__ __forceinline__ uint32_t lane_halves(const LaneWords<K>& lw, int u, uint32_t mult,
-                                                uint32_t neg_shift16) {
+                                                uint32_t neg_shift16, const McgConsts& c) {
   if constexpr (K == 2 || K == 4) {
     constexpr int step = 16 / K;
     const uint32_t xa = lane_window32<K>(lw, u * K) * mult;
     const uint32_t xb = lane_window32<K>(lw, (u + step) * K) * mult;
     const uint32_t x = xb * neg_shift16 + xa;
-    return (x & kMcgMask) ^ kMcgXor;
+    return mcg_maskxor(x, c);
   } else {
-    return mcg_halves(lane_state<K>(lw, u), mult);
+    return mcg_halves(lane_state<K>(lw, u), mult, c);
   }
 }
 

@@ -33,10 +33,11 @@ __global__ void __launch_bounds__(256) decode_dense_kernel(const uint16_t* __res
   fetch_neighbour<K>(lw);
   const int tj = jg * 8 + g;
   const uint32_t neg16 = opaque_u32(0xFFFF0000u);
+  const McgConsts mc = mcg_consts();
 #pragma unroll
   for (int u = 0; u < 64; u += 2) {
-    const uint32_t m0 = lane_halves<K>(lw, u, mult, neg16);
-    const uint32_t m1 = lane_halves<K>(lw, u + 1, mult, neg16);
+    const uint32_t m0 = lane_halves<K>(lw, u, mult, neg16, mc);
+    const uint32_t m1 = lane_halves<K>(lw, u + 1, mult, neg16, mc);
     uint32_t v2 = sum_halves2(m0, m1);
     if (FP8) v2 = e4m3_round2(v2);
 #pragma unroll

@@ -186,11 +186,12 @@ __device__ __forceinline__ void rotate_store_cols(float* xbuf, const float (&a0)
 // tail is carried to the next pp); see lane_halves for the correction.
 template <int K, int PP>
 __device__ __forceinline__ void halves16(const LaneWords<K>& lw, uint32_t mult, uint32_t neg16,
+                                         const McgConsts& mc,
                                          uint32_t (&xp)[16 + (K == 3 ? 0 : 16 / K)],
                                          uint32_t (&m)[16]) {
   if constexpr (K == 3) {
 #pragma unroll
-    for (int t = 0; t < 16; t++) m[t] = mcg_halves(lane_state<K>(lw, 16 * PP + t), mult);
+    for (int t = 0; t < 16; t++) m[t] = mcg_halves(lane_state<K>(lw, 16 * PP + t), mult, mc);
   } else {
     constexpr int step = 16 / K;
     if constexpr (PP == 0) {
@@ -203,7 +204,7 @@ __device__ __forceinline__ void halves16(const LaneWords<K>& lw, uint32_t mult, 
 #pragma unroll
     for (int t = step; t < 16 + step; t++) xp[t] = lane_window32<K>(lw, (16 * PP + t) * K) * mult;
 #pragma unroll
-    for (int t = 0; t < 16; t++) m[t] = ((xp[t + step] * neg16 + xp[t]) & kMcgMask) ^ kMcgXor;
+    for (int t = 0; t < 16; t++) m[t] = mcg_maskxor(xp[t + step] * neg16 + xp[t], mc);
   }
 }
 
@@ -225,11 +226,12 @@ template <int K, int FP8>
 __device__ __forceinline__ void decode_store(const LaneWords<K>& lw, uint32_t mult, uint32_t neg16,
                                              uint8_t* a_blk, const int (&off)[8],
                                              const uint32_t (&s2)[4]) {
+  const McgConsts mc = mcg_consts();
   uint32_t v[8][4];
   uint32_t xp[16 + (K == 3 ? 0 : 16 / K)];
   uint32_t m[16];
 #define EXL3_PP(PP)                                                            \
-  halves16<K, PP>(lw, mult, neg16, xp, m);                                     \
+  halves16<K, PP>(lw, mult, neg16, mc, xp, m);                                 \
   _Pragma("unroll") for (int idx = 0; idx < 8; idx++) {                        \
     const int t0 = idx; /* t = 8 rr + 4 hf + 2 jh + jl, rr = 0 */              \
     uint32_t v2 = sum_halves2(m[t0], m[t0 + 8]);                               \

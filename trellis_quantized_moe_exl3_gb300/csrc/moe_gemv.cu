@@ -292,6 +292,7 @@ template <int K, int FP8>
 __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& b,
                                            float (&acc)[8][4], uint32_t mult) {
   const uint32_t neg16 = opaque_u32(0xFFFF0000u);
+  const McgConsts mc = mcg_consts();
   constexpr int step = K == 3 ? 0 : 16 / K;
   uint32_t xp[8 + (K == 3 ? 0 : 16 / K)];
   if constexpr (K != 3) {
@@ -303,13 +304,13 @@ __device__ __forceinline__ void decode_mma(const LaneWords<K>& lw, const uint4& 
     uint32_t m[8];
     if constexpr (K == 3) {
 #pragma unroll
-      for (int t = 0; t < 8; t++) m[t] = mcg_halves(lane_state<K>(lw, 8 * r0 + t), mult);
+      for (int t = 0; t < 8; t++) m[t] = mcg_halves(lane_state<K>(lw, 8 * r0 + t), mult, mc);
     } else {
       // xp[0..step) already hold weights 8 r0 .. 8 r0 + step - 1
 #pragma unroll
       for (int t = step; t < 8 + step; t++) xp[t] = lane_window32<K>(lw, (8 * r0 + t) * K) * mult;
 #pragma unroll
-      for (int t = 0; t < 8; t++) m[t] = ((xp[t + step] * neg16 + xp[t]) & kMcgMask) ^ kMcgXor;
+      for (int t = 0; t < 8; t++) m[t] = mcg_maskxor(xp[t + step] * neg16 + xp[t], mc);
 #pragma unroll
       for (int t = 0; t < step; t++) xp[t] = xp[t + 8];
     }
