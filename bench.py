@@ -8,9 +8,11 @@ Workloads (synthetic seeded data, the GLM-5.3-Flash MoE layer shape: 288
 routed experts, top-8, hidden 4096, intermediate 2048): the decode step (K2,
 4 bf16 tokens, plus an fp16 shared expert), the speculative-verify batch (32
 tokens, K3 and K4) and the prefill layer (K4 with the E4M3 rule, 7168
-tokens).  By default all four run, one after the other, and rank 0 prints ONE
-JSON line: its top-level numbers are the decode step's, and "configs" holds
-one block per workload with the same fields.
+tokens), the last one also with FP8 x FP8 products ("prefill+fp8": E4M3
+activation rows with an fp32 scale each, tcgen05 kind::f8f6f4).  By default
+all five run, one after the other, and rank 0 prints ONE JSON line: its
+top-level numbers are the decode step's, and "configs" holds one block per
+workload with the same fields.
 
 ours:      the CUDA library through its C ABI; the step is captured once in a
            CUDA graph and replayed; L2 is flushed (512 MiB written, then 512
@@ -39,7 +41,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("decode", "verify3", "verify4", "prefill")
+WORKLOADS = ("decode", "verify3", "verify4", "prefill", "prefill+fp8")
 
 
 def parse():
@@ -50,8 +52,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=",".join(WORKLOADS),
-                    help="comma-separated workloads (decode, verify3, verify4, prefill, long); "
-                         "the first gives the line's top-level numbers")
+                    help="comma-separated workloads (decode, verify3, verify4, prefill, long; "
+                         "a '+fp8' suffix selects FP8 x FP8 products); the first gives the "
+                         "line's top-level numbers")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profilers)")
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
@@ -245,7 +248,8 @@ def oracle_layer(spec, codes=None):
     return oracle.Layer(spec.num_experts, spec.hidden, spec.inter, spec.K, codes,
                         [s[0] for s in sides], [s[1] for s in sides], fp8_round=spec.fp8_round,
                         shared_w=sw, hadamard=spec.hadamard, shared_coded=spec.shared_coded,
-                        expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None)
+                        expert_K=np.array(spec.expert_K, np.uint8) if spec.expert_K else None,
+                        act_fp8=spec.act_fp8)
 
 
 class OracleTokens:
@@ -302,6 +306,8 @@ def pick_workload(args, name):
     import dataclasses
 
     from trellis_quantized_moe_exl3_gb300 import synth
+    fp8_ops = name.endswith("+fp8")
+    name = name[:-4] if fp8_ops else name
     wl = synth.WORKLOADS[name]
     spec = wl.layers[args.layer if name == "long" else 0]
     if name == "long" and args.layer:
@@ -318,6 +324,9 @@ def pick_workload(args, name):
     if args.mixed:
         spec = dataclasses.replace(spec, expert_K=synth.mixed_widths(spec.seed, spec.n_coded))
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-mixedK34")
+    if fp8_ops:  # the E4M3 operand needs the E4M3 rule
+        spec = dataclasses.replace(spec, act_fp8=True, fp8_round=True)
+        wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}+fp8")
     return wl, spec
 
 
@@ -330,10 +339,11 @@ def workload_config(wl, spec):
                          + (", + fp16 shared expert" if s.shared else "")
                          + (", + trellis-coded shared expert" if s.shared_coded else "")
                          + (", Hadamard rotation (format v2)" if s.hadamard else "")
-                         + (", every expert tensor K3 or K4 (seeded)" if s.expert_K else "")),
+                         + (", every expert tensor K3 or K4 (seeded)" if s.expert_K else "")
+                         + (", FP8 x FP8 products (E4M3 activation rows)" if s.act_fp8 else "")),
             "T": wl.T, "top_k": wl.top_k, "experts": s.num_experts, "hidden": s.hidden,
             "inter": s.inter, "K": list(s.K), "fp8_round": s.fp8_round, "hadamard": s.hadamard,
-            "routing": wl.routing,
+            "act_fp8": s.act_fp8, "routing": wl.routing,
             "l2": "flushed before every timed step (512 MiB written, then 512 MiB read)"}
 
 
@@ -411,7 +421,8 @@ def measure_workload(args, name, dev, world, rank, local):
     d_svh = [t16(s[1]).view(torch.float16) for s in sides]
     d_sw = [t16(a).view(torch.float16) for a in sw] if sw else None
     layer = Layer(d_codes, d_suh, d_svh, spec.K, fp8_round=spec.fp8_round, shared=d_sw,
-                  hadamard=spec.hadamard, shared_coded=spec.shared_coded, expert_K=spec.expert_K)
+                  hadamard=spec.hadamard, shared_coded=spec.shared_coded, expert_K=spec.expert_K,
+                  act_fp8=spec.act_fp8)
     act_t = torch.bfloat16 if wl.act == "bf16" else torch.float16
     x = t16(x_np).view(act_t)
     lg = torch.from_numpy(lg_np).to(dev)
@@ -573,6 +584,7 @@ def measure_workload(args, name, dev, world, rank, local):
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
         block["cpu_baseline"] = oracle_baseline(wl, spec, x_np, lg_np, 2, codes=codes)
+    block["dtype"] = "e4m3" if spec.act_fp8 else "f16"
     del layer, d_codes, d_suh, d_svh, d_sw, ws, flush, g, g_stage
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -605,11 +617,16 @@ def roofline(wl, spec, counts, T, k, stage_ms, has_shared):
     traffic = ncu_traffic(wl.name, dom)
     if gemm_path:
         tf = flops[dom] / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_tf,
-                "unit": "TFLOP/s", "frac": tf / bf16_tf, "traffic": traffic,
+        # FP8 products: the measured bf16 peak times the nominal fp8 : bf16
+        # ratio (4.5 : 2.25 PFLOP/s dense)
+        peak_tf = bf16_tf * (2.0 if spec.act_fp8 else 1.0)
+        roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": tf / peak_tf, "traffic": traffic,
                 "traffic_unit": "bytes per step of the stage's launches (ncu)",
                 "algorithmic_flops": flops[dom], "ms": dom_ms,
-                "peak_source": f"{src} (bf16_tflops burst; the fp16 dense rate equals bf16)",
+                "peak_source": (f"{src} bf16_tflops burst x 2 (nominal fp8 : bf16 dense ratio)"
+                                if spec.act_fp8 else
+                                f"{src} (bf16_tflops burst; the fp16 dense rate equals bf16)"),
                 "alu_view": alu_view}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": hbm_rate, "peak": hbm,

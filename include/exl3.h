@@ -99,6 +99,20 @@ typedef struct {
                                     Copied at create (which then allocates two small device
                                     tables, freed by exl3_layer_destroy).  NULL: K[p] for
                                     every expert. */
+    int act_fp8;                 /* 1: FP8 x FP8 products.  The activation operand of
+                                    every routed projection (x * suh for gate and up,
+                                    h * suh for down, after the rotation in format v2) is
+                                    quantised per row to E4M3: s = amax / 448 and
+                                    q = E4M3_RNE_sat(a / s), both divisions in IEEE fp32,
+                                    and the product is s * sum q * v; the tensor-core
+                                    path then multiplies E4M3 by E4M3 (tcgen05
+                                    kind::f8f6f4).  Requires fp8_round = 1 (the weight
+                                    operand is the E4M3 codebook value) ([p4] Widths: with
+                                    the E4M3 codebook the prefill runs on FP8 tensor
+                                    cores; the pages give no activation recipe, this is
+                                    the library's reading).  The dense shared expert is
+                                    not affected.  0: fp16 operands.  Other values, or 1
+                                    without fp8_round: EXL3_ERR_ARG. */
 } exl3_layer_desc;
 
 /* Validate `desc` and build a handle.  codes, suh, svh and shared_w must be
@@ -226,6 +240,17 @@ exl3_status exl3_layer_set_stage_events(exl3_layer_t *layer, void *const *events
  * host-side counter; launches captured into a CUDA graph count once, at
  * capture). */
 uint64_t exl3_launch_count(void);
+
+/* The per-row E4M3 quantisation of a layer with act_fp8 = 1, on its own:
+ * for each of `rows` rows of `n` fp32 values a (device, row-major), the row
+ * scale s = fp32(amax / 448) (0 for an all-zero row) and the E4M3 bytes
+ * q_i = E4M3_RNE_sat(fp32(a_i / s)) (0 when s = 0), the decisions the
+ * activation passes of the FP8 path take ([p4] Widths: FP8 tensor cores; the
+ * recipe is the library's reading).  q: device uint8 [rows][n]; s: device
+ * fp32 [rows].  Errors: EXL3_ERR_SHAPE for negative sizes, EXL3_ERR_ARG for
+ * null pointers, EXL3_ERR_CUDA for a failed launch. */
+exl3_status exl3_quantize_rows_e4m3(const float *a, int rows, int n, uint8_t *q, float *s,
+                                    void *stream);
 
 /* Test hook for the bounded waits of the tensor-core kernels (the pages have
  * no counterpart).  Every wait inside those kernels has a clock budget; when

@@ -31,7 +31,8 @@ class HostLayer:
         return oracle.Layer(s.num_experts, s.hidden, s.inter, s.K, self.codes, self.suh, self.svh,
                             fp8_round=s.fp8_round, shared_w=self.shared, hadamard=s.hadamard,
                             shared_coded=s.shared_coded,
-                            expert_K=np.array(s.expert_K, np.uint8) if s.expert_K else None)
+                            expert_K=np.array(s.expert_K, np.uint8) if s.expert_K else None,
+                            act_fp8=s.act_fp8)
 
     def device(self, mult: int = 0):
         import torch
@@ -43,7 +44,7 @@ class HostLayer:
         return Layer(self.dev["codes"], self.dev["suh"], self.dev["svh"], self.spec.K,
                      fp8_round=self.spec.fp8_round, mcg_mult=mult, shared=self.dev["shared"],
                      hadamard=self.spec.hadamard, shared_coded=self.spec.shared_coded,
-                     expert_K=self.spec.expert_K)
+                     expert_K=self.spec.expert_K, act_fp8=self.spec.act_fp8)
 
 
 def oracle_forward_parallel(olayer: oracle.Layer, x_bits, is_bf16, logits, top_k, tokens,

@@ -86,6 +86,13 @@ def test_layer_create_validation(L):
     d = _desc(E=1024)
     d.shared_coded = 1                                          # 1025 experts in the tables
     assert _create(L, d)[0] == _lib.EXL3_ERR_SHAPE
+    d = _desc()
+    d.act_fp8 = 2                                               # 0 or 1
+    d.fp8_round = 1
+    assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
+    d = _desc()
+    d.act_fp8 = 1                                               # FP8 operands need the E4M3 rule
+    assert _create(L, d)[0] == _lib.EXL3_ERR_ARG
 
 
 def test_route_validation_and_sizes(L):
@@ -124,6 +131,13 @@ def test_forward_validation_without_layer(L):
     assert L.exl3_rmsnorm(vp(4096), 1, 4, 250, 1e-6, vp(4096), None) == _lib.EXL3_ERR_SHAPE
     s = ctypes.c_int32()
     assert L.exl3_get_device_status(None, None, ctypes.byref(s)) == _lib.EXL3_ERR_ARG
+
+
+def test_quantize_rows_validation(L):
+    vp = ctypes.c_void_p
+    assert L.exl3_quantize_rows_e4m3(vp(4096), -1, 16, vp(4096), vp(4096), None) == _lib.EXL3_ERR_SHAPE
+    assert L.exl3_quantize_rows_e4m3(None, 2, 16, vp(4096), vp(4096), None) == _lib.EXL3_ERR_ARG
+    assert L.exl3_quantize_rows_e4m3(None, 0, 16, None, None, None) == _lib.EXL3_OK
 
 
 def test_wait_fault_hook_validation(L):

@@ -516,6 +516,91 @@ def test_forward_argument_errors_leave_output():
     assert not bool((out == 7.0).all())
 
 
+# ------------------------------------------------------------------ FP8 x FP8 operands
+
+
+@pytest.mark.parametrize("E,H,I,K,had,shared,sc,T,k,routing,path", [
+    (10, 384, 256, (2, 2, 3), False, True, False, 37, 4, "normal", 1),   # GEMV
+    (8, 512, 256, (4, 4, 4), True, False, True, 40, 4, "normal", 1),     # GEMV, v2, coded shared
+    (8, 512, 256, (3, 3, 4), False, False, False, 40, 4, "normal", 2),   # small tiles, M 64
+    (8, 512, 256, (4, 4, 2), False, True, False, 120, 4, "normal", 2),   # both small-tile widths
+    (8, 512, 256, (4, 4, 3), False, False, True, 700, 4, "zipf", 2),     # big + small tiles
+    (6, 384, 384, (2, 2, 2), False, False, False, 300, 4, "normal", 2),  # big tiles only
+    (8, 512, 256, (4, 4, 4), True, False, False, 700, 4, "zipf", 2),     # v2, big + small
+    (6, 512, 384, (3, 3, 4), True, False, False, 300, 4, "normal", 2),   # v2, big tiles only
+])
+def test_forward_act_fp8(E, H, I, K, had, shared, sc, T, k, routing, path):
+    """FP8 x FP8 products (every routed projection's activation row
+    quantised to E4M3 with an fp32 row scale): the tensor-core kernels on
+    kind::f8f6f4 with E4M3 weights, and the GEMV with the same operand
+    values, against the oracle in the same mode."""
+    spec = synth.LayerSpec(seed=190 + sum(K), num_experts=E, hidden=H, inter=I, K=K,
+                           fp8_round=True, hadamard=had, shared=shared, shared_coded=sc,
+                           act_fp8=True)
+    out, ref, layer = _run_small(spec, T, k, "bf16", path=path, routing=routing)
+    assert_layer_close(out, ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
+def _adversarial_rows(n=2048):
+    """Rows whose quotients a / s land on E4M3 rounding boundaries, just
+    beside them, and on E4M3 values, for exact and inexact row scales, plus
+    plain N(0, 1) rows at several magnitudes and an all-zero row."""
+    rng = np.random.default_rng(301)
+    e4 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    vals = np.unique(np.abs(e4[np.isfinite(e4)]))
+    mids = (vals[:-1] + vals[1:]) / 2.0                      # every rounding boundary
+    rows = []
+    for amax in (448.0, 1344.0, 1000.0, 0.37, 3.0e5):
+        s = np.float32(np.float32(amax) / np.float32(448.0))
+        targets = np.concatenate([mids, vals])
+        a = (targets.astype(np.float64) * np.float64(s)).astype(np.float32)
+        a = np.concatenate([a, np.nextafter(a, np.float32(np.inf)), np.nextafter(a, np.float32(0))])
+        a = np.concatenate([a, -a])
+        row = np.zeros(n, np.float32)
+        row[:a.size] = a[:n - 1]
+        row[n - 1] = np.float32(amax)                        # fixes the row's amax
+        rows.append(row)
+    for mag in (1e-3, 1.0, 7.0e4):
+        rows.append((rng.standard_normal(n) * mag).astype(np.float32))
+    rows.append(np.zeros(n, np.float32))
+    return np.stack(rows)
+
+
+def test_quantize_rows_e4m3_bit_exact():
+    """The FP8 path's per-row activation quantisation (s = amax / 448 and
+    q = E4M3(a / s), decided as IEEE fp32 divisions would) against the
+    oracle's, bit for bit, on rows built to put quotients on and beside every
+    E4M3 rounding boundary (where the kernel's reciprocal shortcut must fall
+    back to the division)."""
+    import ctypes
+
+    from trellis_quantized_moe_exl3_gb300 import _lib
+    a = _adversarial_rows()
+    R, n = a.shape
+    da = torch.from_numpy(a).cuda()
+    q = torch.empty((R, n), dtype=torch.uint8, device="cuda")
+    sc = torch.empty(R, dtype=torch.float32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    assert _lib.lib().exl3_quantize_rows_e4m3(p(da), R, n, p(q), p(sc), None) == 0
+    torch.cuda.synchronize()
+    qv = q.cpu().view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    s_gpu = sc.cpu().numpy()
+    for r in range(R):
+        amax = np.float32(np.abs(a[r]).max())
+        want_s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(0.0)
+        assert s_gpu[r] == want_s, (r, s_gpu[r], want_s)
+        got = qv[r] * np.float64(s_gpu[r])
+        ref = oracle.quantize_row_e4m3(a[r].astype(np.float64))
+        assert np.array_equal(got, ref), (r, int(np.sum(got != ref)))
+
+
+def test_prefill_workload_act_fp8_sampled():
+    """The prefill workload's layer (K4 with the E4M3 rule) with FP8 x FP8
+    products, full size, against the oracle in the same mode."""
+    _workload_parity("prefill", _prefill_tokens, act_fp8=True)
+
+
 # ------------------------------------------------------------------ bounded waits
 
 

@@ -30,7 +30,7 @@ class LayerDesc(ctypes.Structure):
         ("codes", ctypes.c_void_p * 3), ("suh", ctypes.c_void_p * 3),
         ("svh", ctypes.c_void_p * 3), ("shared_w", ctypes.c_void_p * 3),
         ("hadamard", ctypes.c_int), ("shared_coded", ctypes.c_int),
-        ("expert_K", ctypes.c_void_p),
+        ("expert_K", ctypes.c_void_p), ("act_fp8", ctypes.c_int),
     ]
 
 
@@ -85,6 +85,8 @@ def lib():
     L.exl3_layer_set_stage_events.restype = i
     L.exl3_launch_count.argtypes = []
     L.exl3_launch_count.restype = ctypes.c_uint64
+    L.exl3_quantize_rows_e4m3.argtypes = [vp, i, i, vp, vp, vp]
+    L.exl3_quantize_rows_e4m3.restype = i
     L.exl3_test_set_wait_fault.argtypes = [i, i, ctypes.c_longlong]
     L.exl3_test_set_wait_fault.restype = i
     L.exl3_status_string.argtypes = [i]

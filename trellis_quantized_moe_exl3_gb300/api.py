@@ -52,12 +52,14 @@ class Layer:
     the arrays is a trellis-coded shared expert (weight 1 for every token);
     the router then has E - 1 columns.  expert_K ([E][3] ints): a width per
     expert and projection; codes[p] is then a flat tensor of the experts'
-    codes back to back (K is ignored).  The tensors must stay alive as long
-    as the layer.
+    codes back to back (K is ignored).  act_fp8: FP8 x FP8 products (every
+    routed projection's activation row quantised to E4M3 with an fp32 row
+    scale; requires fp8_round).  The tensors must stay alive as long as the
+    layer.
     """
 
     def __init__(self, codes, suh, svh, K, fp8_round=False, mcg_mult=0, shared=None,
-                 hadamard=False, shared_coded=False, expert_K=None):
+                 hadamard=False, shared_coded=False, expert_K=None, act_fp8=False):
         E, H = suh[0].shape
         I = svh[0].shape[1]
         E -= int(bool(shared_coded))  # routed experts
@@ -86,6 +88,7 @@ class Layer:
         d.hadamard = int(bool(hadamard))
         d.shared_coded = int(bool(shared_coded))
         d.expert_K = self._ek.ctypes.data if self._ek is not None else None
+        d.act_fp8 = int(bool(act_fp8))
         h = ctypes.c_void_p()
         check(_lib.lib().exl3_layer_create(ctypes.byref(d), ctypes.byref(h)), "exl3_layer_create")
         self._h = h

@@ -158,6 +158,52 @@ __device__ __forceinline__ uint32_t e4m3_round2(uint32_t v2) {
   return back;
 }
 
+// The E4M3 rule on two fp16 values, kept as the two E4M3 bytes (low byte =
+// the low fp16 value): the weight operand of the FP8 tensor-core path.
+__device__ __forceinline__ uint32_t e4m3_bytes2(uint32_t v2) {
+  uint16_t f8;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(f8) : "r"(v2));
+  return f8;
+}
+
+// Two fp32 values to E4M3 (RNE, satfinite) bytes: lo -> low byte, hi -> high byte.
+__device__ __forceinline__ uint32_t e4m3_pack2(float lo, float hi) {
+  uint16_t f8;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(f8) : "f"(hi), "f"(lo));
+  return f8;
+}
+
+// Per-row E4M3 activation operand (the FP8 x FP8 product's activations):
+// s = amax / 448 and q = E4M3_RNE_sat(a / s), both divisions IEEE fp32 (the
+// precision in which the quantised code is decided); an all-zero row has
+// s = 0 and q = 0.
+__device__ __forceinline__ float e4m3_row_scale(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 0.0f;
+}
+
+// E4M3 byte of a / s for one element, with r = 1 / s (correctly rounded,
+// taken once per row).  p = a * r is within 2.5 fp32 ulps of the correctly
+// rounded quotient Q = fp32(a / s) (r and the product each round once), so Q
+// lies between the values 4 ulps below and above |p|.  E4M3 rounding is
+// monotonic: when both of those round to the same byte, Q does too, and that
+// byte is the decision an IEEE division would give.  Only a quotient within
+// a few ulps of an E4M3 rounding boundary takes the IEEE division.
+__device__ __forceinline__ uint32_t e4m3_byte_of(float a, float s, float r) {
+  if (!(s > 0.0f)) return 0u;
+  const uint32_t m = __float_as_uint(a * r) & 0x7FFFFFFFu;
+  const uint32_t two = e4m3_pack2(__uint_as_float(m > 4u ? m - 4u : 0u), __uint_as_float(m + 4u));
+  uint32_t b = two & 0xFFu;
+  if (b != (two >> 8)) b = e4m3_pack2(fabsf(__fdiv_rn(a, s)), 0.0f) & 0xFFu;
+  return b | (a < 0.0f ? 0x80u : 0u);
+}
+
+// The same element as a float (every E4M3 value is exact in fp16 and fp32).
+__device__ __forceinline__ float e4m3_value(float a, float s, float r) {
+  uint32_t back;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"((uint16_t)e4m3_byte_of(a, s, r)));
+  return __half2float(__ushort_as_half((unsigned short)(back & 0xFFFFu)));
+}
+
 // Load a quad lane's 8K bytes from global memory (read once: no L1 allocate)
 // and fetch the neighbour's first word with a shuffle inside the quad.
 template <int K>

@@ -101,6 +101,8 @@ struct LayerView {
   const uint16_t* shared_w[3];
   size_t code_stride[3];  // uint16 words per expert
   int had;                // format v2: Hadamard rotation on both sides of each projection
+  int act8;               // FP8 operand mode: every projection's activation row is
+                          // quantised to E4M3 with an fp32 row scale (requires fp8)
   int sc;                 // 1: expert E - 1 of the arrays is the coded shared expert
                           // (E counts it; the logits have E - sc columns)
   // Mixed widths (a width per expert and projection, or gate and up of
@@ -145,7 +147,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
                             cudaStream_t st);
 
 // ---- grouped GEMM path (prefill-sized steps, tcgen05)
-size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had);
+size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had, int act8);
 // ev (may be null): events after gather [2], gate/up [3], down input [4], down [5].
 // *r_out receives the pair-row buffer [P][H] the combine reads.
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,

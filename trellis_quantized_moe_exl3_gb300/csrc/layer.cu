@@ -72,7 +72,7 @@ FwdLayout fwd_layout(const LayerView& L, int has_shared, int T, int k_routed) {
   f.off = o; o += al((size_t)(L.E + 1) * 4);
   f.pairs = o; o += al(P * 4);
   const size_t gv = gemv_scratch_bytes(T, k, L.E, L.H, L.I);
-  const size_t gm = gemm_scratch_bytes(T, k, L.E, L.H, L.I, L.had);
+  const size_t gm = gemm_scratch_bytes(T, k, L.E, L.H, L.I, L.had, L.act8);
   f.gemv = o; o += al(gv > gm ? gv : gm);
   f.shared = o; o += has_shared ? al(shared_scratch_bytes(T, L.H, L.I)) : 0;
   f.total = o;
@@ -114,6 +114,8 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   if (!(mult & 1u)) return EXL3_ERR_ARG;
   int nshared = 0;
   if (d->hadamard != 0 && d->hadamard != 1) return EXL3_ERR_ARG;
+  if (d->act_fp8 != 0 && d->act_fp8 != 1) return EXL3_ERR_ARG;
+  if (d->act_fp8 && !d->fp8_round) return EXL3_ERR_ARG;
   if (n_coded > kMaxExperts) return EXL3_ERR_SHAPE;
   for (int p = 0; p < 3; p++) {
     if (!d->codes[p] || !d->suh[p] || !d->svh[p]) return EXL3_ERR_ARG;
@@ -134,6 +136,7 @@ exl3_status exl3_layer_create(const exl3_layer_desc* d, exl3_layer_t** out) {
   v.fp8 = d->fp8_round ? 1 : 0;
   v.mult = mult;
   v.had = d->hadamard;
+  v.act8 = d->act_fp8;
   for (int p = 0; p < 3; p++) {
     v.K[p] = d->expert_K ? d->expert_K[p] : d->K[p];
     v.codes[p] = d->codes[p];

@@ -43,16 +43,29 @@ namespace {
 
 constexpr int kHalfN = 256;           // tokens per TMEM accumulator (MMA N)
 constexpr int kBN = 2 * kHalfN;       // tokens per tile
-constexpr int kKS = 64;               // inputs per K step
-constexpr int kDec = 12;              // decoder warps
-constexpr int kThreads = (kDec + 2) * 32;
-constexpr int kJobs = 4;              // 16-input blocks per K step
-constexpr int kPar = kDec / kJobs;    // K steps decoded in parallel
+constexpr int kRow = 128;             // bytes of one K step of a K-major operand row
 constexpr int kAStages = 5;           // A ring: decoders up to 5 K steps ahead
-constexpr int kAStage = 128 * kKS * 2;        // 16 KB
-constexpr int kBox = 64 * kKS * 2;            // one TMA box: 64 tokens x 64 inputs, 8 KB
+constexpr int kAStage = 128 * kRow;           // 16 KB: 128 outputs x one K step
+constexpr int kBox = 64 * kRow;               // one TMA box: 64 tokens x one K step, 8 KB
 constexpr int kBStages = 2;
-constexpr int kBStage = kBN * kKS * 2;        // 64 KB
+constexpr int kBStage = kBN * kRow;           // 64 KB
+constexpr int kSDec = 16;                     // decoder warps of the small-tile kernel
+
+// Operand element type of the tensor-core kernels: fp16 (kind::f16) or E4M3
+// (kind::f8f6f4, the FP8 x FP8 product).  A K step is one 128-byte row of a
+// K-major operand either way (64 fp16 or 128 E4M3 inputs), so every stage,
+// box and descriptor offset in bytes is the same for both.
+template <int OP8>
+struct OpT {
+  static constexpr int kKS = OP8 ? 128 : 64;           // inputs per K step
+  static constexpr int kBlk = 16 * 128 * (OP8 ? 1 : 2);  // one 16-input block of a 128-output tile
+  static constexpr int kJobs = kKS / 16;               // 16-input blocks per K step
+  static constexpr int kDec = OP8 ? 8 : 12;            // decoder warps (big tiles)
+  static constexpr int kPar = kDec / kJobs;            // K steps decoded in parallel
+  static constexpr int kThreads = (kDec + 2) * 32;
+  static constexpr int kSJobs = 2 * kJobs;             // small tiles: blocks x 2 code strips
+  static constexpr int kSPar = kSDec / kSJobs;
+};
 
 template <int K>
 struct GCfg {
@@ -250,10 +263,50 @@ __device__ __forceinline__ void decode_store(const LaneWords<K>& lw, uint32_t mu
     *reinterpret_cast<uint4*>(a_blk + off[idx]) = make_uint4(v[idx][0], v[idx][1], v[idx][2], v[idx][3]);
 }
 
-template <int K, int FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+// FP8 operand variant: the lane's 64 weights as E4M3 bytes (the codebook
+// value under the E4M3 rule; suh is on the activation side), in four 16-byte
+// chunks of the 1-byte MN-major stage, one per input column c + 4jh + 8hf,
+// each holding the lane's 16 output rows in order.  off[2hf + jh] is the
+// chunk's swizzled byte offset.
+template <int K>
+__device__ __forceinline__ void decode_store8(const LaneWords<K>& lw, uint32_t mult,
+                                              uint32_t neg16, uint8_t* a_blk,
+                                              const int (&off)[4]) {
+  const McgConsts mc = mcg_consts();
+  uint32_t f[8][4];  // [4hf + 2jh + jl][PP]: E4M3 bytes of rows 2PP + 8jl, 2PP + 1 + 8jl
+  uint32_t xp[16 + (K == 3 ? 0 : 16 / K)];
+  uint32_t m[16];
+#define EXL3_PP8(PP)                                                           \
+  halves16<K, PP>(lw, mult, neg16, mc, xp, m);                                 \
+  _Pragma("unroll") for (int idx = 0; idx < 8; idx++)                         \
+      f[idx][PP] = e4m3_bytes2(sum_halves2(m[idx], m[idx + 8]));
+  EXL3_PP8(0)
+  EXL3_PP8(1)
+  EXL3_PP8(2)
+  EXL3_PP8(3)
+#undef EXL3_PP8
+#pragma unroll
+  for (int c4 = 0; c4 < 4; c4++) {
+    const int i0 = 2 * c4, i1 = 2 * c4 + 1;  // row groups jl = 0 (rows 0..7), 1 (rows 8..15)
+    *reinterpret_cast<uint4*>(a_blk + off[c4]) =
+        make_uint4(__byte_perm(f[i0][0], f[i0][1], 0x5410), __byte_perm(f[i0][2], f[i0][3], 0x5410),
+                   __byte_perm(f[i1][0], f[i1][1], 0x5410), __byte_perm(f[i1][2], f[i1][3], 0x5410));
+  }
+}
+
+// Lane-to-tile map of the FP8 decoders: each quarter warp holds tiles g and
+// g ^ 4, whose 16-byte chunks (chunk index g ^ row) fall in 8 different
+// 16-byte bank groups of the 1-byte stage.
+__device__ __forceinline__ int dec_tile8(int lane) {
+  return ((lane >> 3) & 3) | (((lane >> 2) & 1) << 2);
+}
+
+template <int K, int FP8, int OP8>
+__global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, GemmParams p) {
   using C = GCfg<K>;
+  using T = OpT<OP8>;
+  constexpr int kDec = T::kDec, kJobs = T::kJobs, kPar = T::kPar, kKS = T::kKS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -352,7 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id1 = umma_idesc_f16(128, n1 > 0 ? n1 : 16, 1, 0);
       // descriptor address fields are byte addresses >> 4 (no carry below
       // 256 KB), so stage and K-slice offsets are plain additions
-      const uint64_t a_desc0 = umma_desc(smem_u32(smem), 1024, 2048);
+      // A (decoded weights, MN-major): fp16 rows hold 64 outputs (two atoms
+      // 1024 B apart, 8-input groups 2048 B apart); E4M3 rows hold all 128
+      // (one atom, 8-input groups 1024 B apart)
+      const uint64_t a_desc0 = umma_desc(smem_u32(smem), 1024, OP8 ? 1024 : 2048);
       const uint64_t b_desc0 = umma_desc(smem_u32(b_ring), 16, 1024);
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
@@ -363,12 +419,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ad = a_desc0 + (uint64_t)(sa * (kAStage >> 4));
         const uint64_t bd = b_desc0 + (uint64_t)(sb * (bstage >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kKS / 16; kk++) {
+        for (int kk = 0; kk < 4; kk++) {  // K slices of 32 bytes
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
-          umma_f16(tmem, ad + kk * (4096 >> 4), bd + kk * (32 >> 4), id0, acc);
-          if (n1 > 0)
-            umma_f16(tmem + kHalfN, ad + kk * (4096 >> 4),
-                     bd + ((kHalfN * 128) >> 4) + kk * (32 >> 4), id1, acc);
+          if (OP8) {
+            umma_e4m3(tmem, ad + kk * (4096 >> 4), bd + kk * (32 >> 4), id0, acc);
+            if (n1 > 0)
+              umma_e4m3(tmem + kHalfN, ad + kk * (4096 >> 4),
+                        bd + ((kHalfN * 128) >> 4) + kk * (32 >> 4), id1, acc);
+          } else {
+            umma_f16(tmem, ad + kk * (4096 >> 4), bd + kk * (32 >> 4), id0, acc);
+            if (n1 > 0)
+              umma_f16(tmem + kHalfN, ad + kk * (4096 >> 4),
+                       bd + ((kHalfN * 128) >> 4) + kk * (32 >> 4), id1, acc);
+          }
         }
         umma_commit(&a_empty[sa]);
         umma_commit(&b_empty[sb]);
@@ -389,24 +452,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- decode
     const int blk = warp % kJobs;
     const int ks0 = warp / kJobs;
-    const int g = dec_tile(lane), c = lane & 3;
+    const int g = OP8 ? dec_tile8(lane) : dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
                            (size_t)8 * s * 32 * K;
     const int n_my = (nks - ks0 + kPar - 1) / kPar;
-    // lane-constant swizzled offsets of this lane's 8 output chunks in a block
-    int off[8];
+    // lane-constant swizzled offsets of this lane's output chunks in a block:
+    // fp16, 8 chunks of 8 outputs (input c + 4jh + 8hf, rows 8jl..8jl+7);
+    // E4M3, 4 chunks of 16 outputs (input c + 4jh + 8hf)
+    int off[8], off8[4];
 #pragma unroll
     for (int idx = 0; idx < 8; idx++) {
       const int hf = idx >> 2, jh = (idx >> 1) & 1, jl = idx & 1;
       const int kr = c + 4 * jh;  // input row inside its 8-row K group
       off[idx] = (g >> 2) * 1024 + hf * 2048 + kr * 128 + (((2 * (g & 3) + jl) ^ kr) << 4);
     }
+#pragma unroll
+    for (int c4 = 0; c4 < 4; c4++) {
+      const int hf = c4 >> 1, kr = c + 4 * (c4 & 1);
+      off8[c4] = hf * 1024 + kr * 128 + ((g ^ kr) << 4);
+    }
     const uint32_t neg16 = opaque_u32(0xFFFF0000u);
     // this lane's 8K code bytes of job n (code lane `lane` of the 8-tile chunk)
     auto lane_codes = [&](int n) {
       const int ks = ks0 + n * kPar;
-      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
+      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * kJobs + blk) * row_bytes) +
              (g * 4 + c) * 4 * K;
     };
     // code rows are pulled into L2 kL2Ahead jobs ahead, so the register
@@ -415,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch_l2 = [&](int n) {
       if (n < n_my && lane * 128 < C::kCodeChunk) {
         const int ks = ks0 + n * kPar;
-        const uint8_t* a = cbase + (size_t)(ks * 4 + blk) * row_bytes + lane * 128;
+        const uint8_t* a = cbase + (size_t)(ks * kJobs + blk) * row_bytes + lane * 128;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
       }
     };
@@ -426,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_suh = [&](int n) {
       const int ks = ks0 + n * kPar;
 #pragma unroll
-      for (int q = 0; q < 4; q++)  // format v2: suh is on the activation side
-        s2n[q] = p.had ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+      for (int q = 0; q < 4; q++)  // format v2, FP8 operands: suh is on the activation side
+        s2n[q] = p.had || OP8 ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
     };
     LaneWords<K> nxt;
     if (n_my > 0) {
@@ -447,7 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n + 1 < n_my) load_suh(n + 1);
       fetch_neighbour<K>(lw);
       if (!__all_sync(0xffffffffu, pipe_wait(&a_empty[sa], pa ^ 1, p, abort_flag))) break;
-      decode_store<K, FP8>(lw, p.mult, neg16, smem + sa * kAStage + blk * 4096, off, s2);
+      if (OP8)
+        decode_store8<K>(lw, p.mult, neg16, smem + sa * kAStage + blk * T::kBlk, off8);
+      else
+        decode_store<K, FP8>(lw, p.mult, neg16, smem + sa * kAStage + blk * T::kBlk, off, s2);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
@@ -525,14 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (M 128); column = output.
 constexpr int kSN = 256;                       // outputs per CTA (MMA N)
 constexpr int kSM = 128;                       // tokens at most (MMA M 64 or 128)
-constexpr int kSDec = 16;                      // decoder warps
-constexpr int kSThreads = (kSDec + 2) * 32;
-constexpr int kSJobs = 8;                      // jobs per K step: 4 blocks x 2 strips
-constexpr int kSPar = kSDec / kSJobs;          // K steps decoded in parallel
+constexpr int kSThreads = (kSDec + 2) * 32;    // kSDec decoder warps, TMA, MMA
 constexpr int kSWStages = 5;                   // decoded-weight stages
-constexpr int kSWStage = kSN * kKS * 2;        // 32 KB
+constexpr int kSWStage = kSN * kRow;           // 32 KB
 constexpr int kSXStages = 4;                   // activation stages
-constexpr int kSXStage = kSM * kKS * 2;        // 16 KB (M 64 uses the first half)
+constexpr int kSXStage = kSM * kRow;           // 16 KB (M 64 uses the first half)
 
 struct SCfg {
   static constexpr int kOffX = kSWStages * kSWStage;
@@ -543,9 +613,11 @@ struct SCfg {
 };
 static_assert(SCfg::kSmem <= 227 * 1024, "small-tile kernel shared memory");
 
-template <int K, int FP8>
+template <int K, int FP8, int OP8>
 __global__ void __launch_bounds__(kSThreads, 1)
     gemm64_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmParams p) {
+  using T = OpT<OP8>;
+  constexpr int kSJobs = T::kSJobs, kSPar = T::kSPar, kKS = T::kKS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -638,7 +710,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // groups 4096 B apart, K slice of 16 = +8192 B)
       const uint32_t idesc = umma_idesc_f16(tm, kSN, 0, 1);
       const uint64_t x_desc0 = umma_desc(smem_u32(x_ring), 16, 1024);
-      const uint64_t w_desc0 = umma_desc(smem_u32(smem), 1024, 4096);
+      // E4M3 rows hold 128 outputs: two atoms, 8-input groups 2048 B apart
+      const uint64_t w_desc0 = umma_desc(smem_u32(smem), 1024, OP8 ? 2048 : 4096);
       int sw = 0, sx = 0;
       uint32_t pw = 0, px = 0;
       for (int ks = 0; ks < nks; ks++) {
@@ -648,9 +721,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const uint64_t xd = x_desc0 + (uint64_t)(sx * (kSXStage >> 4));
         const uint64_t wd = w_desc0 + (uint64_t)(sw * (kSWStage >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kKS / 16; kk++)
-          umma_f16(tmem, xd + kk * (32 >> 4), wd + kk * (8192 >> 4), idesc,
-                   (ks > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; kk++) {  // K slices of 32 bytes
+          if (OP8)
+            umma_e4m3(tmem, xd + kk * (32 >> 4), wd + kk * (8192 >> 4), idesc,
+                      (ks > 0 || kk > 0) ? 1u : 0u);
+          else
+            umma_f16(tmem, xd + kk * (32 >> 4), wd + kk * (8192 >> 4), idesc,
+                     (ks > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&w_empty[sw]);
         umma_commit(&x_empty[sx]);
         if (++sw == kSWStages) {
@@ -666,35 +744,42 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- decode
-    // warp w: 16-input block w % 4 of code strip 2s + (w / 4) % 2, K steps
-    // ks = w / 8 (mod 2)
-    const int blk = warp % 4;
-    const int half = (warp / 4) % 2;
+    // warp w: 16-input block w % J of code strip 2s + (w / J) % 2, K steps
+    // ks = w / 2J (mod kSPar), J = blocks per K step
+    const int blk = warp % T::kJobs;
+    const int half = (warp / T::kJobs) % 2;
     const int ks0 = warp / kSJobs;
-    const int g = dec_tile(lane), c = lane & 3;
+    const int g = OP8 ? dec_tile8(lane) : dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
                            (size_t)8 * (2 * s + half) * 32 * K;
     const int n_my = (nks - ks0 + kSPar - 1) / kSPar;
-    int off[8];
+    int off[8], off8[4];
 #pragma unroll
     for (int idx = 0; idx < 8; idx++) {
       const int hf = idx >> 2, jh = (idx >> 1) & 1, jl = idx & 1;
       const int kr = c + 4 * jh;
       off[idx] = (g >> 2) * 1024 + hf * 4096 + kr * 128 + (((2 * (g & 3) + jl) ^ kr) << 4);
     }
-    const int job_off = blk * 8192 + half * 2048;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; c4++) {
+      const int hf = c4 >> 1, kr = c + 4 * (c4 & 1);
+      off8[c4] = hf * 2048 + kr * 128 + ((g ^ kr) << 4);
+    }
+    // a block of 16 inputs spans two 8-input groups; a code strip is one
+    // (E4M3) or two (fp16) 1024-byte atoms wide
+    const int job_off = OP8 ? blk * 4096 + half * 1024 : blk * 8192 + half * 2048;
     const uint32_t neg16 = opaque_u32(0xFFFF0000u);
     auto lane_codes = [&](int n) {
       const int ks = ks0 + n * kSPar;
-      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * 4 + blk) * row_bytes) +
+      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * T::kJobs + blk) * row_bytes) +
              (g * 4 + c) * 4 * K;
     };
     constexpr int kL2Ahead = 8;
     auto prefetch_l2 = [&](int n) {
       if (n < n_my && lane * 128 < 8 * 32 * K) {
         const int ks = ks0 + n * kSPar;
-        const uint8_t* a = cbase + (size_t)(ks * 4 + blk) * row_bytes + lane * 128;
+        const uint8_t* a = cbase + (size_t)(ks * T::kJobs + blk) * row_bytes + lane * 128;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
       }
     };
@@ -704,8 +789,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     auto load_suh = [&](int n) {
       const int ks = ks0 + n * kSPar;
 #pragma unroll
-      for (int q = 0; q < 4; q++)  // format v2: suh is on the activation side
-        s2n[q] = p.had ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+      for (int q = 0; q < 4; q++)  // format v2, FP8 operands: suh is on the activation side
+        s2n[q] = p.had || OP8 ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
     };
     LaneWords<K> nxt;
     if (n_my > 0) {
@@ -724,7 +809,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (n + 1 < n_my) load_suh(n + 1);
       fetch_neighbour<K>(lw);
       if (!__all_sync(0xffffffffu, pipe_wait(&w_empty[sw], pw ^ 1, p, abort_flag))) break;
-      decode_store<K, FP8>(lw, p.mult, neg16, smem + sw * kSWStage + job_off, off, s2);
+      if (OP8)
+        decode_store8<K>(lw, p.mult, neg16, smem + sw * kSWStage + job_off, off8);
+      else
+        decode_store<K, FP8>(lw, p.mult, neg16, smem + sw * kSWStage + job_off, off, s2);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&w_full[sw]);
@@ -904,20 +992,27 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
   if (lane == 0) xinv[pos] = ldexpf(1.0f, -ex);
 }
 
-// Format v2: rows x * suh of gate and up for each position, each 128-input
-// block rotated, fp16 with a power-of-two scale per row that also removes the
-// rotations' factor 128: gate rows at [pos], up rows at [P + pos].  One warp
-// per position; lane l holds inputs 8v .. 8v + 7 of vector v = 32 i + l, so a
+// Rows x * suh of gate and up for each position (gate rows at [pos], up rows
+// at [P + pos]), for the layers whose suh cannot fold into the decoded
+// weights: format v2 (ROT: each 128-input block rotated; the rotation sits
+// between suh and the codes) and the FP8 operand mode (ACT8).  One warp per
+// position; lane l holds inputs 8v .. 8v + 7 of vector v = 32 i + l, so a
 // 128-block is 16 consecutive lanes (3 index bits in registers, 4 by
 // shuffles; H is a multiple of 128, so both half-warps are active or idle
-// together).  The scale comes from a bound instead of the rotated values: an
-// entry of a rotated block is at most the block's L1 norm, so the first pass
-// needs no rotation (the power-of-two scale only has to keep fp16 finite; it
-// does not change the relative rounding of normal fp16 values).
-__global__ void __launch_bounds__(kRowWarps * 32) gather_rows_had_kernel(
+// together).
+//   ACT8 = 0: fp16 rows with a power-of-two scale per row that also removes
+//     the rotations' factor 128.  The scale comes from a bound instead of the
+//     rotated values: an entry of a rotated block is at most the block's L1
+//     norm, so the first pass needs no rotation (the power-of-two scale only
+//     has to keep fp16 finite; it does not change the relative rounding of
+//     normal fp16 values).
+//   ACT8 = 1: E4M3 bytes q = E4M3(a / s), s = amax / 448 over the exact
+//     (rotated) row, the row's scale s (times 2^-7 with the rotation).
+template <int ROT, int ACT8>
+__global__ void __launch_bounds__(kRowWarps * 32) gather_rows_split_kernel(
     const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
     const int32_t* ids, const uint16_t* __restrict__ suh_g, const uint16_t* __restrict__ suh_u,
-    uint16_t* __restrict__ xg, float* __restrict__ xinv) {
+    void* __restrict__ xg, float* __restrict__ xinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -940,43 +1035,78 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_had_kernel(
       fu[q] = fx[q] * b[q];
     }
   };
-  // pass 1: the largest block L1 norm of each row
+  auto rows = [&](int v, float (&fg)[8], float (&fu)[8]) {
+    prods(v, fg, fu);
+    if (ROT) {
+      wht_regs(fg);
+      wht_regs(fu);
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+          fg[q] = wht_lane(fg[q], m, hm);
+          fu[q] = wht_lane(fu[q], m, hm);
+        }
+    }
+  };
+  // pass 1: the largest magnitude (ACT8) or the largest block L1 norm
   float ag = 0.0f, au = 0.0f;
   for (int v = lane; v < nv; v += 32) {
     float fg[8], fu[8];
-    prods(v, fg, fu);
-    float lg = 0.0f, lu = 0.0f;
+    if (ACT8) {
+      rows(v, fg, fu);
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
-      lg += fabsf(fg[q]);
-      lu += fabsf(fu[q]);
-    }
+      for (int q = 0; q < 8; q++) {
+        ag = fmaxf(ag, fabsf(fg[q]));
+        au = fmaxf(au, fabsf(fu[q]));
+      }
+    } else {
+      prods(v, fg, fu);
+      float lg = 0.0f, lu = 0.0f;
 #pragma unroll
-    for (int m = 1; m < 16; m <<= 1) {
-      lg += __shfl_xor_sync(hm, lg, m);
-      lu += __shfl_xor_sync(hm, lu, m);
+      for (int q = 0; q < 8; q++) {
+        lg += fabsf(fg[q]);
+        lu += fabsf(fu[q]);
+      }
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1) {
+        lg += __shfl_xor_sync(hm, lg, m);
+        lu += __shfl_xor_sync(hm, lu, m);
+      }
+      ag = fmaxf(ag, lg);
+      au = fmaxf(au, lu);
     }
-    ag = fmaxf(ag, lg);
-    au = fmaxf(au, lu);
   }
   ag = warp_max(ag);
   au = warp_max(au);
-  auto rows = [&](int v, float (&fg)[8], float (&fu)[8]) {
-    prods(v, fg, fu);
-    wht_regs(fg);
-    wht_regs(fu);
+  const int hs = ROT ? kHadShift : 0;  // the unnormalized rotations' 128
+  if (ACT8) {
+    const float s_g = e4m3_row_scale(ag), s_u = e4m3_row_scale(au);
+    const float r_g = s_g > 0.0f ? __frcp_rn(s_g) : 0.0f, r_u = s_u > 0.0f ? __frcp_rn(s_u) : 0.0f;
+    uint2* dg = reinterpret_cast<uint2*>(static_cast<uint8_t*>(xg) + (size_t)pos * H);
+    uint2* du = reinterpret_cast<uint2*>(static_cast<uint8_t*>(xg) + ((size_t)P + pos) * H);
+    auto q8 = [](const float (&f)[8], float sc, float rc) {
+      uint32_t w[2] = {0u, 0u};
 #pragma unroll
-    for (int m = 1; m < 16; m <<= 1)
-#pragma unroll
-      for (int q = 0; q < 8; q++) {
-        fg[q] = wht_lane(fg[q], m, hm);
-        fu[q] = wht_lane(fu[q], m, hm);
-      }
-  };
+      for (int i = 0; i < 8; i++) w[i >> 2] |= e4m3_byte_of(f[i], sc, rc) << (8 * (i & 3));
+      return make_uint2(w[0], w[1]);
+    };
+    for (int v = lane; v < nv; v += 32) {
+      float fg[8], fu[8];
+      rows(v, fg, fu);
+      dg[v] = q8(fg, s_g, r_g);
+      du[v] = q8(fu, s_u, r_u);
+    }
+    if (lane == 0) {
+      xinv[pos] = ldexpf(s_g, -hs);
+      xinv[(size_t)P + pos] = ldexpf(s_u, -hs);
+    }
+    return;
+  }
   const int eg = fp16_scale_exp(ag), eu = fp16_scale_exp(au);
   const float scg = ldexpf(1.0f, eg), scu = ldexpf(1.0f, eu);
-  uint4* dg = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
-  uint4* du = reinterpret_cast<uint4*>(xg + ((size_t)P + pos) * H);
+  uint4* dg = reinterpret_cast<uint4*>(static_cast<uint16_t*>(xg) + (size_t)pos * H);
+  uint4* du = reinterpret_cast<uint4*>(static_cast<uint16_t*>(xg) + ((size_t)P + pos) * H);
   for (int v = lane; v < nv; v += 32) {
     float fg[8], fu[8];
     rows(v, fg, fu);
@@ -986,20 +1116,24 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_had_kernel(
                        pack_h2(fu[4] * scu, fu[5] * scu), pack_h2(fu[6] * scu, fu[7] * scu));
   }
   if (lane == 0) {
-    xinv[pos] = ldexpf(1.0f, -eg - kHadShift);
-    xinv[(size_t)P + pos] = ldexpf(1.0f, -eu - kHadShift);
+    xinv[pos] = ldexpf(1.0f, -eg - hs);
+    xinv[(size_t)P + pos] = ldexpf(1.0f, -eu - hs);
   }
 }
 
-// h = silu(g) * u per position row, as fp16 with a power-of-two row scale
-// (format v1: suh of down is applied on the weight side by the decoder).
-// Format v2 (suh_d non-null): h * suh_d of the position's expert, each
-// 128-block rotated (lane l holds elements 4v .. 4v + 3 of v = 32 i + l: 2
-// index bits in registers, 5 by shuffles), the scale also removing the
-// factor 128.  I is a multiple of 128.
+// h = silu(g) * u per position row, the down projection's activation rows.
+// Format v1 with fp16 operands: h itself (suh of down is applied on the
+// weight side by the decoders), fp16 with a power-of-two row scale.  With
+// the rotation (ROT, format v2) or FP8 operands (ACT8), h * suh_d of the
+// position's expert (ROT: each 128-block rotated; lane l holds elements
+// 4v .. 4v + 3 of v = 32 i + l: 2 index bits in registers, 5 by shuffles; I
+// is a multiple of 128), the scale also removing the factor 128 of the
+// rotations.  ACT8 stores E4M3 bytes q = E4M3(a / s), s = amax / 448, and
+// the row scale s.
+template <int ROT, int ACT8>
 __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     const float* __restrict__ gu, size_t n_pos, int I, const int32_t* seg_pairs,
-    const int32_t* ids, const uint16_t* __restrict__ suh_d, uint16_t* __restrict__ hs,
+    const int32_t* ids, const uint16_t* __restrict__ suh_d, void* __restrict__ hs,
     float* __restrict__ hinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -1007,29 +1141,31 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
   if (pos >= n_pos) return;
   const float4* gr = reinterpret_cast<const float4*>(gu + pos * I);
   const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
-  uint2* dst = reinterpret_cast<uint2*>(hs + pos * I);
   const int nv = I / 4;
-  const uint2* sd = suh_d ? reinterpret_cast<const uint2*>(suh_d + (size_t)ids[seg_pairs[pos]] * I)
+  constexpr bool kSide = ROT || ACT8;
+  const uint2* sd = kSide ? reinterpret_cast<const uint2*>(suh_d + (size_t)ids[seg_pairs[pos]] * I)
                           : nullptr;
-  // format v2: times suh_d, then rotated (every lane active: nv % 32 == 0)
-  auto rot = [&](float4& h, int v) {
+  // times suh_d, then (ROT) rotated (every lane active: nv % 32 == 0)
+  auto side = [&](float4& h, int v) {
     const uint2 sr = __ldg(sd + v);
     float w[4] = {h.x * __half2float(__ushort_as_half((unsigned short)(sr.x & 0xFFFFu))),
                   h.y * __half2float(__ushort_as_half((unsigned short)(sr.x >> 16))),
                   h.z * __half2float(__ushort_as_half((unsigned short)(sr.y & 0xFFFFu))),
                   h.w * __half2float(__ushort_as_half((unsigned short)(sr.y >> 16)))};
-    wht_regs(w);
+    if (ROT) {
+      wht_regs(w);
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1)
+      for (int m = 1; m < 32; m <<= 1)
 #pragma unroll
-      for (int q = 0; q < 4; q++) w[q] = wht_lane(w[q], m, 0xffffffffu);
+        for (int q = 0; q < 4; q++) w[q] = wht_lane(w[q], m, 0xffffffffu);
+    }
     h = make_float4(w[0], w[1], w[2], w[3]);
   };
   auto h4 = [&](int v) {
     const float4 g = __ldcs(gr + v), u = __ldcs(ur + v);
     float4 h = make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z,
                            silu_f(g.w) * u.w);
-    if (sd) rot(h, v);
+    if (kSide) side(h, v);
     return h;
   };
   auto amax4 = [](float a, const float4& h) {
@@ -1052,14 +1188,33 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     if (v < nv) {
       c[i] = make_float4(silu_f(c[i].x) * cu[i].x, silu_f(c[i].y) * cu[i].y,
                          silu_f(c[i].z) * cu[i].z, silu_f(c[i].w) * cu[i].w);
-      if (sd) rot(c[i], v);
+      if (kSide) side(c[i], v);
       am = amax4(am, c[i]);
     }
   }
   for (int v = kRowCache * 32 + lane; v < nv; v += 32) am = amax4(am, h4(v));
   am = warp_max(am);
+  const int hsh = ROT ? kHadShift : 0;
+  if (ACT8) {
+    const float sc = e4m3_row_scale(am);
+    const float rc = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(hs) + pos * I);
+    auto put = [&](int v, const float4& h) {
+      dst[v] = e4m3_byte_of(h.x, sc, rc) | (e4m3_byte_of(h.y, sc, rc) << 8) |
+               (e4m3_byte_of(h.z, sc, rc) << 16) | (e4m3_byte_of(h.w, sc, rc) << 24);
+    };
+#pragma unroll
+    for (int i = 0; i < kRowCache; i++) {
+      const int v = i * 32 + lane;
+      if (v < nv) put(v, c[i]);
+    }
+    for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, h4(v));
+    if (lane == 0) hinv[pos] = ldexpf(sc, -hsh);
+    return;
+  }
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(hs) + pos * I);
   auto put = [&](int v, const float4& h) {
     dst[v] = make_uint2(pack_h2(h.x * sc, h.y * sc), pack_h2(h.z * sc, h.w * sc));
   };
@@ -1069,7 +1224,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     if (v < nv) put(v, c[i]);
   }
   for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, h4(v));
-  if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex - (sd ? kHadShift : 0));
+  if (lane == 0) hinv[pos] = ldexpf(1.0f, -ex - hsh);
 }
 
 // Token tiles per expert segment (one CTA, thread per expert): tiles of
@@ -1184,24 +1339,26 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major fp16 matrix [rows][cols] as a TMA source of 64 x 64 boxes, 128B swizzle.
-bool make_tmap(CUtensorMap* m, const void* base, size_t rows, size_t cols) {
+// Row-major matrix [rows][cols] of fp16 (esize 2) or E4M3 bytes (esize 1) as
+// a TMA source of boxes of 64 rows x 128 bytes, 128B swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, size_t rows, size_t cols, int esize) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+  cuuint32_t box[2] = {(cuuint32_t)(kRow / esize), 64};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int K, int FP8>
+template <int K, int FP8, int OP8>
 cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, cudaStream_t st) {
   using C = GCfg<K>;
   static bool init = false;
-  auto kfn = gemm_kernel<K, FP8>;
+  auto kfn = gemm_kernel<K, FP8, OP8>;
   if (!init) {
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
@@ -1209,7 +1366,7 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(OpT<OP8>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1222,10 +1379,10 @@ cudaError_t launch_gemm(const CUtensorMap& tm, const GemmParams& gp, int grid, c
   return err;
 }
 
-template <int K, int FP8>
+template <int K, int FP8, int OP8>
 cudaError_t launch_gemm64(const CUtensorMap& tm, const GemmParams& gp, int grid, cudaStream_t st) {
   static bool init = false;
-  auto kfn = gemm64_kernel<K, FP8>;
+  auto kfn = gemm64_kernel<K, FP8, OP8>;
   if (!init) {
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg::kSmem);
     if (e != cudaSuccess) return e;
@@ -1246,28 +1403,39 @@ cudaError_t launch_gemm64(const CUtensorMap& tm, const GemmParams& gp, int grid,
   return err;
 }
 
-cudaError_t dispatch_gemm64(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
-                            cudaStream_t st) {
-  if (fp8) {
-    if (K == 2) return launch_gemm64<2, 1>(tm, gp, grid, st);
-    if (K == 3) return launch_gemm64<3, 1>(tm, gp, grid, st);
-    return launch_gemm64<4, 1>(tm, gp, grid, st);
+// E4M3 operands (op8) exist only with the E4M3 rule (fp8).
+cudaError_t dispatch_gemm64(int K, int fp8, int op8, const CUtensorMap& tm, const GemmParams& gp,
+                            int grid, cudaStream_t st) {
+  if (op8) {
+    if (K == 2) return launch_gemm64<2, 1, 1>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm64<3, 1, 1>(tm, gp, grid, st);
+    return launch_gemm64<4, 1, 1>(tm, gp, grid, st);
   }
-  if (K == 2) return launch_gemm64<2, 0>(tm, gp, grid, st);
-  if (K == 3) return launch_gemm64<3, 0>(tm, gp, grid, st);
-  return launch_gemm64<4, 0>(tm, gp, grid, st);
+  if (fp8) {
+    if (K == 2) return launch_gemm64<2, 1, 0>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm64<3, 1, 0>(tm, gp, grid, st);
+    return launch_gemm64<4, 1, 0>(tm, gp, grid, st);
+  }
+  if (K == 2) return launch_gemm64<2, 0, 0>(tm, gp, grid, st);
+  if (K == 3) return launch_gemm64<3, 0, 0>(tm, gp, grid, st);
+  return launch_gemm64<4, 0, 0>(tm, gp, grid, st);
 }
 
-cudaError_t dispatch_gemm(int K, int fp8, const CUtensorMap& tm, const GemmParams& gp, int grid,
-                          cudaStream_t st) {
-  if (fp8) {
-    if (K == 2) return launch_gemm<2, 1>(tm, gp, grid, st);
-    if (K == 3) return launch_gemm<3, 1>(tm, gp, grid, st);
-    return launch_gemm<4, 1>(tm, gp, grid, st);
+cudaError_t dispatch_gemm(int K, int fp8, int op8, const CUtensorMap& tm, const GemmParams& gp,
+                          int grid, cudaStream_t st) {
+  if (op8) {
+    if (K == 2) return launch_gemm<2, 1, 1>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm<3, 1, 1>(tm, gp, grid, st);
+    return launch_gemm<4, 1, 1>(tm, gp, grid, st);
   }
-  if (K == 2) return launch_gemm<2, 0>(tm, gp, grid, st);
-  if (K == 3) return launch_gemm<3, 0>(tm, gp, grid, st);
-  return launch_gemm<4, 0>(tm, gp, grid, st);
+  if (fp8) {
+    if (K == 2) return launch_gemm<2, 1, 0>(tm, gp, grid, st);
+    if (K == 3) return launch_gemm<3, 1, 0>(tm, gp, grid, st);
+    return launch_gemm<4, 1, 0>(tm, gp, grid, st);
+  }
+  if (K == 2) return launch_gemm<2, 0, 0>(tm, gp, grid, st);
+  if (K == 3) return launch_gemm<3, 0, 0>(tm, gp, grid, st);
+  return launch_gemm<4, 0, 0>(tm, gp, grid, st);
 }
 
 size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -1291,13 +1459,14 @@ struct GemmLayout {
   size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, counts, lists, total;
 };
 
-// Format v2 keeps separate gate and up activation rows (2P rows).
-GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had) {
+// Format v2 and the FP8 operand mode keep separate gate and up activation
+// rows (2P rows); FP8 rows are 1 byte per element.
+GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had, int act8) {
   GemmLayout g{};
   const size_t P = (size_t)T * top_k;
-  const size_t xr = had ? 2 * P : P;
+  const size_t xr = had || act8 ? 2 * P : P;
   size_t o = 0;
-  g.xg = o; o += al(xr * H * 2);
+  g.xg = o; o += al(xr * H * (act8 ? 1 : 2));
   g.xinv = o; o += al(xr * 4);
   g.gu = o; o += al(2 * P * I * 4);
   g.hs = o; o += al(P * I * 2);
@@ -1314,8 +1483,8 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had) {
 
 }  // namespace
 
-size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had) {
-  return gemm_layout(T, top_k, E, H, I, had).total;
+size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had, int act8) {
+  return gemm_layout(T, top_k, E, H, I, had, act8).total;
 }
 
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
@@ -1324,7 +1493,10 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   auto rec = [&](int i) {
     if (ev && ev[i]) record_stage_event(ev[i], st);
   };
-  const GemmLayout g = gemm_layout(T, top_k, L.E, L.H, L.I, L.had);
+  const int a8 = L.act8;
+  const bool split = L.had || a8;  // separate gate and up activation rows
+  const int esize = a8 ? 1 : 2;
+  const GemmLayout g = gemm_layout(T, top_k, L.E, L.H, L.I, L.had, a8);
   char* base = static_cast<char*>(ws);
   uint16_t* xg = reinterpret_cast<uint16_t*>(base + g.xg);
   float* xinv = reinterpret_cast<float*>(base + g.xinv);
@@ -1341,8 +1513,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   const int P = T * top_k;
   const int mt = (int)max_tiles(T, L.E, top_k);
   CUtensorMap tm_x, tm_h;
-  if (!make_tmap(&tm_x, xg, (size_t)P * (L.had ? 2 : 1), (size_t)L.H) ||
-      !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I))
+  if (!make_tmap(&tm_x, xg, (size_t)P * (split ? 2 : 1), (size_t)L.H, esize) ||
+      !make_tmap(&tm_h, hs, (size_t)P, (size_t)L.I, esize))
     return cudaErrorInvalidValue;
   cudaError_t err;
   // grids: big tiles on 128-output strips, small tiles on 256-output chunks
@@ -1367,7 +1539,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   auto run = [&](int kind, int launch, const CUtensorMap& tm, const GemmParams& gp, int grid,
                  int K) -> cudaError_t {
     auto one = [&](int k, const GemmParams& q) {
-      return kind ? dispatch_gemm64(k, L.fp8, tm, q, grid, st) : dispatch_gemm(k, L.fp8, tm, q, grid, st);
+      return kind ? dispatch_gemm64(k, L.fp8, a8, tm, q, grid, st)
+                  : dispatch_gemm(k, L.fp8, a8, tm, q, grid, st);
     };
     if (!L.mixed) return one(K, gp);
     const size_t n = kind ? (size_t)L.E : (size_t)mt;
@@ -1386,11 +1559,13 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     return cudaSuccess;
   };
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
-  if (L.had)
-    err = launch_pdl(gather_rows_had_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x,
-                     x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
-                     L.suh[0], L.suh[1], xg, xinv);
-  else
+  if (split) {
+    auto kfn = a8 ? (L.had ? gather_rows_split_kernel<1, 1> : gather_rows_split_kernel<0, 1>)
+                  : gather_rows_split_kernel<1, 0>;
+    err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H, top_k, P,
+                     (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids, L.suh[0], L.suh[1],
+                     (void*)xg, xinv);
+  } else
     err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
                      L.H, top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
   note_launches(2);
@@ -1408,7 +1583,7 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.budget = kWaitBudgetCycles;
   gu.fault_ks = -1;
   gu.had = L.had;
-  gu.xrow_off = L.had ? P : 0;
+  gu.xrow_off = split ? P : 0;
   gu.proj0 = 0;
   const WaitFault wf = g_fault;
   auto with_fault = [&](GemmParams q, int kernel) {
@@ -1429,9 +1604,13 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   }
   rec(3);
 
-  err = launch_pdl(swiglu_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
-                   (const float*)gu_buf, (size_t)P, L.I, (const int32_t*)rb.seg_pairs,
-                   (const int32_t*)rb.ids, L.had ? L.suh[2] : (const uint16_t*)nullptr, hs, hinv);
+  {
+    auto kfn = L.had ? (a8 ? swiglu_rows_kernel<1, 1> : swiglu_rows_kernel<1, 0>)
+                     : (a8 ? swiglu_rows_kernel<0, 1> : swiglu_rows_kernel<0, 0>);
+    err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, (const float*)gu_buf,
+                     (size_t)P, L.I, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
+                     L.suh[2], (void*)hs, hinv);
+  }
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(4);
@@ -1458,6 +1637,41 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
 }
 
 }  // namespace exl3
+
+namespace exl3 {
+namespace {
+// Rows of fp32 values to their E4M3 operand bytes and fp32 scales, with the
+// device functions the activation passes use (one CTA per row).
+__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const float* __restrict__ a, int n,
+                                                                 uint8_t* __restrict__ q,
+                                                                 float* __restrict__ s) {
+  __shared__ float s_w[8];
+  const float* row = a + (size_t)blockIdx.x * n;
+  float am = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(row[i]));
+  am = warp_max(am);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = am;
+  __syncthreads();
+  am = 0.0f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); w++) am = fmaxf(am, s_w[w]);
+  const float sc = e4m3_row_scale(am);
+  const float rc = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    q[(size_t)blockIdx.x * n + i] = (uint8_t)e4m3_byte_of(row[i], sc, rc);
+  if (threadIdx.x == 0) s[blockIdx.x] = sc;
+}
+}  // namespace
+}  // namespace exl3
+
+extern "C" exl3_status exl3_quantize_rows_e4m3(const float* a, int rows, int n, uint8_t* q,
+                                               float* s, void* stream) {
+  if (rows < 0 || n < 0) return EXL3_ERR_SHAPE;
+  if (rows == 0 || n == 0) return EXL3_OK;
+  if (!a || !q || !s) return EXL3_ERR_ARG;
+  exl3::quantize_rows_e4m3_kernel<<<rows, 256, 0, static_cast<cudaStream_t>(stream)>>>(a, n, q, s);
+  exl3::note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA;
+}
 
 extern "C" exl3_status exl3_test_set_wait_fault(int kernel, int ks, long long budget_cycles) {
   if (kernel == 0) {

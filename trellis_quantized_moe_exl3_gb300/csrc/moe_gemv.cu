@@ -139,6 +139,14 @@ __device__ __forceinline__ void rotate_block16(float (&f)[16]) {
     for (int q = 0; q < 16; q++) f[q] = wht_lane(f[q], m, gm);
 }
 
+// FP8 operand mode: the 16 values as their E4M3 operand values q = E4M3(a / s)
+// (exact in fp16, so the GEMV's fp16 operand carries them unchanged).
+__device__ __forceinline__ void quant16(float (&f)[16], float s) {
+  const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+#pragma unroll
+  for (int q = 0; q < 16; q++) f[q] = e4m3_value(f[q], s, r);
+}
+
 __device__ __forceinline__ float amax16(float a, const float (&f)[16]) {
 #pragma unroll
   for (int q = 0; q < 16; q++) a = fmaxf(a, fabsf(f[q]));
@@ -148,12 +156,14 @@ __device__ __forceinline__ float amax16(float a, const float (&f)[16]) {
 // x rows of the pairs, times suh of gate and up (rotated when had), scaled,
 // into the group-interleaved layout [group][proj][in/16][8 tokens][16]
 // (fp16x2).  blockDim is a multiple of 8, so thread b's block shares its
-// 128-input block with threads b ^ 1 .. b ^ 7 in every step.
+// 128-input block with threads b ^ 1 .. b ^ 7 in every step.  act8 (FP8
+// operand mode): the rows' E4M3 operand values with their fp32 row scales
+// instead of a power-of-two scale.
 __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__ x, int x_bf16,
                                                         int H, int k, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_g,
                                                         const uint16_t* __restrict__ suh_u,
-                                                        int had, uint32_t* __restrict__ xs,
+                                                        int had, int act8, uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
@@ -202,23 +212,28 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
   ag = block_max(ag, s_tmp);
   au = block_max(au, s_tmp);
   const int eg = fp16_scale_exp(ag), eu = fp16_scale_exp(au);
-  const float scg = ldexpf(1.0f, eg), scu = ldexpf(1.0f, eu);
+  const float qg = e4m3_row_scale(ag), qu = e4m3_row_scale(au);
+  const float scg = act8 ? 1.0f : ldexpf(1.0f, eg), scu = act8 ? 1.0f : ldexpf(1.0f, eu);
   uint32_t* og = xs + (size_t)g * 2 * nb * kXsChunk / 4;
   uint32_t* ou = og + (size_t)nb * kXsChunk / 4;
-  if (b0 < nb) {
-    put16(og, b0, slot, cg, scg);
-    put16(ou, b0, slot, cu, scu);
-  }
+  auto put2 = [&](int b, float (&fg)[16], float (&fu)[16]) {
+    if (act8) {
+      quant16(fg, qg);
+      quant16(fu, qu);
+    }
+    put16(og, b, slot, fg, scg);
+    put16(ou, b, slot, fu, scu);
+  };
+  if (b0 < nb) put2(b0, cg, cu);
   for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
     float fg[16], fu[16];
     prod(b, fg, fu);
-    put16(og, b, slot, fg, scg);
-    put16(ou, b, slot, fu, scu);
+    put2(b, fg, fu);
   }
   if (threadIdx.x == 0) {
     const int hs = had ? kHadShift : 0;  // the unnormalized rotations' 128
-    xs_inv[2 * pos] = ldexpf(1.0f, -eg - hs);
-    xs_inv[2 * pos + 1] = ldexpf(1.0f, -eu - hs);
+    xs_inv[2 * pos] = act8 ? ldexpf(qg, -hs) : ldexpf(1.0f, -eg - hs);
+    xs_inv[2 * pos + 1] = act8 ? ldexpf(qu, -hs) : ldexpf(1.0f, -eu - hs);
   }
 }
 
@@ -228,7 +243,7 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
 __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, int ns,
                                                         size_t n_pos, int I, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
-                                                        int had, uint32_t* __restrict__ xs,
+                                                        int had, int act8, uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
@@ -277,15 +292,21 @@ __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict_
   }
   am = block_max(am, s_tmp);
   const int ex = fp16_scale_exp(am);
-  const float sc = ldexpf(1.0f, ex);
+  const float qs = e4m3_row_scale(am);
+  const float sc = act8 ? 1.0f : ldexpf(1.0f, ex);
   uint32_t* o = xs + (size_t)g * nb * kXsChunk / 4;
-  if (b0 < nb) put16(o, b0, slot, c, sc);
+  if (b0 < nb) {
+    if (act8) quant16(c, qs);
+    put16(o, b0, slot, c, sc);
+  }
   for (int b = b0 + blockDim.x; b < nb; b += blockDim.x) {
     float h[16];
     hval(b, h);
+    if (act8) quant16(h, qs);
     put16(o, b, slot, h, sc);
   }
-  if (threadIdx.x == 0) xs_inv[pos] = ldexpf(1.0f, -ex - (had ? kHadShift : 0));
+  if (threadIdx.x == 0)
+    xs_inv[pos] = act8 ? ldexpf(qs, -(had ? kHadShift : 0)) : ldexpf(1.0f, -ex - (had ? kHadShift : 0));
 }
 
 template <int K, int FP8>
@@ -739,7 +760,8 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     if (err != cudaSuccess) return err;
   }
   err = launch_pdl(gather_xs_kernel, dim3(P), dim3(input_pass_threads(L.H)), 0, st, x,
-                   x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, gb.xs_gu, gb.xs_gu_inv);
+                   x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, L.act8, gb.xs_gu,
+                   gb.xs_gu_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(2);
@@ -772,7 +794,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   rec(3);
 
   err = launch_pdl(prep_down_kernel, dim3(P), dim3(input_pass_threads(L.I)), 0, st, gb.gu,
-                   gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, gb.xs_d, gb.xs_d_inv);
+                   gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, L.act8, gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(4);

@@ -3,7 +3,11 @@
 //
 // Shared-memory operand layouts used by this library (both 128-byte
 // swizzled: the 16-byte chunk index inside each 128-byte row is XORed with
-// the row index modulo 8, so every 8-row atom must start 1024-byte aligned):
+// the row index modulo 8, so every 8-row atom must start 1024-byte aligned).
+// Described for fp16 elements; with E4M3 (1-byte) elements a 128-byte row
+// holds twice the elements (128 K elements, or 128 M elements, so a 128-row
+// MN-major tile is a single atom wide), and a K slice of 32 takes the byte
+// offsets a K slice of 16 takes with fp16:
 //   * K-major (activations, B operand): row n = 64 consecutive K elements
 //     (128 B); 8 rows form a 1024 B atom; atoms of consecutive rows are
 //     adjacent (stride-dimension offset 1024 B).  A K slice of 16 starts at
@@ -47,6 +51,19 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// kind::f8f6f4 with E4M3 A and B (the instruction descriptor's A and B
+// format fields are 0 for E4M3, as they are for fp16 under kind::f16, so
+// umma_idesc_f16 serves both), fp32 accumulate; K = 32 per instruction, i.e.
+// the same 32 bytes of a K-major row as a kind::f16 instruction's K = 16.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -43,6 +43,7 @@ class LayerSpec:
     hadamard: bool = False  # format v2 (rotation on both sides); no effect on the draws
     shared_coded: bool = False  # one more coded expert (the shared one) after the routed ones
     expert_K: tuple | None = None  # per expert (gate, up, down) widths; codes then flat
+    act_fp8: bool = False  # FP8 x FP8 products (E4M3 activation rows); no effect on the draws
 
     @property
     def n_coded(self) -> int:
