@@ -188,12 +188,16 @@ __device__ __forceinline__ float e4m3_row_scale(float amax) {
 // monotonic: when both of those round to the same byte, Q does too, and that
 // byte is the decision an IEEE division would give.  Only a quotient within
 // a few ulps of an E4M3 rounding boundary takes the IEEE division.
+// (kept out of line so that the common path does not carry the division)
+static __device__ __noinline__ uint32_t e4m3_byte_div(float a, float s) {
+  return e4m3_pack2(fabsf(__fdiv_rn(a, s)), 0.0f) & 0xFFu;
+}
 __device__ __forceinline__ uint32_t e4m3_byte_of(float a, float s, float r) {
   if (!(s > 0.0f)) return 0u;
   const uint32_t m = __float_as_uint(a * r) & 0x7FFFFFFFu;
   const uint32_t two = e4m3_pack2(__uint_as_float(m > 4u ? m - 4u : 0u), __uint_as_float(m + 4u));
   uint32_t b = two & 0xFFu;
-  if (b != (two >> 8)) b = e4m3_pack2(fabsf(__fdiv_rn(a, s)), 0.0f) & 0xFFu;
+  if (__builtin_expect(b != (two >> 8), 0)) b = e4m3_byte_div(a, s);
   return b | (a < 0.0f ? 0x80u : 0u);
 }
 

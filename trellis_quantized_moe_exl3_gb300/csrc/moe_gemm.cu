@@ -60,8 +60,7 @@ struct OpT {
   static constexpr int kKS = OP8 ? 128 : 64;           // inputs per K step
   static constexpr int kBlk = 16 * 128 * (OP8 ? 1 : 2);  // one 16-input block of a 128-output tile
   static constexpr int kJobs = kKS / 16;               // 16-input blocks per K step
-  static constexpr int kDec = OP8 ? 8 : 12;            // decoder warps (big tiles)
-  static constexpr int kPar = kDec / kJobs;            // K steps decoded in parallel
+  static constexpr int kDec = 12;                      // decoder warps (big tiles)
   static constexpr int kThreads = (kDec + 2) * 32;
   static constexpr int kSJobs = 2 * kJobs;             // small tiles: blocks x 2 code strips
   static constexpr int kSPar = kSDec / kSJobs;
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, GemmParams p) {
   using C = GCfg<K>;
   using T = OpT<OP8>;
-  constexpr int kDec = T::kDec, kJobs = T::kJobs, kPar = T::kPar, kKS = T::kKS;
+  constexpr int kDec = T::kDec, kJobs = T::kJobs, kKS = T::kKS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -450,13 +449,14 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- decode
-    const int blk = warp % kJobs;
-    const int ks0 = warp / kJobs;
+    // jobs are the tile's 16-input blocks j = 0 .. nks * kJobs - 1 (K step
+    // j / kJobs, block j % kJobs of it); warp w takes j = w, w + kDec, ...
     const int g = OP8 ? dec_tile8(lane) : dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
     const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
                            (size_t)8 * s * 32 * K;
-    const int n_my = (nks - ks0 + kPar - 1) / kPar;
+    const int n_jobs = nks * kJobs;
+    const int n_my = warp < n_jobs ? (n_jobs - warp + kDec - 1) / kDec : 0;
     // lane-constant swizzled offsets of this lane's output chunks in a block:
     // fp16, 8 chunks of 8 outputs (input c + 4jh + 8hf, rows 8jl..8jl+7);
     // E4M3, 4 chunks of 16 outputs (input c + 4jh + 8hf)
@@ -473,41 +473,41 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
       off8[c4] = hf * 1024 + kr * 128 + ((g ^ kr) << 4);
     }
     const uint32_t neg16 = opaque_u32(0xFFFF0000u);
-    // this lane's 8K code bytes of job n (code lane `lane` of the 8-tile chunk)
+    // this lane's 8K code bytes of job n (code lane `lane` of the 8-tile
+    // chunk); the code row of block j of the tile is row j of the expert
     auto lane_codes = [&](int n) {
-      const int ks = ks0 + n * kPar;
-      return reinterpret_cast<const uint16_t*>(cbase + (size_t)(ks * kJobs + blk) * row_bytes) +
-             (g * 4 + c) * 4 * K;
+      const int j = warp + n * kDec;
+      return reinterpret_cast<const uint16_t*>(cbase + (size_t)j * row_bytes) + (g * 4 + c) * 4 * K;
     };
     // code rows are pulled into L2 kL2Ahead jobs ahead, so the register
     // prefetch one job ahead hits L2
     constexpr int kL2Ahead = 8;
     auto prefetch_l2 = [&](int n) {
       if (n < n_my && lane * 128 < C::kCodeChunk) {
-        const int ks = ks0 + n * kPar;
-        const uint8_t* a = cbase + (size_t)(ks * kJobs + blk) * row_bytes + lane * 128;
+        const uint8_t* a = cbase + (size_t)(warp + n * kDec) * row_bytes + lane * 128;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
       }
     };
     for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
-    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
-    // suh of this lane's 4 inputs of a block, loaded one job ahead
+    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + c;
+    // suh of this lane's 4 inputs of a block (inputs 16 j + c + 4 jh + 8 hf),
+    // loaded one job ahead
     uint32_t s2n[4];
     auto load_suh = [&](int n) {
-      const int ks = ks0 + n * kPar;
+      const int j = warp + n * kDec;
 #pragma unroll
       for (int q = 0; q < 4; q++)  // format v2, FP8 operands: suh is on the activation side
-        s2n[q] = p.had || OP8 ? 0x3C00u : __ldg(suh_e + ks * kKS + 4 * (q & 1) + 8 * (q >> 1));
+        s2n[q] = p.had || OP8 ? 0x3C00u : __ldg(suh_e + 16 * j + 4 * (q & 1) + 8 * (q >> 1));
     };
     LaneWords<K> nxt;
     if (n_my > 0) {
       load_suh(0);
       load_lane_words<K>(nxt, lane_codes(0));
     }
-    // this warp's A stage and phase advance by kPar stages per job (kPar < nast)
-    int sa = ks0;
-    uint32_t pa = 0;
     for (int n = 0; n < n_my; n++) {
+      const int j = warp + n * kDec, ks = j / kJobs, blk = j % kJobs;
+      const int sa = ks % nast;                      // the K step's A stage
+      const uint32_t pa = (uint32_t)(ks / nast) & 1u;  // and its fill count's parity
       LaneWords<K> lw = nxt;
       if (n + 1 < n_my) load_lane_words<K>(nxt, lane_codes(n + 1));
       prefetch_l2(n + kL2Ahead);
@@ -524,11 +524,6 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
-      sa += kPar;
-      if (sa >= nast) {
-        sa -= nast;
-        pa ^= 1;
-      }
     }
 
     // ------------------------------------------------------------- epilogue
@@ -1559,12 +1554,15 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     return cudaSuccess;
   };
   const int row_blocks = (P + kRowWarps - 1) / kRowWarps;
-  if (split) {
-    auto kfn = a8 ? (L.had ? gather_rows_split_kernel<1, 1> : gather_rows_split_kernel<0, 1>)
-                  : gather_rows_split_kernel<1, 0>;
+  if (a8) {
+    auto kfn = L.had ? gather_rows_split_kernel<1, 1> : gather_rows_split_kernel<0, 1>;
     err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H, top_k, P,
                      (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids, L.suh[0], L.suh[1],
                      (void*)xg, xinv);
+  } else if (split) {
+    err = launch_pdl(gather_rows_split_kernel<1, 0>, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
+                     x, x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
+                     L.suh[0], L.suh[1], (void*)xg, xinv);
   } else
     err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
                      L.H, top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
