@@ -215,6 +215,33 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t *layer, const void *x, exl3_d
                                 const float *logits, int T, int top_k, const void *residual,
                                 void *out, int path, void *ws, size_t ws_bytes, void *stream);
 
+/* One layer forward over a range of experts, for expert parallelism
+ * (expert-parallel sharding of the routed experts over N ranks; the pages
+ * split the layer over GPUs and sum the partial outputs with one
+ * all-reduce per layer: [p2] Why the overlay exists).  Routing covers every
+ * token and expert as in exl3_moe_forward; only the (token, expert) pairs
+ * whose expert e has expert_begin <= e < expert_end are computed (with a
+ * coded shared expert, its index is num_experts, the last one), plus the
+ * dense shared expert when with_shared = 1.  out (device fp32 [T][H]) gets
+ * their unrounded sum, summed in pair order, so the ranks' outputs summed
+ * over a partition of [0, num_experts + shared_coded) with the shared expert
+ * on exactly one rank give the layer before its final rounding (finish with
+ * exl3_round_output).  The workspace and path are as for
+ * exl3_moe_forward_ex.  Errors: those of exl3_moe_forward_ex, and
+ * EXL3_ERR_ARG for a range outside [0, num_experts + shared_coded] or
+ * with_shared not 0 / 1. */
+exl3_status exl3_moe_forward_experts(const exl3_layer_t *layer, const void *x, exl3_dtype dt,
+                                     const float *logits, int T, int top_k, int expert_begin,
+                                     int expert_end, int with_shared, float *out, int path,
+                                     void *ws, size_t ws_bytes, void *stream);
+
+/* out = round(y + residual) to dt: the last step of a layer whose partial
+ * sums were reduced outside the library.  y device fp32 [T][H], residual
+ * device [T][H] in dt or NULL, out device [T][H] in dt; all 16-byte aligned,
+ * H a multiple of 4. */
+exl3_status exl3_round_output(const float *y, int T, int H, const void *residual, exl3_dtype dt,
+                              void *out, void *stream);
+
 /* Unweighted RMSNorm of each row: out = round(x / sqrt(mean(x^2) + eps)),
  * fp32 arithmetic, x and out device [T][H] in dt (out may alias x).  Used
  * between layers of a stacked prefill. */

@@ -133,6 +133,16 @@ def test_forward_validation_without_layer(L):
     assert L.exl3_get_device_status(None, None, ctypes.byref(s)) == _lib.EXL3_ERR_ARG
 
 
+def test_expert_range_and_round_validation(L):
+    vp = ctypes.c_void_p
+    assert L.exl3_moe_forward_experts(None, vp(4096), 1, vp(4096), 4, 8, 0, 8, 1, vp(8192), 0,
+                                      vp(4096), 1 << 20, None) == _lib.EXL3_ERR_ARG
+    assert L.exl3_round_output(vp(4096), 4, 250, None, 1, vp(8192), None) == _lib.EXL3_ERR_SHAPE
+    assert L.exl3_round_output(vp(4096), 4, 256, None, 7, vp(8192), None) == _lib.EXL3_ERR_ARG
+    assert L.exl3_round_output(None, 4, 256, None, 1, vp(8192), None) == _lib.EXL3_ERR_ARG
+    assert L.exl3_round_output(None, 0, 256, None, 1, None, None) == _lib.EXL3_OK
+
+
 def test_quantize_rows_validation(L):
     vp = ctypes.c_void_p
     assert L.exl3_quantize_rows_e4m3(vp(4096), -1, 16, vp(4096), vp(4096), None) == _lib.EXL3_ERR_SHAPE

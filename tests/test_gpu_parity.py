@@ -601,6 +601,58 @@ def test_prefill_workload_act_fp8_sampled():
     _workload_parity("prefill", _prefill_tokens, act_fp8=True)
 
 
+# ------------------------------------------------------------------ expert parallelism
+
+
+@pytest.mark.parametrize("E,H,I,K,fp8,a8,shared,sc,T,k,routing,path", [
+    (10, 384, 256, (2, 2, 3), False, False, True, False, 37, 4, "normal", 1),   # GEMV, dense shared
+    (8, 512, 256, (3, 3, 4), False, False, False, True, 40, 4, "normal", 1),    # GEMV, coded shared
+    (8, 512, 256, (4, 4, 3), False, False, True, False, 700, 4, "zipf", 2),     # big + small tiles
+    (8, 512, 256, (4, 4, 4), True, True, False, True, 300, 4, "normal", 2),     # FP8, coded shared
+])
+def test_forward_experts_partition(E, H, I, K, fp8, a8, shared, sc, T, k, routing, path):
+    """Expert-parallel shards on one GPU: forwards over a partition of the
+    experts into three ranges (the dense shared expert in one of them), their
+    fp32 partial sums added and rounded once, against the oracle's whole
+    layer; an empty range gives zeros."""
+    from trellis_quantized_moe_exl3_gb300.api import round_output
+    from trellis_quantized_moe_exl3_gb300.ep import expert_range
+    spec = synth.LayerSpec(seed=230 + sum(K), num_experts=E, hidden=H, inter=I, K=K,
+                           fp8_round=fp8, act_fp8=a8, shared=shared, shared_coded=sc)
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x = synth.activations(231, T, H, "bf16")
+    logits = synth.router_logits(231, T, E, routing)
+    xt, lg = _act(x, "bf16"), torch.from_numpy(logits).cuda()
+    y = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    for r in range(3):
+        e0, e1 = expert_range(r, 3, layer.n_coded)
+        y += layer.forward_experts(xt, lg, k, e0, e1, with_shared=(r == 1), path=path)
+    out = round_output(y, torch.bfloat16)
+    torch.cuda.synchronize()
+    assert_layer_close(act_to_f64(out), hl.oracle().forward(x, True, logits, k))
+    assert device_status(layer.workspace(T, k)) == 0
+    empty = layer.forward_experts(xt, lg, k, 2, 2, with_shared=False, path=path)
+    torch.cuda.synchronize()
+    assert bool((empty == 0).all())
+
+
+def test_moe_forward_ep_single_rank():
+    """moe_forward_ep without a process group (one rank: every expert) equals
+    the plain forward's output within the layer tolerance, residual included."""
+    from trellis_quantized_moe_exl3_gb300.ep import moe_forward_ep
+    spec = synth.LayerSpec(seed=240, num_experts=8, hidden=256, inter=128, K=(2, 2, 2), shared=True)
+    hl = HostLayer(spec)
+    layer = hl.device()
+    x = _act(synth.activations(241, 9, 256, "bf16"), "bf16")
+    res = _act(synth.activations(242, 9, 256, "bf16"), "bf16")
+    lg = torch.from_numpy(synth.router_logits(241, 9, 8, "normal")).cuda()
+    a = moe_forward_ep(layer, x, lg, 2, residual=res)
+    b = layer.forward(x, lg, 2, residual=res)
+    torch.cuda.synchronize()
+    assert_layer_close(act_to_f64(a), act_to_f64(b))
+
+
 # ------------------------------------------------------------------ bounded waits
 
 

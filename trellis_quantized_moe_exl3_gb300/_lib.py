@@ -77,6 +77,10 @@ def lib():
     L.exl3_moe_forward.restype = i
     L.exl3_moe_forward_ex.argtypes = [vp, vp, i, vp, i, i, vp, vp, i, vp, sz, vp]
     L.exl3_moe_forward_ex.restype = i
+    L.exl3_moe_forward_experts.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, i, vp, sz, vp]
+    L.exl3_moe_forward_experts.restype = i
+    L.exl3_round_output.argtypes = [vp, i, i, vp, i, vp, vp]
+    L.exl3_round_output.restype = i
     L.exl3_rmsnorm.argtypes = [vp, i, i, i, ctypes.c_float, vp, vp]
     L.exl3_rmsnorm.restype = i
     L.exl3_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]

@@ -93,6 +93,7 @@ class Layer:
         check(_lib.lib().exl3_layer_create(ctypes.byref(d), ctypes.byref(h)), "exl3_layer_create")
         self._h = h
         self._ws = None
+        self._sc = bool(shared_coded)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -138,6 +139,43 @@ class Layer:
                                             _ptr(ws), ws.numel(), _stream(stream))
         check(st, "exl3_moe_forward_ex")
         return out
+
+
+    @property
+    def n_coded(self) -> int:
+        """Experts in the code arrays (routed, plus a coded shared expert)."""
+        return self.E + int(self._sc)
+
+    def forward_experts(self, x, logits, top_k: int, expert_begin: int, expert_end: int,
+                        with_shared: bool = True, out=None, path: int = 0, ws=None,
+                        stream=None) -> torch.Tensor:
+        """fp32 [T, H] sum of the pairs whose expert is in [expert_begin,
+        expert_end) (+ the dense shared expert when with_shared), unrounded."""
+        _req(x, "x", (torch.float16, torch.bfloat16))
+        _req(logits, "logits", torch.float32)
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.float32, device=x.device)
+        _req(out, "out", torch.float32)
+        if ws is None:
+            ws = self.workspace(T, top_k, x.device)
+        st = _lib.lib().exl3_moe_forward_experts(
+            self._h, _ptr(x), _dtype_code(x.dtype), _ptr(logits), T, top_k, int(expert_begin),
+            int(expert_end), int(bool(with_shared)), _ptr(out), int(path), _ptr(ws), ws.numel(),
+            _stream(stream))
+        check(st, "exl3_moe_forward_experts")
+        return out
+
+
+def round_output(y, dtype, residual=None, out=None, stream=None):
+    """round(y + residual) to dtype (fp16 or bf16); y fp32 [T, H]."""
+    _req(y, "y", torch.float32)
+    if out is None:
+        out = torch.empty(y.shape, dtype=dtype, device=y.device)
+    T, H = y.shape
+    check(_lib.lib().exl3_round_output(_ptr(y), T, H, _ptr(residual), _dtype_code(dtype), _ptr(out),
+                                       _stream(stream)), "exl3_round_output")
+    return out
 
 
 def route(logits, top_k: int, ws=None, stream=None):

@@ -28,13 +28,29 @@ __device__ __forceinline__ void store_act4(void* out, int bf16, size_t idx, floa
   }
 }
 
+// Pair j of token t takes part when its expert is in the call's range.
+__device__ __forceinline__ bool in_shard(const int32_t* ids, size_t pair, Shard sh) {
+  const int e = ids[pair];
+  return e >= sh.e0 && e < sh.e1;
+}
+
+// The 4 outputs: rounded to the activation dtype, or (out_f32) the fp32 sum.
+__device__ __forceinline__ void store_out4(void* out, int bf16, int f32, size_t idx, float4 v) {
+  if (f32)
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+  else
+    store_act4(out, bf16, idx, v);
+}
+
 // One thread per group of 4 outputs, for unsplit pair rows: the k pair rows
 // and the shared-expert partials are added in order.
 __global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restrict__ r, int T,
-                                                           int k, int H,
+                                                           int k, int H, const int32_t* ids,
+                                                           Shard sh,
                                                            const float* __restrict__ sp, int ns,
                                                            const void* __restrict__ resid,
-                                                           void* __restrict__ out, int bf16) {
+                                                           void* __restrict__ out, int bf16,
+                                                           int f32) {
   pdl_wait();
   const size_t n4 = (size_t)T * H / 4;
   for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n4;
@@ -42,6 +58,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restri
     const size_t t = v / (H / 4), o = (v % (H / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; j++) {
+      if (!in_shard(ids, t * k + j, sh)) continue;
       const float4 q = __ldcs(reinterpret_cast<const float4*>(r + (t * k + j) * H + o));
       acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
     }
@@ -59,7 +76,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restri
       acc.z += load_act(resid, bf16, t * H + o + 2);
       acc.w += load_act(resid, bf16, t * H + o + 3);
     }
-    store_act4(out, bf16, t * H + o, acc);
+    store_out4(out, bf16, f32, t * H + o, acc);
   }
 }
 
@@ -68,9 +85,10 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const float* __restri
 // partials s = l, l + 8, ... (in order); lane 0 then adds the eight lanes'
 // sums in lane order, so the result is the same on every run.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ r, int nr, int T,
-                                                      int k, int H, const float* __restrict__ sp,
+                                                      int k, int H, const int32_t* ids, Shard sh,
+                                                      const float* __restrict__ sp,
                                                       int ns, const void* __restrict__ resid,
-                                                      void* __restrict__ out, int bf16) {
+                                                      void* __restrict__ out, int bf16, int f32) {
   pdl_wait();
   const int lane = threadIdx.x & 31, l8 = lane & 7, base = lane & 24;
   const size_t n4 = (size_t)T * H / 4;
@@ -86,6 +104,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (live) {
       for (int j = l8; j < k; j += 8) {
+        if (!in_shard(ids, t * k + j, sh)) continue;
         const float* rp = r + (t * k + j) * H + o;
         float4 pr = *reinterpret_cast<const float4*>(rp);
 #pragma unroll 8
@@ -121,8 +140,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         acc.z += load_act(resid, bf16, t * H + o + 2);
         acc.w += load_act(resid, bf16, t * H + o + 3);
       }
-      store_act4(out, bf16, t * H + o, acc);
+      store_out4(out, bf16, f32, t * H + o, acc);
     }
+  }
+}
+
+// out = round(y + residual), 4 outputs per thread.
+__global__ void __launch_bounds__(256) round_output_kernel(const float* __restrict__ y, size_t n4,
+                                                           const void* __restrict__ resid,
+                                                           void* __restrict__ out, int bf16) {
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n4;
+       v += (size_t)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4*>(y)[v];
+    if (resid) {
+      a.x += load_act(resid, bf16, 4 * v + 0);
+      a.y += load_act(resid, bf16, 4 * v + 1);
+      a.z += load_act(resid, bf16, 4 * v + 2);
+      a.w += load_act(resid, bf16, 4 * v + 3);
+    }
+    store_act4(out, bf16, 4 * v, a);
   }
 }
 
@@ -156,8 +192,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const void* __restrict__ x
 }  // namespace
 
 cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H,
-                           const float* shared_part, int shared_splits, const void* residual,
-                           void* out, int out_bf16, cudaStream_t st) {
+                           const int32_t* ids, Shard sh, const float* shared_part,
+                           int shared_splits, const void* residual, void* out, int out_bf16,
+                           int out_f32, cudaStream_t st) {
   const size_t n4 = (size_t)T * H / 4;
   cudaError_t err;
   if (r_splits == 1) {
@@ -165,14 +202,27 @@ cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(combine_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, r, T, top_k, H,
-                     shared_part, shared_splits, residual, out, out_bf16);
+                     ids, sh, shared_part, shared_splits, residual, out, out_bf16, out_f32);
   } else {
     size_t blocks = (n4 * 8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, r, r_splits, T,
-                     top_k, H, shared_part, shared_splits, residual, out, out_bf16);
+                     top_k, H, ids, sh, shared_part, shared_splits, residual, out, out_bf16,
+                     out_f32);
   }
+  note_launches(1);
+  return err;
+}
+
+cudaError_t launch_round_output(const float* y, int T, int H, const void* residual, void* out,
+                                int out_bf16, cudaStream_t st) {
+  const size_t n4 = (size_t)T * H / 4;
+  if (n4 == 0) return cudaSuccess;
+  size_t blocks = (n4 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  const cudaError_t err = launch_pdl(round_output_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                                     y, n4, residual, out, out_bf16);
   note_launches(1);
   return err;
 }

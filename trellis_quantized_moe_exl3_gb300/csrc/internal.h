@@ -90,6 +90,13 @@ void route_carve(void* ws, int T, int E, int top_k, RouteBuffers* rb);
 cudaError_t launch_route(const float* logits, int T, int E, int top_k, const RouteBuffers& rb,
                          cudaStream_t st, int shared = 0);
 
+// Expert range of one call: only (token, expert) pairs whose expert e has
+// e0 <= e < e1 are computed and summed (expert parallelism: each rank takes
+// a range, the ranks' partial outputs are summed).  [0, E) is the whole layer.
+struct Shard {
+  int e0, e1;
+};
+
 struct LayerView {
   int E, H, I;
   int K[3];
@@ -144,7 +151,7 @@ void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb
 // ev (may be null): events recorded after gather [2], gate/up [3], down prep [4], down [5].
 cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
                             const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,
-                            cudaStream_t st);
+                            Shard sh, cudaStream_t st);
 
 // ---- grouped GEMM path (prefill-sized steps, tcgen05)
 size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had, int act8);
@@ -152,7 +159,7 @@ size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had, int ac
 // *r_out receives the pair-row buffer [P][H] the combine reads.
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
                             const RouteBuffers& rb, void* ws, const cudaEvent_t* ev, float** r_out,
-                            cudaStream_t st);
+                            Shard sh, cudaStream_t st);
 
 // ---- shared expert (dense fp16)
 size_t shared_scratch_bytes(int T, int H, int I);
@@ -162,10 +169,16 @@ cudaError_t launch_shared(const LayerView& L, const void* x, int x_bf16, int T, 
                           const float** part_d, int* nsplit_d, cudaStream_t st);
 
 // ---- combine / norm
-// r: [r_splits][T*top_k][H] pair rows (K-split partials, added in order).
+// r: [r_splits][T*top_k][H] pair rows (K-split partials, added in order);
+// only pairs whose expert (ids) lies in the shard's range are added.
+// out_f32: out is fp32 and takes the sum unrounded (no residual).
 cudaError_t launch_combine(const float* r, int r_splits, int T, int top_k, int H,
-                           const float* shared_part, int shared_splits, const void* residual,
-                           void* out, int out_bf16, cudaStream_t st);
+                           const int32_t* ids, Shard sh, const float* shared_part,
+                           int shared_splits, const void* residual, void* out, int out_bf16,
+                           int out_f32, cudaStream_t st);
+// out = round(y + residual) to bf16 / fp16 (y fp32 [T][H]; residual may be null).
+cudaError_t launch_round_output(const float* y, int T, int H, const void* residual, void* out,
+                                int out_bf16, cudaStream_t st);
 cudaError_t launch_rmsnorm(const void* x, int bf16, int T, int H, float eps, void* out,
                            cudaStream_t st);
 

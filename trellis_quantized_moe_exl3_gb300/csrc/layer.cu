@@ -250,9 +250,17 @@ size_t exl3_moe_workspace_size(const exl3_layer_t* layer, int T, int top_k) {
   return fwd_layout(layer->v, layer->has_shared, T, top_k).total;
 }
 
-exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
-                                const float* logits, int T, int top_k, const void* residual,
-                                void* out, int path, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One forward over the experts of `sh` (all of them for a whole layer).
+// with_shared: add the dense shared expert; out_f32: out is the fp32 sum
+// (no residual, no rounding), else round(residual + sum) in dt.
+exl3_status forward_impl(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
+                         const float* logits, int T, int top_k, const void* residual, void* out,
+                         int path, void* ws, size_t ws_bytes, void* stream, Shard sh,
+                         int with_shared, int out_f32) {
   if (!layer) return EXL3_ERR_ARG;
   const LayerView& L = layer->v;
   if (dt != EXL3_F16 && dt != EXL3_BF16) return EXL3_ERR_ARG;
@@ -266,6 +274,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   if (!x || !logits || !out) return EXL3_ERR_ARG;
   if (!aligned16(x) || !aligned16(out) || (residual && !aligned16(residual))) return EXL3_ERR_ARG;
   if (x == out) return EXL3_ERR_ARG;
+  const bool run_shared = layer->has_shared && with_shared;
   // the dense shared expert's gate/up launch has a grid z of 2 * ceil(T / 8)
   if (layer->has_shared && (size_t)T > (size_t)8 * (65535 / 2)) return EXL3_ERR_SHAPE;
   const FwdLayout f = fwd_layout(L, layer->has_shared, T, top_k);
@@ -297,7 +306,7 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   // mind SMs it occupies) instead of delaying the one-CTA routing kernel
   const float* sp = nullptr;
   int ns = 0;
-  if (layer->has_shared) {
+  if (run_shared) {
     if (cudaEventRecord(layer->fork, st) != cudaSuccess ||
         cudaStreamWaitEvent(layer->side, layer->fork, 0) != cudaSuccess)
       return EXL3_ERR_CUDA;
@@ -310,23 +319,61 @@ exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_d
   float* pair_rows = nullptr;
   int pair_splits = 1;
   if (use_gemm(L, T, kp, path)) {
-    if (launch_moe_gemm(L, x, bf16, T, kp, rb, base + f.gemv, ev, &pair_rows, st) != cudaSuccess)
+    if (launch_moe_gemm(L, x, bf16, T, kp, rb, base + f.gemv, ev, &pair_rows, sh, st) !=
+        cudaSuccess)
       return EXL3_ERR_CUDA;
   } else {
     GemvBuffers gb{};
     gemv_carve(base + f.gemv, T, kp, L.E, L.H, L.I, &gb);
-    if (launch_moe_gemv(L, x, bf16, T, kp, rb, gb, ev, st) != cudaSuccess) return EXL3_ERR_CUDA;
+    if (launch_moe_gemv(L, x, bf16, T, kp, rb, gb, ev, sh, st) != cudaSuccess) return EXL3_ERR_CUDA;
     pair_rows = gb.r;
     pair_splits = gb.ns_d;
   }
 
-  if (layer->has_shared && cudaStreamWaitEvent(st, layer->join, 0) != cudaSuccess)
+  if (run_shared && cudaStreamWaitEvent(st, layer->join, 0) != cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(6);
-  if (launch_combine(pair_rows, pair_splits, T, kp, L.H, sp, ns, residual, out, bf16, st) !=
-      cudaSuccess)
+  if (launch_combine(pair_rows, pair_splits, T, kp, L.H, rb.ids, sh, sp, ns,
+                     out_f32 ? nullptr : residual, out, bf16, out_f32, st) != cudaSuccess)
     return EXL3_ERR_CUDA;
   rec(7);
+  return EXL3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+exl3_status exl3_moe_forward_ex(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
+                                const float* logits, int T, int top_k, const void* residual,
+                                void* out, int path, void* ws, size_t ws_bytes, void* stream) {
+  if (!layer) return EXL3_ERR_ARG;
+  return forward_impl(layer, x, dt, logits, T, top_k, residual, out, path, ws, ws_bytes, stream,
+                      Shard{0, layer->v.E}, 1, 0);
+}
+
+exl3_status exl3_moe_forward_experts(const exl3_layer_t* layer, const void* x, exl3_dtype dt,
+                                     const float* logits, int T, int top_k, int expert_begin,
+                                     int expert_end, int with_shared, float* out, int path,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (!layer) return EXL3_ERR_ARG;
+  if (expert_begin < 0 || expert_end > layer->v.E || expert_begin > expert_end)
+    return EXL3_ERR_ARG;
+  if (with_shared != 0 && with_shared != 1) return EXL3_ERR_ARG;
+  return forward_impl(layer, x, dt, logits, T, top_k, nullptr, out, path, ws, ws_bytes, stream,
+                      Shard{expert_begin, expert_end}, with_shared, 1);
+}
+
+exl3_status exl3_round_output(const float* y, int T, int H, const void* residual, exl3_dtype dt,
+                              void* out, void* stream) {
+  if (dt != EXL3_F16 && dt != EXL3_BF16) return EXL3_ERR_ARG;
+  if (T < 0 || H <= 0 || H % 4) return EXL3_ERR_SHAPE;
+  if (T == 0) return EXL3_OK;
+  if (!y || !out || !aligned16(y) || !aligned16(out) || (residual && !aligned16(residual)))
+    return EXL3_ERR_ARG;
+  if (launch_round_output(y, T, H, residual, out, dt == EXL3_BF16,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXL3_ERR_CUDA;
   return EXL3_OK;
 }
 

@@ -941,11 +941,12 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // chosen from its max |x| (undone in the epilogue).  H is a multiple of 128.
 __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
     const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
-    uint16_t* __restrict__ xg, float* __restrict__ xinv) {
+    const int32_t* pos_lo, const int32_t* pos_hi, uint16_t* __restrict__ xg,
+    float* __restrict__ xinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  if (pos >= P) return;
+  if (pos >= P || pos < *pos_lo || pos >= *pos_hi) return;  // outside the call's experts
   const int t = seg_pairs[pos] / k;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
@@ -1006,12 +1007,13 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
 template <int ROT, int ACT8>
 __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_split_kernel(
     const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
-    const int32_t* ids, const uint16_t* __restrict__ suh_g, const uint16_t* __restrict__ suh_u,
+    const int32_t* pos_lo, const int32_t* pos_hi, const int32_t* ids,
+    const uint16_t* __restrict__ suh_g, const uint16_t* __restrict__ suh_u,
     void* __restrict__ xg, float* __restrict__ xinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  if (pos >= P) return;
+  if (pos >= P || pos < *pos_lo || pos >= *pos_hi) return;  // outside the call's experts
   const int pr = seg_pairs[pos];
   const int t = pr / k, e = ids[pr];
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
@@ -1128,12 +1130,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_split_kernel(
 template <int ROT, int ACT8>
 __global__ void __launch_bounds__(kRowWarps * 32) swiglu_rows_kernel(
     const float* __restrict__ gu, size_t n_pos, int I, const int32_t* seg_pairs,
-    const int32_t* ids, const uint16_t* __restrict__ suh_d, void* __restrict__ hs,
-    float* __restrict__ hinv) {
+    const int32_t* pos_lo, const int32_t* pos_hi, const int32_t* ids,
+    const uint16_t* __restrict__ suh_d, void* __restrict__ hs, float* __restrict__ hinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const size_t pos = (size_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  if (pos >= n_pos) return;
+  if (pos >= n_pos || pos < (size_t)*pos_lo || pos >= (size_t)*pos_hi) return;
   const float4* gr = reinterpret_cast<const float4*>(gu + pos * I);
   const float4* ur = reinterpret_cast<const float4*>(gu + (n_pos + pos) * I);
   const int nv = I / 4;
@@ -1252,12 +1254,13 @@ __device__ int block_excl_scan(int v, int* s_warp, int* total) {
 }
 
 __global__ void __launch_bounds__(1024) build_tiles_kernel(int E, const int32_t* seg_offsets,
-                                                           int use_small, int32_t* tiles,
+                                                           int use_small, Shard sh, int32_t* tiles,
                                                            int32_t* tiles_s, int32_t* n_tiles) {
   pdl_wait();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
-  const int cnt = e < E ? seg_offsets[e + 1] - seg_offsets[e] : 0;
+  // experts outside the call's range get no tiles
+  const int cnt = e < E && e >= sh.e0 && e < sh.e1 ? seg_offsets[e + 1] - seg_offsets[e] : 0;
   const int nt = (cnt + kBN - 1) / kBN;
   const int last = nt > 0 ? cnt - (nt - 1) * kBN : 0;
   const int small = use_small && nt > 0 && last <= kSM ? 1 : 0;
@@ -1484,7 +1487,7 @@ size_t gemm_scratch_bytes(int T, int top_k, int E, int H, int I, int had, int ac
 
 cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
                             const RouteBuffers& rb, void* ws, const cudaEvent_t* ev, float** r_out,
-                            cudaStream_t st) {
+                            Shard sh, cudaStream_t st) {
   auto rec = [&](int i) {
     if (ev && ev[i]) record_stage_event(ev[i], st);
   };
@@ -1516,8 +1519,11 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   // (the small-tile kernel needs H and I to be multiples of 256; otherwise
   // every tile takes the big-tile kernel)
   const bool small_ok = L.H % kSN == 0 && L.I % kSN == 0;
+  // positions of the call's experts: [seg_offsets[e0], seg_offsets[e1])
+  const int32_t* pos_lo = rb.seg_offsets + sh.e0;
+  const int32_t* pos_hi = rb.seg_offsets + sh.e1;
   if ((err = launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, st, L.E,
-                        (const int32_t*)rb.seg_offsets, (int)small_ok, tiles, tiles_s, ntiles)) !=
+                        (const int32_t*)rb.seg_offsets, (int)small_ok, sh, tiles, tiles_s, ntiles)) !=
       cudaSuccess)
     return err;
   if (L.mixed) {
@@ -1557,15 +1563,15 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   if (a8) {
     auto kfn = L.had ? gather_rows_split_kernel<1, 1> : gather_rows_split_kernel<0, 1>;
     err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H, top_k, P,
-                     (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids, L.suh[0], L.suh[1],
-                     (void*)xg, xinv);
+                     (const int32_t*)rb.seg_pairs, pos_lo, pos_hi, (const int32_t*)rb.ids,
+                     L.suh[0], L.suh[1], (void*)xg, xinv);
   } else if (split) {
     err = launch_pdl(gather_rows_split_kernel<1, 0>, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
-                     x, x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
-                     L.suh[0], L.suh[1], (void*)xg, xinv);
+                     x, x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi,
+                     (const int32_t*)rb.ids, L.suh[0], L.suh[1], (void*)xg, xinv);
   } else
     err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
-                     L.H, top_k, P, (const int32_t*)rb.seg_pairs, xg, xinv);
+                     L.H, top_k, P, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi, xg, xinv);
   note_launches(2);
   if (err != cudaSuccess) return err;
   rec(2);
@@ -1606,8 +1612,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     auto kfn = L.had ? (a8 ? swiglu_rows_kernel<1, 1> : swiglu_rows_kernel<1, 0>)
                      : (a8 ? swiglu_rows_kernel<0, 1> : swiglu_rows_kernel<0, 0>);
     err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, (const float*)gu_buf,
-                     (size_t)P, L.I, (const int32_t*)rb.seg_pairs, (const int32_t*)rb.ids,
-                     L.suh[2], (void*)hs, hinv);
+                     (size_t)P, L.I, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi,
+                     (const int32_t*)rb.ids, L.suh[2], (void*)hs, hinv);
   }
   note_launches(1);
   if (err != cudaSuccess) return err;

@@ -163,13 +163,15 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
                                                         int H, int k, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_g,
                                                         const uint16_t* __restrict__ suh_u,
-                                                        int had, int act8, uint32_t* __restrict__ xs,
+                                                        int had, int act8, Shard sh,
+                                                        uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
   const int p = rb.seg_pairs[pos];
   const int t = p / k, e = rb.ids[p];
+  if (e < sh.e0 || e >= sh.e1) return;  // another call's expert (whole CTA)
   int g, slot;
   group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
   const uint4* xv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
@@ -243,12 +245,14 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
 __global__ void __launch_bounds__(256) prep_down_kernel(const float* __restrict__ gu, int ns,
                                                         size_t n_pos, int I, RouteBuffers rb,
                                                         const uint16_t* __restrict__ suh_d,
-                                                        int had, int act8, uint32_t* __restrict__ xs,
+                                                        int had, int act8, Shard sh,
+                                                        uint32_t* __restrict__ xs,
                                                         float* __restrict__ xs_inv) {
   pdl_wait();
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
   const int e = rb.ids[rb.seg_pairs[pos]];
+  if (e < sh.e0 || e >= sh.e1) return;  // another call's expert (whole CTA)
   int g, slot;
   group_of(rb.seg_offsets, rb.group_off, e, pos, &g, &slot);
   const uint4* sd = reinterpret_cast<const uint4*>(suh_d + (size_t)e * I);
@@ -381,7 +385,8 @@ struct GemvParams {
   const uint32_t* xs;      // [group][nproj][in/16][8][16] fp16x2
   const float* xs_inv;     // [pos][nproj]
   const int32_t* groups;   // [g][4] {expert, pos0, count, 0}
-  const int32_t* n_groups; // device scalar
+  const int32_t* g_begin;  // device scalar: first group of the call's expert range
+  const int32_t* n_groups; // device scalar: end of the range's groups
   const int32_t* seg_pairs;
   const float* wts;        // router weights by pair id (down launch)
   float* gu_out;           // gate/up launch: [split][proj][pos][out]
@@ -404,13 +409,14 @@ struct GemvParams {
 __global__ void __launch_bounds__(256) width_lists_kernel(const int32_t* __restrict__ n_groups,
                                                           const int32_t* __restrict__ groups,
                                                           const int32_t* __restrict__ kt,
-                                                          int cap_gu, int cap_d,
+                                                          int cap_gu, int cap_d, Shard sh,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ entries) {
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= 3 * n_groups[0]) return;
   const int g = i / 3, pg = i % 3;
+  if (groups[4 * g] < sh.e0 || groups[4 * g] >= sh.e1) return;  // another call's expert
   const int w = kt[(size_t)groups[4 * g] * 3 + pg] - 2;
   const int launch = pg == 2 ? 1 : 0;
   const int cap = launch ? cap_d : cap_gu;
@@ -447,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
   const int strips = p.out / 128;
   const int nblk = p.in / 16;
   const int bps = nblk / p.nsplit;   // blocks (jobs) per item, >= kStages - 1
-  const int n_items = (p.entries ? p.n_entries[0] : p.n_groups[0] * p.nproj) * p.nsplit * strips;
+  const int g_first = p.g_begin[0];
+  const int n_items =
+      (p.entries ? p.n_entries[0] : (p.n_groups[0] - g_first) * p.nproj) * p.nsplit * strips;
   const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
 
   // item id -> (group, projection, split, strip); consecutive ids are
@@ -462,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
       pj = p.entries[2 * r + 1];
     } else {
       pj = r % p.nproj;
-      g = r / p.nproj;
+      g = g_first + r / p.nproj;
     }
   };
   // first code word of projection pj of expert e
@@ -743,7 +751,7 @@ void gemv_carve(void* ws, int T, int top_k, int E, int H, int I, GemvBuffers* gb
 
 cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T, int top_k,
                             const RouteBuffers& rb, const GemvBuffers& gb, const cudaEvent_t* ev,
-                            cudaStream_t st) {
+                            Shard sh, cudaStream_t st) {
   auto rec = [&](int i) {
     if (ev && ev[i]) record_stage_event(ev[i], st);
   };
@@ -755,12 +763,12 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
     const int threads = (int)(3 * G);
     err = launch_pdl(width_lists_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st,
                      (const int32_t*)(rb.group_off + L.E), (const int32_t*)rb.groups, L.d_kt,
-                     (int)(2 * G), (int)G, gb.n_entries, gb.entries);
+                     (int)(2 * G), (int)G, sh, gb.n_entries, gb.entries);
     note_launches(1);
     if (err != cudaSuccess) return err;
   }
   err = launch_pdl(gather_xs_kernel, dim3(P), dim3(input_pass_threads(L.H)), 0, st, x,
-                   x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, L.act8, gb.xs_gu,
+                   x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, L.act8, sh, gb.xs_gu,
                    gb.xs_gu_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
@@ -773,7 +781,8 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
   gu.svh[0] = L.svh[0]; gu.svh[1] = L.svh[1];
   gu.xs = gb.xs_gu; gu.xs_inv = gb.xs_gu_inv;
-  gu.groups = rb.groups; gu.n_groups = rb.group_off + L.E;
+  // the call's groups: those of experts e0 .. e1 - 1 (groups are in expert order)
+  gu.groups = rb.groups; gu.g_begin = rb.group_off + sh.e0; gu.n_groups = rb.group_off + sh.e1;
   gu.seg_pairs = rb.seg_pairs; gu.wts = rb.w; gu.gu_out = gb.gu; gu.n_pos = (size_t)P;
   gu.work = gb.counters; gu.nsplit = gb.ns_gu; gu.proj0 = 0;
   const int ub_gu = (int)(G * 2 * (L.I / 128) * gu.nsplit);
@@ -794,7 +803,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   rec(3);
 
   err = launch_pdl(prep_down_kernel, dim3(P), dim3(input_pass_threads(L.I)), 0, st, gb.gu,
-                   gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, L.act8, gb.xs_d, gb.xs_d_inv);
+                   gb.ns_gu, (size_t)P, L.I, rb, L.suh[2], L.had, L.act8, sh, gb.xs_d, gb.xs_d_inv);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(4);
@@ -804,7 +813,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   dn.in = L.I; dn.out = L.H; dn.nproj = 1; dn.mult = L.mult;
   dn.svh[0] = L.svh[2];
   dn.xs = gb.xs_d; dn.xs_inv = gb.xs_d_inv;
-  dn.groups = rb.groups; dn.n_groups = rb.group_off + L.E;
+  dn.groups = rb.groups; dn.g_begin = rb.group_off + sh.e0; dn.n_groups = rb.group_off + sh.e1;
   dn.seg_pairs = rb.seg_pairs; dn.wts = rb.w; dn.r_out = gb.r; dn.n_pos = (size_t)P;
   dn.work = gb.counters + 3; dn.nsplit = gb.ns_d; dn.proj0 = 2;
   const int ub_d = (int)(G * (L.H / 128) * dn.nsplit);
