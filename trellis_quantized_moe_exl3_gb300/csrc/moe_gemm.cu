@@ -10,26 +10,32 @@
 // One CTA = (token tile of <= 512 positions of one expert, projection,
 // 128-output strip).  D[o][n] = sum_i W[i][o] x[n][i] with A = decoded
 // weights (M = 128 outputs, MN-major in shared memory) and B = activation rows
-// (N = tokens, K-major, loaded by TMA with 128-byte swizzle); fp16 operands,
-// fp32 accumulators in TMEM: two 256-column accumulators, so every decoded
-// weight serves up to 512 tokens.
-//   warps 0..kDec-1  decode: each takes one 16-input block of a 64-input K
-//              step (kDec/4 K steps in flight), loads its code row one job
-//              ahead into registers (pulled into L2 8 jobs ahead), hashes each
-//              32-bit window once, sums the codebook halves into fp16 (E4M3
-//              rule if set), applies suh and stores 16-byte chunks into the
-//              swizzled A stage;
+// (N = tokens, K-major, loaded by TMA with 128-byte swizzle; each CTA loads
+// its own boxes, the neighbouring strips' loads mostly hit L2); fp16 or E4M3
+// operands (kind::f16 or kind::f8f6f4), fp32 accumulators in TMEM: two
+// 256-column accumulators, so every decoded weight serves up to 512 tokens.
+//   warps 0..kDec-1  decode: they take the tile's 16-input blocks
+//              round-robin (block j = warp + n kDec), load a block's code row
+//              one job ahead into registers (pulled into L2 8 jobs ahead),
+//              hash each 32-bit window once, sum the codebook halves into
+//              fp16 (E4M3 rule if set), apply suh (fp16 operands, format v1)
+//              or keep E4M3 bytes (FP8 operands), and store 16-byte chunks
+//              into the swizzled A stage;
 //   warp kDec  TMA producer of the B stages, and TMEM allocator;
 //   warp kDec+1  one thread issues tcgen05.mma and commits stage releases.
 // The epilogue (the decoder warps) reads TMEM: gate/up launch -> svh * acc per
-// position (SwiGLU follows in the down projection's input pass); down launch
-// -> router weight * svh * acc into the pair's own row (no atomics).
+// position, or, fused (format v1, fp16 operands, one width), gate and up of
+// the same 64 outputs in one CTA (A rows 0-63 and 64-127) and h = silu(g) u
+// written as fp16; down launch -> router weight * svh * acc into the pair's
+// own row (no atomics).  Every pipeline wait is bounded; a role whose wait
+// gives up stops issuing and unwinds (see pipe_wait).
 //
-// Format v2 (Hadamard rotation): suh cannot be folded into the weights, since
-// the rotation sits between it and the codes, so the input passes apply it
-// and rotate each 128-input block (gate and up then have separate activation
-// rows, [P + pos] for up); the decoders multiply by 1; the epilogue rotates
-// each 128-output block through shared memory before svh.
+// Format v2 (Hadamard rotation) and FP8 operands: suh cannot be folded into
+// the weights (the rotation sits between it and the codes; an E4M3 value
+// times suh is no E4M3 value), so the input passes apply it (and rotate each
+// 128-input block), gate and up have separate activation rows ([P + pos] for
+// up), and the h pass runs after the gate/up launch; the format v2 epilogue
+// rotates each 128-output block through shared memory before svh.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -103,7 +109,29 @@ struct GemmParams {
   const int32_t* n_entries;
   const unsigned long long* off;  // [E][3] code word offsets, or null: stride * e
   int proj0;                // global index of this launch's projection 0 (0 or 2)
+  // SwiGLU in the gate/up epilogue (format v1, fp16 operands, one width):
+  // each CTA holds gate and up of the same outputs and writes fp16 h
+  int fused;
+  uint16_t* h_out;          // [pos][out] fp16 h, times 2^e of its row
+  float* hinv;              // [pos] 2^-e (a power of two), written by the chunk-0 CTAs
+  const float* hb;          // [E] bound on |h| / |x_t|_1^2 per expert
+  const float* l1;          // [T] |x_t|_1
+  int top_k;                // pairs per token (position -> token)
 };
+
+// Fused SwiGLU: the power-of-two scale 2^e of position pos's h row, from the
+// bound hb[e] |x_t|_1^2 on |h| (see side_bound_kernel): the bound times 2^e
+// stays below 2^15, so fp16 h never overflows; a power-of-two scale does not
+// change the relative rounding of normal fp16 values.
+__device__ __forceinline__ float h_row_scale(const GemmParams& p, int e, int pos) {
+  const float l = p.l1[p.seg_pairs[pos] / p.top_k];
+  const float bound = p.hb[e] * l * l;
+  int eh = 0;
+  if (!isfinite(bound)) eh = -100;
+  else if (bound > 0.0f) eh = 14 - ilogbf(bound);
+  eh = eh < -100 ? -100 : (eh > 100 ? 100 : eh);
+  return ldexpf(1.0f, eh);
+}
 
 // (tile, projection) of the CTA's work unit u (its index over strips): from
 // the width's list in mixed mode, else u = tile * nproj + projection.  False
@@ -125,6 +153,32 @@ __device__ __forceinline__ const uint16_t* gemm_expert_codes(const GemmParams& p
   return (pj ? p.codes[1] : p.codes[0]) +
          (p.off ? (size_t)p.off[(size_t)e * 3 + p.proj0 + pj]
                 : (pj ? p.stride[1] : p.stride[0]) * (size_t)e);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// 8 activations (fp16 or bf16 bits) as floats.
+__device__ __forceinline__ void act8(const uint4& r, int bf16, float (&f)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+    if (bf16) {
+      f[2 * i] = __uint_as_float(lo << 16);
+      f[2 * i + 1] = __uint_as_float(hi << 16);
+    } else {
+      f[2 * i] = __half2float(__ushort_as_half((unsigned short)lo));
+      f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)hi));
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Pipeline wait of one CTA role.  A false return means: stop issuing work
@@ -309,7 +363,9 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  const int strips = p.out / 128;
+  // fused gate/up: 64 outputs of each projection per CTA (A rows 0-63 gate,
+  // 64-127 up, against the same activation rows)
+  const int strips = p.out / (p.fused ? 64 : 128);
   const int s = blockIdx.x % strips;
   pdl_wait();
   int tile, pj;
@@ -356,9 +412,13 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     const int pos = pos0 + n;
     float sc = p.xinv[xrow0 + n];
     int pid = 0;
-    if (!p.gu_out) {
+    if (p.r_out) {  // down launch: the pair's row and router weight
       pid = p.seg_pairs[pos];
       sc *= p.wts[pid];
+    } else if (p.fused) {  // fused gate/up: the scale of h's row, 2^e
+      const float hs = h_row_scale(p, e, pos);
+      if (s == 0) p.hinv[pos] = 1.0f / hs;  // for the down launch
+      pid = __float_as_int(hs);
     }
     s_scale[n] = sc;
     s_pid[n] = pid;
@@ -453,8 +513,19 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     // j / kJobs, block j % kJobs of it); warp w takes j = w, w + kDec, ...
     const int g = OP8 ? dec_tile8(lane) : dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
-    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
-                           (size_t)8 * s * 32 * K;
+    // this lane's tile: tile g of the strip, or (fused) tile g & 3 of the
+    // 64-output chunk of gate (g < 4) or up (g >= 4)
+    const int pg = p.fused ? g >> 2 : pj;
+    const int tcol = p.fused ? 4 * s + (g & 3) : 8 * s + g;
+    const uint8_t* lbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pg)) +
+                           ((size_t)tcol * 4 + c) * 8 * K;
+    // the 16-input block rows this warp pulls into L2: one strip, or (fused)
+    // the gate half (lanes 0-15) and the up half (lanes 16-31)
+    const int lpf = p.fused ? lane & 15 : lane;
+    const uint8_t* pbase =
+        reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, p.fused ? lane >> 4 : pj)) +
+        (size_t)(p.fused ? 4 * s : 8 * s) * 32 * K + lpf * 128;
+    const int pf_bytes = (p.fused ? 4 : 8) * 32 * K;
     const int n_jobs = nks * kJobs;
     const int n_my = warp < n_jobs ? (n_jobs - warp + kDec - 1) / kDec : 0;
     // lane-constant swizzled offsets of this lane's output chunks in a block:
@@ -477,19 +548,19 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     // chunk); the code row of block j of the tile is row j of the expert
     auto lane_codes = [&](int n) {
       const int j = warp + n * kDec;
-      return reinterpret_cast<const uint16_t*>(cbase + (size_t)j * row_bytes) + (g * 4 + c) * 4 * K;
+      return reinterpret_cast<const uint16_t*>(lbase + (size_t)j * row_bytes);
     };
     // code rows are pulled into L2 kL2Ahead jobs ahead, so the register
     // prefetch one job ahead hits L2
     constexpr int kL2Ahead = 8;
     auto prefetch_l2 = [&](int n) {
-      if (n < n_my && lane * 128 < C::kCodeChunk) {
-        const uint8_t* a = cbase + (size_t)(warp + n * kDec) * row_bytes + lane * 128;
+      if (n < n_my && lpf * 128 < pf_bytes) {
+        const uint8_t* a = pbase + (size_t)(warp + n * kDec) * row_bytes;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
       }
     };
     for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
-    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + c;
+    const uint16_t* suh_e = (pg ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + c;
     // suh of this lane's 4 inputs of a block (inputs 16 j + c + 4 jh + 8 hf),
     // loaded one job ahead
     uint32_t s2n[4];
@@ -537,6 +608,42 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
     const int o = 128 * s + 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh_e = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out;
+    if (live && p.fused) {
+      // SwiGLU: TMEM lanes 0-63 hold gate outputs 0-63 of the 64-output
+      // chunk, lanes 64-127 the up outputs of the same channels.  Per 16
+      // token columns the 4 warps of a column group stage their scaled
+      // values in shared memory (the A ring is idle; [row][17] floats,
+      // conflict free both ways); then each warp takes 4 of the columns, lane
+      // l forms h = silu(g) u for channels l and l + 32, scales it by the
+      // row's 2^e and the warp stores 64 consecutive fp16 outputs per token.
+      float* xbuf = reinterpret_cast<float*>(smem) + cgrp * (128 * 17);
+      const int row = 32 * q4 + lane;  // TMEM lane = A row
+      const float svf = __half2float(__ushort_as_half(
+          p.svh[q4 >> 1][(size_t)e * p.out + 64 * s + (row & 63)]));
+      for (int c0 = 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
+        float a0[16];
+        tmem_ld16(trow + c0, a0);
+        tmem_ld_wait(a0);
+#pragma unroll
+        for (int i = 0; i < 16; i++) xbuf[row * 17 + i] = a0[i] * svf;
+        named_bar_sync(1 + cgrp, 128);
+#pragma unroll
+        for (int tt = 0; tt < 4; tt++) {
+          const int cl = 4 * q4 + tt, n = c0 + cl;
+          if (n < cnt) {
+            const float sc = s_scale[n], hsc = __int_as_float(s_pid[n]);
+            uint16_t* dst = p.h_out + (size_t)(pos0 + n) * p.out + 64 * s;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+              const int ch = lane + 32 * hh;
+              const float gv = xbuf[ch * 17 + cl] * sc, uv = xbuf[(64 + ch) * 17 + cl] * sc;
+              dst[ch] = __half_as_ushort(__float2half_rn(silu_f(gv) * uv * hsc));
+            }
+          }
+        }
+        named_bar_sync(1 + cgrp, 128);  // the buffer is refilled by the next chunk
+      }
+    }
     if (live && p.had) {
       // the A ring is idle once the accumulator is complete
       float* xbuf = reinterpret_cast<float*>(smem) + cgrp * (128 * 17);
@@ -553,7 +660,7 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
       }
     }
     const float sv = __half2float(__ushort_as_half(svh_e[o]));
-    for (int c0 = p.had || !live ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
+    for (int c0 = p.had || p.fused || !live ? cnt : 16 * cgrp; c0 < cnt; c0 += 16 * (kDec / 4)) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait(a0);
@@ -562,7 +669,7 @@ __global__ void __launch_bounds__(OpT<OP8>::kThreads, 1)
         const int n = c0 + i;
         if (n < cnt) {
           const float v = a0[i] * s_scale[n] * sv;
-          if (p.gu_out)
+          if (!p.r_out)
             p.gu_out[((size_t)pj * p.n_pos + pos0 + n) * p.out + o] = v;
           else
             p.r_out[(size_t)s_pid[n] * p.out + o] = v;
@@ -616,7 +723,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  const int chunks = p.out / kSN;
+  // fused gate/up: 128 outputs of each projection per CTA (B columns 0-127
+  // gate, 128-255 up)
+  const int chunks = p.out / (p.fused ? kSN / 2 : kSN);
   const int s = blockIdx.x % chunks;
   pdl_wait();
   int tile, pj;
@@ -659,9 +768,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int pos = pos0 + n;
     float sc = p.xinv[xrow0 + n];
     int pid = 0;
-    if (!p.gu_out) {
+    if (p.r_out) {  // down launch: the pair's row and router weight
       pid = p.seg_pairs[pos];
       sc *= p.wts[pid];
+    } else if (p.fused) {  // fused gate/up: the scale of h's row, 2^e
+      const float hs = h_row_scale(p, e, pos);
+      if (s == 0) p.hinv[pos] = 1.0f / hs;  // for the down launch
+      pid = __float_as_int(hs);
     }
     s_scale[n] = sc;
     s_pid[n] = pid;
@@ -746,8 +859,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int ks0 = warp / kSJobs;
     const int g = OP8 ? dec_tile8(lane) : dec_tile(lane), c = lane & 3;
     const size_t row_bytes = (size_t)(p.out / 16) * 32 * K;
-    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pj)) +
-                           (size_t)8 * (2 * s + half) * 32 * K;
+    // code strip of this warp: strip 2s + half, or (fused) strip s of gate
+    // (half 0) or up (half 1)
+    const int pg = p.fused ? half : pj;
+    const uint8_t* cbase = reinterpret_cast<const uint8_t*>(gemm_expert_codes(p, e, pg)) +
+                           (size_t)8 * (p.fused ? s : 2 * s + half) * 32 * K;
     const int n_my = (nks - ks0 + kSPar - 1) / kSPar;
     int off[8], off8[4];
 #pragma unroll
@@ -779,7 +895,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     };
     for (int n = 0; n < kL2Ahead; n++) prefetch_l2(n);
-    const uint16_t* suh_e = (pj ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
+    const uint16_t* suh_e = (pg ? p.suh[1] : p.suh[0]) + (size_t)e * p.in + 16 * blk + c;
     uint32_t s2n[4];
     auto load_suh = [&](int n) {
       const int ks = ks0 + n * kSPar;
@@ -829,6 +945,47 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int n = (tm == 128 ? 32 : 16) * q4 + lane;  // token of this lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const uint16_t* svh = (pj ? p.svh[1] : p.svh[0]) + (size_t)e * p.out + kSN * s;
+    if (live && p.fused) {
+      // SwiGLU: this lane's token has gate output 128 s + j in column j and
+      // up output 128 s + j in column 128 + j; warp (q4, cg) takes outputs
+      // 32 cg .. 32 cg + 31 of the chunk and stores 32 fp16 h of its token
+      const uint16_t* svg = p.svh[0] + (size_t)e * p.out + 128 * s;
+      const uint16_t* svu = p.svh[1] + (size_t)e * p.out + 128 * s;
+#pragma unroll
+      for (int hc = 0; hc < 2; hc++) {
+        const int c0 = 32 * cg + 16 * hc;
+        float ag[16], au[16];
+        tmem_ld16(trow + c0, ag);
+        tmem_ld16(trow + 128 + c0, au);
+        tmem_ld_wait(ag);
+        tmem_ld_wait(au);
+        if (lane_live && n < cnt) {
+          const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(svg + c0));
+          const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(svg + c0 + 8));
+          const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(svu + c0));
+          const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(svu + c0 + 8));
+          const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          const float sc = s_scale[n], hsc = __int_as_float(s_pid[n]);
+          uint32_t hw[8];
+#pragma unroll
+          for (int j2 = 0; j2 < 8; j2++) {
+            float hv[2];
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+              const int j = 2 * j2 + b;
+              const float sg = __half2float(__ushort_as_half((unsigned short)(b ? gw[j2] >> 16 : gw[j2] & 0xFFFFu)));
+              const float su = __half2float(__ushort_as_half((unsigned short)(b ? uw[j2] >> 16 : uw[j2] & 0xFFFFu)));
+              hv[b] = silu_f(ag[j] * sc * sg) * (au[j] * sc * su) * hsc;
+            }
+            hw[j2] = pack_h2(hv[0], hv[1]);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.h_out + (size_t)(pos0 + n) * p.out + 128 * s + c0);
+          dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        }
+      }
+    }
     if (live && p.had) {
       // Format v2: warps (q4, 2b) and (q4, 2b + 1) hold the two halves of the
       // 128-output block b for the same 32 TMEM lanes (tokens).  Both stage
@@ -872,7 +1029,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
       }
     }
-    for (int c0 = p.had || !live ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
+    for (int c0 = p.had || p.fused || !live ? 64 * cg + 64 : 64 * cg; c0 < 64 * cg + 64; c0 += 16) {
       float a0[16];
       tmem_ld16(trow + c0, a0);
       tmem_ld_wait(a0);
@@ -888,7 +1045,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           const float sv = __half2float(__ushort_as_half((unsigned short)(j & 1 ? w2 >> 16 : w2 & 0xFFFFu)));
           v[j] = a0[j] * sc * sv;
         }
-        float* dst = p.gu_out ? p.gu_out + ((size_t)pj * p.n_pos + pos0 + n) * p.out
+        float* dst = !p.r_out ? p.gu_out + ((size_t)pj * p.n_pos + pos0 + n) * p.out
                               : p.r_out + (size_t)s_pid[n] * p.out;
         float4* d4 = reinterpret_cast<float4*>(dst + kSN * s + c0);
 #pragma unroll
@@ -911,30 +1068,64 @@ __global__ void __launch_bounds__(kSThreads, 1)
 constexpr int kRowWarps = 8;
 constexpr int kRowCache = 16;
 
-__device__ __forceinline__ float warp_max(float v) {
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
-// 8 activations (fp16 or bf16 bits) as floats.
-__device__ __forceinline__ void act8(const uint4& r, int bf16, float (&f)[8]) {
-  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+// Bound on |h| per expert for the fused SwiGLU epilogue: with |v| <= 4 (the
+// codebook, E4M3 rule included) and the fp16 rounding of v * suh, |g_o| <=
+// 8 max|suh_g| max|svh_g| |x|_1, likewise u, and |silu(g) u| <= |g| |u|, so
+// |h| <= hb[e] |x|_1^2 with hb[e] = 64 max|suh_g| max|svh_g| max|suh_u|
+// max|svh_u|.  CTAs 0 .. E-1: one expert each; the rest: |x_t|_1 of 8
+// tokens each (one warp per token).
+__global__ void __launch_bounds__(256) side_bound_kernel(const uint16_t* __restrict__ suh_g,
+                                                         const uint16_t* __restrict__ suh_u,
+                                                         const uint16_t* __restrict__ svh_g,
+                                                         const uint16_t* __restrict__ svh_u,
+                                                         int E, int H, int I,
+                                                         const void* __restrict__ x, int x_bf16,
+                                                         int T, float* __restrict__ hb,
+                                                         float* __restrict__ l1) {
+  pdl_wait();
+  __shared__ float s_w[4][8];
+  if ((int)blockIdx.x >= E) {
+    const int t = (blockIdx.x - E) * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
+    float a = 0.0f;
+    for (int v = lane; v < H / 8; v += 32) {
+      float f[8];
+      act8(src[v], x_bf16, f);
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-    if (bf16) {
-      f[2 * i] = __uint_as_float(lo << 16);
-      f[2 * i + 1] = __uint_as_float(hi << 16);
-    } else {
-      f[2 * i] = __half2float(__ushort_as_half((unsigned short)lo));
-      f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)hi));
+      for (int q = 0; q < 8; q++) a += fabsf(f[q]);
     }
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (lane == 0) l1[t] = a;
+    return;
   }
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
+  const int e = blockIdx.x;
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  auto fmax16 = [](float a, uint16_t b) { return fmaxf(a, fabsf(__half2float(__ushort_as_half(b)))); };
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    m[0] = fmax16(m[0], suh_g[(size_t)e * H + i]);
+    m[1] = fmax16(m[1], suh_u[(size_t)e * H + i]);
+  }
+  for (int i = threadIdx.x; i < I; i += blockDim.x) {
+    m[2] = fmax16(m[2], svh_g[(size_t)e * I + i]);
+    m[3] = fmax16(m[3], svh_u[(size_t)e * I + i]);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    m[q] = warp_max(m[q]);
+    if ((threadIdx.x & 31) == 0) s_w[q][threadIdx.x >> 5] = m[q];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = 64.0f;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      float a = 0.0f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); w++) a = fmaxf(a, s_w[q][w]);
+      r *= a;
+    }
+    hb[e] = r;
+  }
 }
 
 // Activation rows in position order, fp16 with a power-of-two scale per row
@@ -1454,7 +1645,7 @@ size_t max_tiles(int T, int E, int top_k) {
 }
 
 struct GemmLayout {
-  size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, counts, lists, total;
+  size_t xg, xinv, gu, hs, hinv, r, tiles, tiles_s, ntiles, counts, lists, hb, hl1, total;
 };
 
 // Format v2 and the FP8 operand mode keep separate gate and up activation
@@ -1475,6 +1666,8 @@ GemmLayout gemm_layout(int T, int top_k, int E, int H, int I, int had, int act8)
   g.ntiles = o; o += al(16);
   g.counts = o; o += al(12 * 4);  // mixed widths: list lengths
   g.lists = o; o += al((size_t)18 * (max_tiles(T, E, top_k) + E) * 4);
+  g.hb = o; o += al((size_t)E * 4);  // fused SwiGLU: per-expert bound on |h|
+  g.hl1 = o; o += al((size_t)T * 4);  // and per-token |x|_1
   g.total = o;
   return g;
 }
@@ -1493,6 +1686,9 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   };
   const int a8 = L.act8;
   const bool split = L.had || a8;  // separate gate and up activation rows
+  // SwiGLU in the gate/up epilogue: gate and up share the activation row
+  // (format v1, fp16 operands) and one code width
+  const bool fused = !split && !L.mixed;
   const int esize = a8 ? 1 : 2;
   const GemmLayout g = gemm_layout(T, top_k, L.E, L.H, L.I, L.had, a8);
   char* base = static_cast<char*>(ws);
@@ -1507,6 +1703,8 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   int32_t* ntiles = reinterpret_cast<int32_t*>(base + g.ntiles);
   int32_t* lcounts = reinterpret_cast<int32_t*>(base + g.counts);
   int32_t* lists = reinterpret_cast<int32_t*>(base + g.lists);
+  float* hb = reinterpret_cast<float*>(base + g.hb);
+  float* hl1 = reinterpret_cast<float*>(base + g.hl1);
   *r_out = r;
   const int P = T * top_k;
   const int mt = (int)max_tiles(T, L.E, top_k);
@@ -1569,9 +1767,16 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
     err = launch_pdl(gather_rows_split_kernel<1, 0>, dim3(row_blocks), dim3(kRowWarps * 32), 0, st,
                      x, x_bf16, L.H, top_k, P, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi,
                      (const int32_t*)rb.ids, L.suh[0], L.suh[1], (void*)xg, xinv);
-  } else
+  } else {
+    if (fused) {
+      err = launch_pdl(side_bound_kernel, dim3(L.E + (T + 7) / 8), dim3(256), 0, st, L.suh[0],
+                       L.suh[1], L.svh[0], L.svh[1], L.E, L.H, L.I, x, x_bf16, T, hb, hl1);
+      note_launches(1);
+      if (err != cudaSuccess) return err;
+    }
     err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
                      L.H, top_k, P, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi, xg, xinv);
+  }
   note_launches(2);
   if (err != cudaSuccess) return err;
   rec(2);
@@ -1581,8 +1786,16 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   gu.stride[0] = L.code_stride[0]; gu.stride[1] = L.code_stride[1];
   gu.suh[0] = L.suh[0]; gu.suh[1] = L.suh[1];
   gu.svh[0] = L.svh[0]; gu.svh[1] = L.svh[1];
-  gu.in = L.H; gu.out = L.I; gu.nproj = 2; gu.mult = L.mult;
-  gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.gu_out = gu_buf; gu.n_pos = (size_t)P;
+  gu.in = L.H; gu.out = L.I; gu.nproj = fused ? 1 : 2; gu.mult = L.mult;
+  gu.tiles = tiles; gu.n_tiles = ntiles; gu.xinv = xinv; gu.n_pos = (size_t)P;
+  gu.gu_out = fused ? nullptr : gu_buf;
+  gu.fused = fused;
+  gu.h_out = fused ? hs : nullptr;
+  gu.hinv = hinv;
+  gu.hb = hb;
+  gu.l1 = hl1;
+  gu.top_k = top_k;
+  gu.seg_pairs = rb.seg_pairs;
   gu.status = rb.status;
   gu.budget = kWaitBudgetCycles;
   gu.fault_ks = -1;
@@ -1608,15 +1821,15 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
   }
   rec(3);
 
-  {
+  if (!fused) {
     auto kfn = L.had ? (a8 ? swiglu_rows_kernel<1, 1> : swiglu_rows_kernel<1, 0>)
                      : (a8 ? swiglu_rows_kernel<0, 1> : swiglu_rows_kernel<0, 0>);
     err = launch_pdl(kfn, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, (const float*)gu_buf,
                      (size_t)P, L.I, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi,
                      (const int32_t*)rb.ids, L.suh[2], (void*)hs, hinv);
+    note_launches(1);
+    if (err != cudaSuccess) return err;
   }
-  note_launches(1);
-  if (err != cudaSuccess) return err;
   rec(4);
 
   GemmParams dn{};
