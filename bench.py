@@ -129,27 +129,20 @@ def expert_work(spec, counts, per: int):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant stage's launches in one step, from ncu captures of this bench
-# (decode: the GEMV gate/up and down launches; prefill: the big- and
-# small-tile tensor-core launches of each stage, captured on the 64-expert
-# case and scaled); reported only while the kernel sources hash to what was
-# captured (otherwise null).
+# dominant stage's launch in one decode step, from an ncu capture of this
+# bench's decode workload (the GEMV gate/up and down launches); reported
+# only while the kernel sources hash to what was captured (otherwise null).
+# The prefill stages have no full-size capture (their counters come from a
+# 64-expert case), so their traffic is null.
 NCU_TRAFFIC = {
-    ("decode", "gate_up"): 128.116736e6 + 4.404480e6,
-    ("prefill", "gate_up"): 4072320512,  # big-tile + small-tile launches
-    ("prefill", "down"): 2429370624,
-    ("decode", "down"): 63.692288e6 + 0.870144e6,
+    ("decode", "gate_up"): 128090880 + 4737792,
+    ("decode", "down"): 63690496 + 900608,
 }
 NCU_SOURCES = {
     "decode": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "d195d448e473addceaac4a0d4c850cd1e9550ed8",
-        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
-    },
-    "prefill": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemm.cu": "6b460aa5a90cb5bd2a19b8ac321fa9d9eacfb102",
-        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "4009ec5d411a93aadb8d82381585cf05645c8e6c",
-        "trellis_quantized_moe_exl3_gb300/csrc/umma.cuh": "b447c8cca474276a478c6b77fc3e35111d3004a0",
-        "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "90e55f7d8ddca6b4f57fedbba41ac44ecb974179",
+        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "450a003e19f51f8a4883ac21384c05d0d88eb99c",
+        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "2aea299283238ac179878ee331ce022a87044f62",
+        "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "1f11aa433c95c15ed0fd2ec1605b876b5f7100cc",
     },
 }
 
