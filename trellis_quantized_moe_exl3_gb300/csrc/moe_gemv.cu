@@ -38,6 +38,8 @@
 // rotates each item's partial sums over its 128-output strip (16 outputs of a
 // lane in registers, the 8 lane quads by shuffles) before svh; the rotation
 // is linear, so rotating every K-split partial equals rotating their sum.
+#include <math.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -680,14 +682,19 @@ cudaError_t dispatch_gemv(int K, int fp8, int had, const GemvParams& gp, int ite
              : dispatch_gemv_fmt<0>(K, fp8, gp, items_ub, st);
 }
 
-// K splits: the smallest power of two that gives ~8 items per resident warp
-// (2 CTAs of 8 warps on 152 SMs) for the upper bound on token groups, keeping
-// >= 8 blocks per item (more than any ring is deep) and at most 16 splits.
-int choose_nsplit(size_t groups_ub, int items_per_group, int nblk) {
-  const size_t target = (size_t)8 * 152 * 2 * kCW;
+// K splits: the largest power of two (at most 16, keeping >= 8 blocks per
+// item, more than any ring is deep) that keeps the expected items at or
+// below 4.5 per resident warp (2 CTAs of 8 warps on 152 SMs).  The expected
+// token groups are the expected distinct experts of P pairs over E experts,
+// E (1 - exp(-P / E)).  Measured on the decode (T 4) and verify (T 32)
+// layers: 3-4 items per warp balance the per-item overhead (prologue,
+// epilogue, partial rows) against the tail of the dynamic schedule.
+int choose_nsplit(size_t P, int E, int items_per_group, int nblk) {
+  const double groups = (double)E * (1.0 - exp(-(double)P / (double)E));
+  const double cap = 4.5 * 152 * 2 * kCW;
   int ns = 1;
   while (ns < 16 && nblk % (2 * ns) == 0 && nblk / (2 * ns) >= 8 &&
-         groups_ub * items_per_group * ns < target)
+         groups * items_per_group * (2 * ns) <= cap)
     ns *= 2;
   return ns;
 }
@@ -712,8 +719,8 @@ GemvLayout gemv_layout(int T, int top_k, int E, int H, int I) {
   GemvLayout g{};
   const size_t P = (size_t)T * top_k;
   const size_t G = max_groups(T, E, top_k);
-  g.ns_gu = choose_nsplit(G, 2 * (I / 128), H / 16);
-  g.ns_d = choose_nsplit(G, H / 128, I / 16);
+  g.ns_gu = choose_nsplit(P, E, 2 * (I / 128), H / 16);
+  g.ns_d = choose_nsplit(P, E, H / 128, I / 16);
   size_t o = 0;
   g.xs_gu = o; o += al(G * 2 * (H / 16) * kXsChunk);
   g.xs_gu_inv = o; o += al(P * 2 * 4);
