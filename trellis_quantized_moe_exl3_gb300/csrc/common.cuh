@@ -201,6 +201,25 @@ __device__ __forceinline__ uint32_t e4m3_byte_of(float a, float s, float r) {
   return b | (a < 0.0f ? 0x80u : 0u);
 }
 
+// Two elements at once (low byte = a0), the same decisions, cheaper: when
+// |p| >= 2^-6 (E4M3's normal range, where every rounding boundary is a float
+// whose 20 low mantissa bits are 0x80000) and p lies more than 5 ulps from
+// such a float, no boundary separates p from fp32(a / s) (2.5 ulps away at
+// most), so p itself is converted, two per instruction.  Any other element
+// (a quotient near a boundary, a small or zero one) takes e4m3_byte_of; rows
+// with many small elements (products such as h) do better with
+// e4m3_byte_of throughout.
+__device__ __forceinline__ bool e4m3_clear(float p) {
+  const uint32_t m = __float_as_uint(p) & 0x7FFFFFFFu;
+  return m >= 0x3C800000u && ((m & 0xFFFFFu) - 0x7FFFBu) > 10u;
+}
+__device__ __forceinline__ uint32_t e4m3_pair_of(float a0, float a1, float s, float r) {
+  const float p0 = a0 * r, p1 = a1 * r;
+  if (__builtin_expect(s > 0.0f && e4m3_clear(p0) && e4m3_clear(p1), 1))
+    return e4m3_pack2(p0, p1);
+  return e4m3_byte_of(a0, s, r) | (e4m3_byte_of(a1, s, r) << 8);
+}
+
 // The same element as a float (every E4M3 value is exact in fp16 and fp32).
 __device__ __forceinline__ float e4m3_value(float a, float s, float r) {
   uint32_t back;

@@ -1274,10 +1274,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_split_kernel(
     uint2* dg = reinterpret_cast<uint2*>(static_cast<uint8_t*>(xg) + (size_t)pos * H);
     uint2* du = reinterpret_cast<uint2*>(static_cast<uint8_t*>(xg) + ((size_t)P + pos) * H);
     auto q8 = [](const float (&f)[8], float sc, float rc) {
-      uint32_t w[2] = {0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 8; i++) w[i >> 2] |= e4m3_byte_of(f[i], sc, rc) << (8 * (i & 3));
-      return make_uint2(w[0], w[1]);
+      return make_uint2(e4m3_pair_of(f[0], f[1], sc, rc) | (e4m3_pair_of(f[2], f[3], sc, rc) << 16),
+                        e4m3_pair_of(f[4], f[5], sc, rc) | (e4m3_pair_of(f[6], f[7], sc, rc) << 16));
     };
     for (int v = lane; v < nv; v += 32) {
       float fg[8], fu[8];
@@ -1873,8 +1871,16 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const float* __
   for (int w = 0; w < (int)(blockDim.x >> 5); w++) am = fmaxf(am, s_w[w]);
   const float sc = e4m3_row_scale(am);
   const float rc = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    q[(size_t)blockIdx.x * n + i] = (uint8_t)e4m3_byte_of(row[i], sc, rc);
+  // pairs of elements, as the activation passes take them (an odd last one alone)
+  for (int i = 2 * threadIdx.x; i < n; i += 2 * blockDim.x) {
+    if (i + 1 < n) {
+      const uint32_t two = e4m3_pair_of(row[i], row[i + 1], sc, rc);
+      q[(size_t)blockIdx.x * n + i] = (uint8_t)(two & 0xFFu);
+      q[(size_t)blockIdx.x * n + i + 1] = (uint8_t)(two >> 8);
+    } else {
+      q[(size_t)blockIdx.x * n + i] = (uint8_t)e4m3_byte_of(row[i], sc, rc);
+    }
+  }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
 }  // namespace
