@@ -135,13 +135,13 @@ def expert_work(spec, counts, per: int):
 # The prefill stages have no full-size capture (their counters come from a
 # 64-expert case), so their traffic is null.
 NCU_TRAFFIC = {
-    ("decode", "gate_up"): 128090880 + 4737792,
-    ("decode", "down"): 63690496 + 900608,
+    ("decode", "gate_up"): 128089856 + 3795968,
+    ("decode", "down"): 63690752 + 617728,
 }
 NCU_SOURCES = {
     "decode": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "450a003e19f51f8a4883ac21384c05d0d88eb99c",
-        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "2aea299283238ac179878ee331ce022a87044f62",
+        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "cc2ae90b1afe401cc3c9eda130e7a6b0e7ae3824",
+        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "91ce3402e4abd315dd1aaa25eaa71d9884431157",
         "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "1f11aa433c95c15ed0fd2ec1605b876b5f7100cc",
     },
 }

@@ -516,6 +516,30 @@ def test_forward_argument_errors_leave_output():
     assert not bool((out == 7.0).all())
 
 
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 3e2])
+@pytest.mark.parametrize("path,a8", [(2, False), (2, True), (1, False)], ids=["gemm", "gemm_fp8", "gemv"])
+def test_forward_input_magnitudes(scale, path, a8):
+    """Activations far from N(0, 1): the fp16 operand scales (per-row powers
+    of two from the row maximum, and in the fused SwiGLU epilogue from the
+    bound hb[e] |x|_1^2 on |h|) and the FP8 row scales must keep the layer
+    within tolerance at any magnitude (|h| reaches ~1e9 at scale 300)."""
+    spec = synth.LayerSpec(seed=250, num_experts=8, hidden=512, inter=256, K=(4, 4, 3),
+                           fp8_round=True, act_fp8=a8)
+    hl = HostLayer(spec)
+    layer = hl.device()
+    T, k = (300, 4) if path == 2 else (20, 4)
+    x = synth.activations(251, T, spec.hidden, "bf16")
+    xs = (oracle.bf16_bits_to_f64(x) * scale)
+    x_bits = np.array([oracle.double_to_bf16(v) for v in xs.ravel()], np.uint16).reshape(xs.shape)
+    logits = synth.router_logits(251, T, 8, "zipf")
+    out = layer.forward(_act(x_bits, "bf16"), torch.from_numpy(logits).cuda(), k, path=path)
+    torch.cuda.synchronize()
+    ref = hl.oracle().forward(x_bits, True, logits, k)
+    assert np.isfinite(act_to_f64(out)).all()
+    assert_layer_close(act_to_f64(out), ref)
+    assert device_status(layer.workspace(T, k)) == 0
+
+
 # ------------------------------------------------------------------ FP8 x FP8 operands
 
 
