@@ -57,6 +57,8 @@ def parse():
                          "line's top-level numbers")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profilers)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the token count (small cases for profilers)")
     ap.add_argument("--layer", type=int, default=0, help="layer of a stacked workload (long)")
     ap.add_argument("--hadamard", action="store_true",
                     help="format v2: the workload's layer with the 128-point Hadamard rotation")
@@ -308,6 +310,8 @@ def pick_workload(args, name):
     if args.experts:
         spec = dataclasses.replace(spec, num_experts=args.experts)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-E{args.experts}")
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=args.tokens, name=f"{wl.name}-T{args.tokens}")
     if args.hadamard:
         spec = dataclasses.replace(spec, hadamard=True)
         wl = dataclasses.replace(wl, layers=(spec,), name=f"{wl.name}-hadamard")
@@ -575,7 +579,7 @@ def measure_workload(args, name, dev, world, rank, local):
                 "path": roof["path"], "launches_per_step": launches_per_step,
                 "stage_times": "separate graph with stage events" if stage_live else "eager re-run"},
     }
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not args.experts and not args.tokens:
         block["cpu_baseline"] = oracle_baseline(wl, spec, x_np, lg_np, 2, codes=codes)
     block["dtype"] = "e4m3" if spec.act_fp8 else "f16"
     del layer, d_codes, d_suh, d_svh, d_sw, ws, flush, g, g_stage
