@@ -40,7 +40,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 constexpr uint32_t kDefaultMcgMult = 0x9E3779B1u;
-constexpr int kRouteChunk = 128;   // tokens per routing CTA
+constexpr int kRouteChunk = 64;    // tokens per routing CTA
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kGroup = 8;          // tokens per GEMV token group (MMA N)

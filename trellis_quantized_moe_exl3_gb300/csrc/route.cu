@@ -216,11 +216,21 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, Ro
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   int tot = 0;
+  // (8 chunks per turn: their loads are issued together instead of one
+  // dependent load-store round trip per chunk)
+  constexpr int kB = 8;
   if (e < E) {
-    for (int c = 0; c < nchunks; c++) {
-      const int v = rb.chunk_counts[(size_t)c * E + e];
-      rb.chunk_counts[(size_t)c * E + e] = tot;
-      tot += v;
+    for (int c0 = 0; c0 < nchunks; c0 += kB) {
+      int v[kB];
+#pragma unroll
+      for (int i = 0; i < kB; i++)
+        v[i] = c0 + i < nchunks ? rb.chunk_counts[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kB; i++)
+        if (c0 + i < nchunks) {
+          rb.chunk_counts[(size_t)(c0 + i) * E + e] = tot;
+          tot += v[i];
+        }
     }
   }
   int total = 0, n_act = 0, n_grp = 0;
@@ -231,7 +241,15 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nchunks, Ro
   if (e < E) {
     rb.seg_offsets[e] = off;
     if (tot > 0) rb.active[1 + aidx] = e;
-    for (int c = 0; c < nchunks; c++) rb.chunk_counts[(size_t)c * E + e] += off;
+    for (int c0 = 0; c0 < nchunks; c0 += kB) {
+      int v[kB];
+#pragma unroll
+      for (int i = 0; i < kB; i++)
+        v[i] = c0 + i < nchunks ? rb.chunk_counts[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kB; i++)
+        if (c0 + i < nchunks) rb.chunk_counts[(size_t)(c0 + i) * E + e] = v[i] + off;
+    }
     write_groups(rb, e, off, tot, goff);
   }
   if (threadIdx.x == 0) {
