@@ -1144,19 +1144,30 @@ __global__ void __launch_bounds__(256) side_bound_kernel(const uint16_t* __restr
   }
 }
 
-// Activation rows in position order, fp16 with a power-of-two scale per row
-// chosen from its max |x| (undone in the epilogue).  H is a multiple of 128.
+// Format v1 input pass: one warp per token.  Its row (bf16 or fp16) is read
+// once, scaled to fp16 by the power of two that puts its amax in [2^14,
+// 2^15), and written to the positions of the token's pairs that fall in the
+// call's expert range (identical rows: the activation boxes of every segment
+// the token is in); xinv[pos] = the inverse scale.  (One warp per position
+// would read each token's row once per pair, and with the written rows
+// streaming through L2 those reads come from HBM.)
 __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
-    const void* __restrict__ x, int x_bf16, int H, int k, int P, const int32_t* seg_pairs,
-    const int32_t* pos_lo, const int32_t* pos_hi, uint16_t* __restrict__ xg,
-    float* __restrict__ xinv) {
+    const void* __restrict__ x, int x_bf16, int H, int k, int T,
+    const int32_t* __restrict__ pair_pos, const int32_t* pos_lo, const int32_t* pos_hi,
+    uint16_t* __restrict__ xg, float* __restrict__ xinv) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int pos = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  if (pos >= P || pos < *pos_lo || pos >= *pos_hi) return;  // outside the call's experts
-  const int t = seg_pairs[pos] / k;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lo = *pos_lo, hi = *pos_hi;
+  int my_pos = -1;  // lane j < k: position of pair t k + j, if in range
+  if (lane < k) {
+    const int ps = pair_pos[(size_t)t * k + lane];
+    if (ps >= lo && ps < hi) my_pos = ps;
+  }
+  const unsigned used = __ballot_sync(0xffffffffu, my_pos >= 0);
+  if (!used) return;  // none of this token's pairs is the call's
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H);
-  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
   const int nv = H / 8;  // 16-byte vectors per row
   uint4 c[kRowCache];
   float am = 0.0f;
@@ -1180,19 +1191,26 @@ __global__ void __launch_bounds__(kRowWarps * 32) gather_rows_kernel(
   am = warp_max(am);
   const int ex = fp16_scale_exp(am);
   const float sc = ldexpf(1.0f, ex);
-  auto put = [&](int v, const uint4& r) {
+  auto conv = [&](const uint4& r) {
     float f[8];
     act8(r, x_bf16, f);
-    dst[v] = make_uint4(pack_h2(f[0] * sc, f[1] * sc), pack_h2(f[2] * sc, f[3] * sc),
-                        pack_h2(f[4] * sc, f[5] * sc), pack_h2(f[6] * sc, f[7] * sc));
+    return make_uint4(pack_h2(f[0] * sc, f[1] * sc), pack_h2(f[2] * sc, f[3] * sc),
+                      pack_h2(f[4] * sc, f[5] * sc), pack_h2(f[6] * sc, f[7] * sc));
   };
 #pragma unroll
-  for (int i = 0; i < kRowCache; i++) {
-    const int v = i * 32 + lane;
-    if (v < nv) put(v, c[i]);
+  for (int i = 0; i < kRowCache; i++)
+    if (i * 32 + lane < nv) c[i] = conv(c[i]);
+  for (unsigned m = used; m; m &= m - 1) {
+    const int pos = __shfl_sync(0xffffffffu, my_pos, __ffs(m) - 1);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * H);
+#pragma unroll
+    for (int i = 0; i < kRowCache; i++) {
+      const int v = i * 32 + lane;
+      if (v < nv) dst[v] = c[i];
+    }
+    for (int v = kRowCache * 32 + lane; v < nv; v += 32) dst[v] = conv(src[v]);
+    if (lane == 0) xinv[pos] = ldexpf(1.0f, -ex);
   }
-  for (int v = kRowCache * 32 + lane; v < nv; v += 32) put(v, src[v]);
-  if (lane == 0) xinv[pos] = ldexpf(1.0f, -ex);
 }
 
 // Rows x * suh of gate and up for each position (gate rows at [pos], up rows
@@ -1788,8 +1806,9 @@ cudaError_t launch_moe_gemm(const LayerView& L, const void* x, int x_bf16, int T
       note_launches(1);
       if (err != cudaSuccess) return err;
     }
-    err = launch_pdl(gather_rows_kernel, dim3(row_blocks), dim3(kRowWarps * 32), 0, st, x, x_bf16,
-                     L.H, top_k, P, (const int32_t*)rb.seg_pairs, pos_lo, pos_hi, xg, xinv);
+    err = launch_pdl(gather_rows_kernel, dim3((unsigned)((T + kRowWarps - 1) / kRowWarps)),
+                     dim3(kRowWarps * 32), 0, st, x, x_bf16, L.H, top_k, T,
+                     (const int32_t*)rb.pair_pos, pos_lo, pos_hi, xg, xinv);
   }
   note_launches(2);
   if (err != cudaSuccess) return err;
