@@ -31,7 +31,7 @@
  * reference; the Hadamard matrix against scipy's Sylvester construction and a
  * closed-form rotated layer; the E4M3 activation operand against torch's
  * float8_e4m3fn conversion).  Compatibility with real EXL3/exlr8 checkpoints is unpinned: no
- * checkpoint or test vector exists for this build.
+ * checkpoint or test vector is available to check them against.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (contraction off so
  * that the fp32 routing arithmetic is the written sequence of roundings).
@@ -202,7 +202,7 @@ uint16_t oracle_weight_f16(uint32_t s, uint32_t mult, int fp8_round)
 
 /* Tile order "gb300_v1": position of weight t inside its 16x16 tile.
  * reading: the pages name tile orders (sm70_colmajor, sm80, strip-major) but
- * define none, so this build fixes its own.  t = 64*c + 8*r0 + 4*hf + j with
+ * define none, so the library fixes its own.  t = 64*c + 8*r0 + 4*hf + j with
  * c, j in 0..3, r0 in 0..7, hf in 0..1:
  *   output row  = r0 + 8*(j & 1)
  *   input col   = c + 4*(j >> 1) + 8*hf                                       */
