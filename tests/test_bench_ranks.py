@@ -73,3 +73,24 @@ def test_expert_work_accounting():
     want_t = H * I * (2 / bench.DECODE_PEAK[3] + 2 / bench.DECODE_PEAK[4] + 2 / bench.DECODE_PEAK[4])
     assert abs(dec_t["gate_up"] - want_t) < 1e-15
     assert code_b["down"] == H * I * 2 // 8 + H * I * 4 // 8 + 2 * (H + I) * 2
+
+
+def test_workload_overrides_for_profiling():
+    """--experts and --tokens shrink a workload (for profiler captures) and
+    rename it, leaving the other fields as they were."""
+    import argparse
+
+    import bench
+    from trellis_quantized_moe_exl3_gb300 import synth
+    args = argparse.Namespace(layer=0, experts=64, tokens=1024, hadamard=False,
+                              shared_coded=False, mixed=False)
+    wl, spec = bench.pick_workload(args, "prefill+fp8")
+    base = synth.WORKLOADS["prefill"]
+    assert wl.T == 1024 and spec.num_experts == 64
+    assert spec.act_fp8 and spec.fp8_round and spec.K == base.layers[0].K
+    assert wl.top_k == base.top_k and wl.routing == base.routing
+    assert "E64" in wl.name and "T1024" in wl.name
+    args = argparse.Namespace(layer=0, experts=0, tokens=0, hadamard=False,
+                              shared_coded=False, mixed=False)
+    wl, spec = bench.pick_workload(args, "prefill")
+    assert wl.T == base.T and spec.num_experts == base.layers[0].num_experts and not spec.act_fp8
