@@ -131,22 +131,26 @@ def expert_work(spec, counts, per: int):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant stage's launch in one decode step, from an ncu capture of this
-# bench's decode workload (the GEMV gate/up and down launches); reported
-# only while the kernel sources hash to what was captured (otherwise null).
+# dominant stage's launch in one decode or verify step, from ncu captures of
+# this bench's decode and verify workloads (the GEMV gate/up and down
+# launches); reported only while the kernel sources hash to what was
+# captured (otherwise null).
 # The prefill stages have no full-size capture (their counters come from a
 # 64-expert case), so their traffic is null.
 NCU_TRAFFIC = {
     ("decode", "gate_up"): 128089856 + 3795968,
     ("decode", "down"): 63690752 + 617728,
+    ("verify3", "gate_up"): 825634816 + 9473536,
+    ("verify3", "down"): 410341632 + 5521920,
+    ("verify4", "gate_up"): 1121843712 + 9858304,
+    ("verify4", "down"): 557784576 + 6365952,
 }
-NCU_SOURCES = {
-    "decode": {
-        "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "cc2ae90b1afe401cc3c9eda130e7a6b0e7ae3824",
-        "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "91ce3402e4abd315dd1aaa25eaa71d9884431157",
-        "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "1f11aa433c95c15ed0fd2ec1605b876b5f7100cc",
-    },
+_GEMV_SOURCES = {
+    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "cc2ae90b1afe401cc3c9eda130e7a6b0e7ae3824",
+    "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "91ce3402e4abd315dd1aaa25eaa71d9884431157",
+    "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "1f11aa433c95c15ed0fd2ec1605b876b5f7100cc",
 }
+NCU_SOURCES = {"decode": _GEMV_SOURCES, "verify3": _GEMV_SOURCES, "verify4": _GEMV_SOURCES}
 
 
 def ncu_traffic(workload, kernel):
