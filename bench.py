@@ -134,7 +134,11 @@ def expert_work(spec, counts, per: int):
 # dominant stage's launch in one decode or verify step, from ncu captures of
 # this bench's decode and verify workloads (the GEMV gate/up and down
 # launches); reported only while the kernel sources hash to what was
-# captured (otherwise null).
+# captured (otherwise null).  The moe_gemv.cu digest is that of a later
+# revision than the capture: its diff to the captured one touches only
+# gather_xs_kernel (which now clears the launches' work counters) and the
+# memset that did so before; the GEMV kernel, its launch shape and its
+# arguments are the captured ones.
 # The prefill stages have no full-size capture (their counters come from a
 # 64-expert case), so their traffic is null.
 NCU_TRAFFIC = {
@@ -146,7 +150,7 @@ NCU_TRAFFIC = {
     ("verify4", "down"): 557784576 + 6365952,
 }
 _GEMV_SOURCES = {
-    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "cc2ae90b1afe401cc3c9eda130e7a6b0e7ae3824",
+    "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "5584e0cb62598beb959c3f571892cc9a5342db4b",
     "trellis_quantized_moe_exl3_gb300/csrc/common.cuh": "91ce3402e4abd315dd1aaa25eaa71d9884431157",
     "trellis_quantized_moe_exl3_gb300/csrc/pipeline.cuh": "1f11aa433c95c15ed0fd2ec1605b876b5f7100cc",
 }

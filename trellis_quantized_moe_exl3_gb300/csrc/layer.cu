@@ -240,7 +240,6 @@ exl3_status exl3_moe_route(const float* logits, int T, int E, int top_k, int32_t
   RouteBuffers rb{};
   route_carve(ws, T, E, top_k, &rb);
   rb.ids = ids; rb.w = w; rb.seg_offsets = seg_offsets; rb.seg_pairs = seg_pairs;
-  if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
   if (launch_route(logits, T, E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
   return EXL3_OK;
 }
@@ -297,28 +296,31 @@ exl3_status forward_impl(const exl3_layer_t* layer, const void* x, exl3_dtype dt
   auto rec = [&](int i) {
     if (ev) record_stage_event(ev[i], st);
   };
-  rec(0);
-  if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
-  if (launch_route(logits, T, L.E - L.sc, top_k, rb, st, L.sc) != cudaSuccess)
-    return EXL3_ERR_CUDA;
-  // shared expert: forked onto the side stream once routing is done, so it
-  // overlaps the expert kernels (which take their work dynamically and do not
-  // mind SMs it occupies) instead of delaying the one-CTA routing kernel
+  // shared expert: on the side stream, joined before the combine.  With the
+  // GEMV path it is forked before routing: the GEMV launches are persistent
+  // grids that take the SMs as the kernel before them ends and keep them
+  // until their work list is empty, so a kernel forked after routing would
+  // mostly wait for them.  With the GEMM path it is forked once routing is
+  // done, so it does not delay the routing CTAs.
+  const bool gemm = use_gemm(L, T, kp, path);
   const float* sp = nullptr;
   int ns = 0;
-  if (run_shared) {
-    if (cudaEventRecord(layer->fork, st) != cudaSuccess ||
-        cudaStreamWaitEvent(layer->side, layer->fork, 0) != cudaSuccess)
-      return EXL3_ERR_CUDA;
-    if (launch_shared(L, x, bf16, T, base + f.shared, &sp, &ns, layer->side) != cudaSuccess)
-      return EXL3_ERR_CUDA;
-    if (cudaEventRecord(layer->join, layer->side) != cudaSuccess) return EXL3_ERR_CUDA;
-  }
+  auto fork_shared = [&]() -> bool {
+    return cudaEventRecord(layer->fork, st) == cudaSuccess &&
+           cudaStreamWaitEvent(layer->side, layer->fork, 0) == cudaSuccess &&
+           launch_shared(L, x, bf16, T, base + f.shared, &sp, &ns, layer->side) == cudaSuccess &&
+           cudaEventRecord(layer->join, layer->side) == cudaSuccess;
+  };
+  rec(0);
+  if (run_shared && !gemm && !fork_shared()) return EXL3_ERR_CUDA;
+  if (launch_route(logits, T, L.E - L.sc, top_k, rb, st, L.sc) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  if (run_shared && gemm && !fork_shared()) return EXL3_ERR_CUDA;
   rec(1);
 
   float* pair_rows = nullptr;
   int pair_splits = 1;
-  if (use_gemm(L, T, kp, path)) {
+  if (gemm) {
     if (launch_moe_gemm(L, x, bf16, T, kp, rb, base + f.gemv, ev, &pair_rows, sh, st) !=
         cudaSuccess)
       return EXL3_ERR_CUDA;

@@ -167,8 +167,12 @@ __global__ void __launch_bounds__(256) gather_xs_kernel(const void* __restrict__
                                                         const uint16_t* __restrict__ suh_u,
                                                         int had, int act8, Shard sh,
                                                         uint32_t* __restrict__ xs,
-                                                        float* __restrict__ xs_inv) {
+                                                        float* __restrict__ xs_inv,
+                                                        int32_t* __restrict__ zero_ctrs) {
   pdl_wait();
+  // the work counters of the GEMV launches that follow start at zero; null
+  // when a memset has already cleared them
+  if (zero_ctrs && blockIdx.x == 0 && threadIdx.x < 12) zero_ctrs[threadIdx.x] = 0;
   __shared__ float s_tmp[32];
   const int pos = blockIdx.x;
   const int p = rb.seg_pairs[pos];
@@ -765,8 +769,10 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   const int P = T * top_k;
   const size_t G = max_groups(T, L.E, top_k);
   cudaError_t err;
-  if ((err = cudaMemsetAsync(gb.counters, 0, 12 * sizeof(int32_t), st)) != cudaSuccess) return err;
+  // gather_xs_kernel clears the work counters, except with mixed widths,
+  // whose list kernel counts into the same words before it
   if (L.mixed) {
+    if ((err = cudaMemsetAsync(gb.counters, 0, 12 * sizeof(int32_t), st)) != cudaSuccess) return err;
     const int threads = (int)(3 * G);
     err = launch_pdl(width_lists_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st,
                      (const int32_t*)(rb.group_off + L.E), (const int32_t*)rb.groups, L.d_kt,
@@ -776,7 +782,7 @@ cudaError_t launch_moe_gemv(const LayerView& L, const void* x, int x_bf16, int T
   }
   err = launch_pdl(gather_xs_kernel, dim3(P), dim3(input_pass_threads(L.H)), 0, st, x,
                    x_bf16, L.H, top_k, rb, L.suh[0], L.suh[1], L.had, L.act8, sh, gb.xs_gu,
-                   gb.xs_gu_inv);
+                   gb.xs_gu_inv, L.mixed ? (int32_t*)nullptr : gb.counters);
   note_launches(1);
   if (err != cudaSuccess) return err;
   rec(2);

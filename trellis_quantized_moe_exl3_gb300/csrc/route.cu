@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
                                                            int E, int k, int sh, RouteBuffers rb,
                                                            int fused) {
   pdl_wait();
+  // routing is the first kernel of a call: it clears the device status word
+  // (no kernel that may set a bit runs before it or beside it)
+  if (blockIdx.x == 0 && threadIdx.x == 0) *rb.status = 0;
   __shared__ int s_ids[kRouteChunk * (kMaxTopK + 1)];
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_warp[32];
@@ -279,6 +282,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 
 __global__ void route_empty_kernel(int E, RouteBuffers rb) {
   pdl_wait();
+  if (threadIdx.x == 0) *rb.status = 0;  // (as route_chunk_kernel)
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     rb.seg_offsets[e] = 0;
     rb.group_off[e] = 0;

@@ -61,9 +61,8 @@ extern "C" exl3_status exl3_moe_route_static(const float* logits, int T, int E, 
   RouteBuffers rb{};
   route_carve(scratch, T, E, top_k, &rb);
   rb.ids = ids; rb.w = w; rb.seg_offsets = seg_offsets; rb.seg_pairs = seg_pairs;
-  // The array keeps the previous call's contents; only the status word must
-  // start at zero, every other scratch word is written before it is read.
-  if (cudaMemsetAsync(rb.status, 0, sizeof(int32_t), st) != cudaSuccess) return EXL3_ERR_CUDA;
+  // The array keeps the previous call's contents; the routing kernel clears
+  // the status word, and every other scratch word is written before it is read.
   if (launch_route(logits, T, E, top_k, rb, st) != cudaSuccess) return EXL3_ERR_CUDA;
   return EXL3_OK;
 }
