@@ -24,61 +24,71 @@ namespace exl3 {
 
 namespace {
 
-// One warp selects the top-k of one token.  MAXPL = logits held per lane.
+// Order-preserving unsigned key of a logit: a larger logit has a larger key,
+// NaN counts as -inf and -0 as +0 (they compare equal as floats), and every
+// key is above 0, which stands for "no candidate".
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  if (isnan(f)) f = -INFINITY;
+  if (f == 0.0f) f = 0.0f;
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One warp selects the top-k of one token.  MAXPL = logits held per lane
+// (lane l holds experts l, l + 32, ...).  Round j: each lane offers its best
+// expert not yet taken (its lowest index among equal keys), one warp max over
+// the keys and one warp min over the indices offering that key pick expert j.
 template <int MAXPL>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ lrow, int E, int k,
                                           int* my_id, float* my_w) {
   const int lane = threadIdx.x & 31;
-  float v[MAXPL];
-  uint32_t taken = 0;
+  uint32_t key[MAXPL];
 #pragma unroll
   for (int i = 0; i < MAXPL; i++) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      const float f = lrow[e];
-      v[i] = isnan(f) ? -INFINITY : f;
-    } else {
-      v[i] = -INFINITY;
-      taken |= 1u << i;
-    }
+    key[i] = e < E ? logit_key(lrow[e]) : 0u;  // 0: never offered
   }
-  float lmax = 0.0f, mine_l = 0.0f;
+  uint32_t kmax = 0, mine_k = 0;
   int mine_e = 0;
   for (int j = 0; j < k; j++) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
-    for (int i = 0; i < MAXPL; i++) {
-      const int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
+    for (int i = 0; i < MAXPL; i++)
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = i;
       }
-    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int be = __reduce_min_sync(0xffffffffu, bk == m ? lane + 32 * bi : 0x7fffffff);
+    if ((be & 31) == lane) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
+      for (int i = 0; i < MAXPL; i++)
+        if (i == (be >> 5)) key[i] = 0u;  // taken
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
       mine_e = be;
-      mine_l = bv;
+      mine_k = m;
     }
-    if (j == 0) lmax = bv;
+    if (j == 0) kmax = m;
   }
   // softmax over the k selected, in j order
+  const float lmax = key_logit(kmax), mine_l = key_logit(mine_k);
   float ex = 0.0f;
   if (lane < k) {
     const float d = (mine_l == lmax) ? 0.0f : __fsub_rn(mine_l, lmax);
     ex = exp_route(d);
   }
+  float exs[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; j++) exs[j] = __shfl_sync(0xffffffffu, ex, j);
   float sum = 0.0f;
-  for (int j = 0; j < k; j++) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; j++)
+    if (j < k) sum = __fadd_rn(sum, exs[j]);
   *my_id = mine_e;
   *my_w = (lane < k) ? __fdiv_rn(ex, sum) : 0.0f;
 }
@@ -138,8 +148,10 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
   // routing is the first kernel of a call: it clears the device status word
   // (no kernel that may set a bit runs before it or beside it)
   if (blockIdx.x == 0 && threadIdx.x == 0) *rb.status = 0;
+  static_assert(kRouteChunk <= 64, "one bit per token of a chunk");
   __shared__ int s_ids[kRouteChunk * (kMaxTopK + 1)];
   __shared__ int s_cnt[kMaxExperts];
+  __shared__ unsigned long long s_tok[kMaxExperts];  // bit tl: token tl has the expert
   __shared__ int s_warp[32];
   const int chunk = blockIdx.x;
   const int t0 = chunk * kRouteChunk;
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int kp = k + sh, Et = E + sh;  // pairs per token, experts in the tables
 
-  for (int e = threadIdx.x; e < Et; e += blockDim.x) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) s_tok[e] = 0ull;
   for (int tl = wid; tl < nt; tl += nw) {
     const int t = t0 + tl;
     int id;
@@ -164,25 +176,24 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
     }
   }
   __syncthreads();
-  // stable local ranks: one warp walks the tokens in order; the k experts of a
-  // token are distinct, so lane j can bump its counter without conflicts
-  if (wid == 0) {
-    for (int tl = 0; tl < nt; tl++) {
-      if (lane < kp) {
-        const int e = s_ids[tl * kp + lane];
-        const int r = s_cnt[e];
-        s_cnt[e] = r + 1;
-        rb.rank[(size_t)(t0 + tl) * kp + lane] = r;
-      }
-      __syncwarp();
-    }
-  }
+  // stable local ranks: the rank of pair (tl, j) is the number of earlier
+  // tokens of the chunk routed to the same expert (the k experts of a token
+  // are distinct), read off the expert's token mask
+  const int np = nt * kp;
+  for (int pl = threadIdx.x; pl < np; pl += blockDim.x)
+    atomicOr(&s_tok[s_ids[pl]], 1ull << (pl / kp));
   __syncthreads();
+  auto rank_of = [&](int pl) {
+    return __popcll(s_tok[s_ids[pl]] & ((1ull << (pl / kp)) - 1ull));
+  };
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) s_cnt[e] = __popcll(s_tok[e]);
   if (!fused) {
+    for (int pl = threadIdx.x; pl < np; pl += blockDim.x) rb.rank[(size_t)t0 * kp + pl] = rank_of(pl);
     for (int e = threadIdx.x; e < Et; e += blockDim.x)
       rb.chunk_counts[(size_t)chunk * Et + e] = s_cnt[e];
     return;
   }
+  __syncthreads();
   // fused: offsets = exclusive scan of the counts, active list, scatter
   int total = 0, n_act = 0, n_grp = 0;
   const int cnt = threadIdx.x < Et ? s_cnt[threadIdx.x] : 0;
@@ -203,10 +214,10 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const float* __restri
   __syncthreads();
   if (threadIdx.x < Et) s_cnt[threadIdx.x] = off;  // segment starts
   __syncthreads();
-  for (int pl = threadIdx.x; pl < nt * kp; pl += blockDim.x) {
+  for (int pl = threadIdx.x; pl < np; pl += blockDim.x) {
     const size_t p = (size_t)t0 * kp + pl;
     const int e = s_ids[pl];
-    const int pos = s_cnt[e] + rb.rank[p];
+    const int pos = s_cnt[e] + rank_of(pl);
     rb.seg_pairs[pos] = (int)p;
     rb.pair_pos[p] = pos;
   }
@@ -293,11 +304,12 @@ __global__ void route_empty_kernel(int E, RouteBuffers rb) {
 template <int MAXPL>
 cudaError_t launch_chunks(const float* logits, int T, int E, int k, int sh, const RouteBuffers& rb,
                           int nchunks, cudaStream_t st) {
-  // one chunk: the scans need a thread per expert, the top-k a warp per token
-  // (in turns); fewer warps make the CTA's barriers cheaper
-  int threads = 512;
+  // a warp per token for the top-k (in turns past 32 tokens); one chunk also
+  // needs a thread per expert for its scans, and no more warps than either
+  // (fewer warps make the CTA's barriers cheaper)
+  int threads = 1024;
   if (nchunks == 1) {
-    const int need_e = (E + sh + 31) / 32 * 32, need_t = 32 * (T < 16 ? T : 16);
+    const int need_e = (E + sh + 31) / 32 * 32, need_t = 32 * (T < 32 ? T : 32);
     threads = need_e > need_t ? need_e : need_t;
   }
   const cudaError_t err = launch_pdl(route_chunk_kernel<MAXPL>, dim3(nchunks), dim3(threads), 0, st,
