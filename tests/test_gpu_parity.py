@@ -97,7 +97,13 @@ def _route_cases():
     odd[4, :] = -np.inf
     odd[5, :] = np.nan
     odd[6, :3] = np.inf
+    odd[7, :] = 0.0
+    odd[7, ::3] = -0.0                                          # +0 and -0 compare equal
+    odd[8, :] = -1.0
+    odd[8, 3], odd[8, 10] = 0.0, -0.0
     cases.append(("odd", odd, 5))
+    zeros = rng.choice(np.array([0.0, -0.0, 1.0, -1.0], np.float32), (20, 288))
+    cases.append(("signed_zeros", zeros, 8))                     # one chunk, many ties
     cases.append(("k1", rng.standard_normal((129, 288)).astype(np.float32), 1))
     cases.append(("k16", rng.standard_normal((77, 64)).astype(np.float32), 16))
     cases.append(("T1", rng.standard_normal((1, 288)).astype(np.float32), 8))
