@@ -134,20 +134,16 @@ def expert_work(spec, counts, per: int):
 # dominant stage's launch in one decode or verify step, from ncu captures of
 # this bench's decode and verify workloads (the GEMV gate/up and down
 # launches); reported only while the kernel sources hash to what was
-# captured (otherwise null).  The moe_gemv.cu digest is that of a later
-# revision than the capture: its diff to the captured one touches only
-# gather_xs_kernel (which now clears the launches' work counters) and the
-# memset that did so before; the GEMV kernel, its launch shape and its
-# arguments are the captured ones.
+# captured (otherwise null).
 # The prefill stages have no full-size capture (their counters come from a
 # 64-expert case), so their traffic is null.
 NCU_TRAFFIC = {
-    ("decode", "gate_up"): 128089856 + 3795968,
-    ("decode", "down"): 63690752 + 617728,
-    ("verify3", "gate_up"): 825634816 + 9473536,
-    ("verify3", "down"): 410341632 + 5521920,
-    ("verify4", "gate_up"): 1121843712 + 9858304,
-    ("verify4", "down"): 557784576 + 6365952,
+    ("decode", "gate_up"): 128107264 + 3334656,
+    ("decode", "down"): 63692800 + 86016,
+    ("verify3", "gate_up"): 828007680 + 9542656,
+    ("verify3", "down"): 410294784 + 5534208,
+    ("verify4", "gate_up"): 1121739520 + 9833472,
+    ("verify4", "down"): 557677824 + 5964800,
 }
 _GEMV_SOURCES = {
     "trellis_quantized_moe_exl3_gb300/csrc/moe_gemv.cu": "5584e0cb62598beb959c3f571892cc9a5342db4b",
